@@ -1,0 +1,400 @@
+"""Pins for the oracle: values printed on the pages, hand-worked examples, closed
+forms, invariants and brute force.  CPU only."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+
+
+def _lines(path):
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+# ---------------------------------------------------------------- formulas
+
+def test_kv_bytes_examples(golden_dir):
+    n = 0
+    for line in _lines(os.path.join(golden_dir, "kv_bytes_examples.txt")):
+        f = line.split()
+        L, H, d, S, b, expect = (int(x) for x in f[:6])
+        assert O.kv_cache_bytes(L, H, d, S, b) == expect
+        n += 1
+    assert n == 6
+
+
+def test_kv_bytes_page_roundings():
+    # "~10.7 GB", "~43 GB", "~8.59 GB" (decimal GB), "> 50 GB"
+    assert round(O.kv_cache_bytes(80, 8, 128, 32768, 2) / 1e9, 1) == 10.7
+    assert round(O.kv_cache_bytes(80, 8, 128, 131072, 2) / 1e9) == 43
+    assert round(O.kv_cache_bytes(64, 4, 128, 65536, 2) / 1e9, 2) == 8.59
+    assert O.kv_cache_bytes(80, 64, 128, 20000, 2) > 50e9
+    # exercise 1's "2-bit ~2.15 GB (4x saving)" is the FP16 figure divided by 4,
+    # as printed; the pure 2-bit code payload is FP16/8.
+    fp16 = O.kv_cache_bytes(64, 4, 128, 65536, 2)
+    assert round(fp16 / 4 / 1e9, 2) == 2.15
+    assert O.kv_cache_bytes(64, 4, 128, 65536, 2 / 8) == fp16 / 8
+
+
+def test_equivalent_bits(golden_dir):
+    for line in _lines(os.path.join(golden_dir, "equivalent_bits.txt")):
+        pairs_s, expect = line.split()
+        pairs = [tuple(int(t) for t in p.split(":")) for p in pairs_s.split(",")]
+        assert O.equivalent_bits(pairs) == pytest.approx(float(expect), abs=1e-12)
+    # KVmix averages: keys 70/32 ~ 2.19, values 76/32 ~ 2.38
+    k_avg = (6 * 3 + 26 * 2) / 32
+    v_avg = (6 * 4 + 26 * 2) / 32
+    assert round(k_avg, 2) == 2.19 and round(v_avg, 2) == 2.38
+    # search-space sizes quoted by KVTuner section A2: 9^32 ~ 3.4e30, 5^6 = 15625
+    assert f"{9 ** 32:.1e}" == "3.4e+30"
+    assert 5 ** 6 == 15625
+
+
+def test_equivalent_bits_workloads():
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    eq = [O.equivalent_bits([(kb, vb) for kb, vb, _ in W.workload(i).layers]) for i in range(1, 6)]
+    assert eq[0] == 3.0
+    assert eq[1] == 111 / 32 and round(eq[1], 2) == 3.47
+    assert eq[2] == 4.0
+    assert eq[3] == 2.28125
+    assert eq[4] == 3.1875
+    w3 = W.workload(3)
+    assert w3.layers[0][:2] == (8, 8) and w3.layers[-1][:2] == (8, 8)
+    assert set(p[:2] for p in w3.layers) <= {(8, 8), (8, 4), (4, 4), (4, 2)}
+    w4 = W.workload(4)
+    hi = [l for l, p in enumerate(w4.layers) if p[:2] == (4, 3)]
+    assert len(hi) == 6
+    assert all(p[2] == 800 for p in w4.layers if p[:2] == (4, 3))
+    assert all(p[2] == 384 for p in w4.layers if p[:2] == (2, 2))
+
+
+# ---------------------------------------------------------------- quantizer
+
+def _parse_q(line):
+    bits, xs, codes, s, z = (p.strip() for p in line.split("|"))
+    return (int(bits), np.array([float(t) for t in xs.split()], dtype=np.float16),
+            np.array([int(t) for t in codes.split()]), float(s), float(z))
+
+
+def test_quantizer_worked_examples(golden_dir):
+    n = 0
+    for line in _lines(os.path.join(golden_dir, "quantizer_worked.txt")):
+        bits, x, codes, s, z = _parse_q(line)
+        c, s16, z16 = O.quantize_values_tokens(x[None, :], bits)
+        assert list(c[0]) == list(codes), line
+        assert float(s16[0]) == s and float(z16[0]) == z
+        # same numbers through the per-channel key path (a column)
+        ck, sk, zk = O.quantize_keys_group(x[:, None], bits)
+        assert list(ck[:, 0]) == list(codes)
+        assert float(sk[0]) == s and float(zk[0]) == z
+        n += 1
+    assert n == 5
+
+
+def test_key_group_worked(golden_dir):
+    lines = list(_lines(os.path.join(golden_dir, "key_group_worked.txt")))
+    bits = int(lines[0].split()[1])
+    i_tok = lines.index("tokens")
+    i_cod = lines.index("codes")
+    toks = np.array([[float(t) for t in l.split()] for l in lines[i_tok + 1:i_cod]], dtype=np.float16)
+    codes = np.array([[int(t) for t in l.split()] for l in lines[i_cod + 1:i_cod + 1 + toks.shape[0]]])
+    scale = [float(t) for t in lines[-2].split()[1:]]
+    zero = [float(t) for t in lines[-1].split()[1:]]
+    c, s, z = O.quantize_keys_group(toks, bits)
+    assert (c == codes).all()
+    assert [float(v) for v in s] == scale
+    assert [float(v) for v in z] == zero
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_quantizer_error_bound_and_endpoints(bits):
+    rng = np.random.default_rng(7 + bits)
+    x = (rng.standard_normal((64, 128)) * rng.lognormal(0, 1, (64, 1)) + rng.normal(0, 3, (64, 1)))
+    x = x.astype(np.float16)
+    codes, s16, z16 = O.quantize_values_tokens(x, bits)
+    xh = O.dequant_values(codes, s16, z16, bits)
+    s = s16.astype(np.float64)[:, None] * np.ones((1, 128))
+    qmax = np.full((1, 128), 2 ** bits - 1, dtype=np.float64)
+    if bits == 3:
+        two = O.is_slot10(128)[None, :]
+        s = np.where(two, O.slot10_scale(s16).astype(np.float64)[:, None], s)
+        qmax = np.where(two, 3.0, 7.0)
+    err = np.abs(x.astype(np.float64) - xh)
+    bound = s / 2 + 4 * 2.0 ** -24 * (np.abs(z16.astype(np.float64))[:, None] + qmax * s)
+    assert (err <= bound).all()
+    # min -> code 0, max -> code qmax
+    mn_idx = x.astype(np.float64).argmin(axis=1)
+    mx_idx = x.astype(np.float64).argmax(axis=1)
+    rows = np.arange(64)
+    assert (codes[rows, mn_idx] == 0).all()
+    top = np.where(O.is_slot10(128)[mx_idx], 3, 2 ** bits - 1) if bits == 3 else 2 ** bits - 1
+    assert (codes[rows, mx_idx] == top).all()
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_quantizer_power_of_two_grid_exact(bits):
+    # x = mn + k * delta with delta a power of two and the full range used:
+    # s = delta exactly, codes = k, reconstruction exact.
+    rng = np.random.default_rng(bits)
+    delta = 2.0 ** -3
+    mn = -1.25
+    k = rng.integers(0, 2 ** bits, size=200)
+    k[0], k[1] = 0, 2 ** bits - 1
+    x = (mn + k * delta).astype(np.float16)
+    c, s, z = O.quantize_keys_group(x[:, None], bits)
+    assert float(s[0]) == delta and float(z[0]) == mn
+    assert (c[:, 0] == k).all()
+    assert (O.dequant_keys(c, s, z, bits)[:, 0] == x.astype(np.float64)).all()
+
+
+def test_quantizer_constant_group_exact():
+    x = np.full((32, 128), 1.5, dtype=np.float16)
+    for bits in (2, 3, 4, 8):
+        c, s, z = O.quantize_keys_group(x, bits)
+        assert (c == 0).all() and (s == 0).all()
+        assert (O.dequant_keys(c, s, z, bits) == 1.5).all()
+
+
+def test_ties_half_to_even():
+    # b = 2, min 0, max 3 -> s = 1; x = 0.5, 1.5, 2.5 -> 0, 2, 2
+    x = np.array([0, 3, 0.5, 1.5, 2.5], dtype=np.float16)
+    c, s, _ = O.quantize_values_tokens(x[None, :], 2)
+    assert float(s[0]) == 1.0
+    assert list(c[0, 2:]) == [0, 2, 2]
+
+
+def test_three_bit_slot10_scale():
+    # the 2-bit field of a 3-bit word uses s2 = (s*7)/3 over the same range:
+    # with min 0 and max 7 (s = 1), s2 = 7/3 and codes of 0, 7/3, 14/3, 7 are 0..3
+    d = 11
+    v = np.zeros((1, d), dtype=np.float16)
+    v[0, 0] = 7
+    for val, code in ((0.0, 0), (2.33, 1), (4.66, 2), (7.0, 3), (1.2, 1), (1.1, 0)):
+        v[0, 10] = val
+        c, s, z = O.quantize_values_tokens(v, 3)
+        assert float(s[0]) == 1.0
+        assert c[0, 10] == code, (val, c[0, 10])
+
+
+# ---------------------------------------------------------------- packing
+
+def test_packing_worked(golden_dir):
+    n = 0
+    for line in _lines(os.path.join(golden_dir, "packing_worked.txt")):
+        bits, codes, words = (p.strip() for p in line.split("|"))
+        bits = int(bits)
+        codes = np.array([[int(t) for t in codes.split()]], dtype=np.uint8)
+        expect = [int(t, 16) for t in words.split()]
+        got = O.pack_rows(codes, bits)
+        assert [int(w) for w in got[0]] == expect, line
+        assert (O.unpack_rows(got, bits, codes.shape[1]) == codes).all()
+        n += 1
+    assert n == 5
+
+
+@pytest.mark.parametrize("bits,d", [(2, 64), (2, 128), (3, 64), (3, 128), (4, 64), (4, 128), (8, 64), (8, 128)])
+def test_pack_roundtrip_random(bits, d):
+    rng = np.random.default_rng(bits * 1000 + d)
+    codes = rng.integers(0, 2 ** bits, size=(50, d)).astype(np.uint8)
+    if bits == 3:
+        codes[:, O.is_slot10(d)] &= 3
+    w = O.pack_rows(codes, bits)
+    assert w.shape == (50, O.words_per_row(d, bits))
+    assert (O.unpack_rows(w, bits, d) == codes).all()
+    # independent bit-level check: rebuild each word from a Python int
+    for r in range(3):
+        for wi in range(w.shape[1]):
+            acc = 0
+            if bits == 3:
+                for j in range(11):
+                    c = wi * 11 + j
+                    if c < d:
+                        acc |= int(codes[r, c]) << (30 if j == 10 else 3 * j)
+            else:
+                per = 32 // bits
+                for j in range(per):
+                    acc |= int(codes[r, wi * per + j]) << (bits * j)
+            assert acc == int(w[r, wi])
+
+
+def test_three_bit_density():
+    # 11 codes per word: 12 words per 128-vector, against 13 for 10 per word;
+    # channels 10, 21, ..., 120 sit in the 2-bit fields
+    assert O.words_per_row(128, 3) == 12
+    assert math.ceil(128 / 10) == 13
+    assert list(np.nonzero(O.is_slot10(128))[0]) == list(range(10, 128, 11))
+
+
+# ---------------------------------------------------------------- attention
+
+def test_attention_closed_form():
+    # d = 2; scores q.k/sqrt(2): 0 and ln 3 -> weights 1/4, 3/4
+    q = np.array([1.0, 0.0])
+    k = np.array([[0.0, 0.0], [math.log(3) * math.sqrt(2), 5.0]])
+    v = np.array([[4.0, 0.0], [0.0, 8.0]])
+    o = O.attention_fp64(q, k, v)
+    assert np.allclose(o, [1.0, 6.0], atol=1e-14)
+
+
+def test_attention_brute_force_tiny():
+    rng = np.random.default_rng(3)
+    for T in range(1, 9):
+        d = 4
+        q = rng.standard_normal(d)
+        k = rng.standard_normal((T, d))
+        v = rng.standard_normal((T, d))
+        # hand-expanded: weights exp(s_t) / sum exp(s_j), no max subtraction
+        s = [sum(q[c] * k[t, c] for c in range(d)) / 2.0 for t in range(T)]
+        e = [math.exp(x) for x in s]
+        tot = sum(e)
+        expect = [sum(e[t] / tot * v[t, c] for t in range(T)) for c in range(d)]
+        assert np.allclose(O.attention_fp64(q, k, v), expect, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(4)
+    d = 16
+    q = rng.standard_normal(d)
+    v = rng.standard_normal((5, d))
+    k = np.tile(rng.standard_normal(d), (5, 1))
+    assert np.allclose(O.attention_fp64(q, k, v), v.mean(axis=0))
+    assert np.allclose(O.attention_fp64(q, k[:1], v[:1]), v[0])
+
+
+def test_gqa_head_mapping():
+    # query head h reads kv head h // (Hq/Hkv): with constant keys the output
+    # of every query head is the mean of its kv head's values
+    Hq, Hkv, T, d = 8, 2, 6, 4
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((Hq, d))
+    k = np.zeros((Hkv, T, d))
+    v = rng.standard_normal((Hkv, T, d))
+    out = O.gqa_attention_fp64(q, k, v)
+    for h in range(Hq):
+        assert np.allclose(out[h], v[h // 4].mean(axis=0))
+
+
+def test_lemma1_dominant_key():
+    # KVTuner appendix Lemma 1: with one dominant key, quantization does not
+    # move the attention output: both outputs ~ v_i
+    rng = np.random.default_rng(6)
+    d, T = 128, 64
+    q = rng.standard_normal(d).astype(np.float16).astype(np.float64)
+    k = rng.standard_normal((T, d)) * 0.1
+    i = 17
+    k[i] = q / np.linalg.norm(q) * 60 * math.sqrt(d) / np.linalg.norm(q)
+    k16 = k.astype(np.float16)
+    v16 = rng.standard_normal((T, d)).astype(np.float16)
+    sc = (k16.astype(np.float64) @ q) / math.sqrt(d)
+    assert sc[i] - np.delete(sc, i).max() >= 30
+    codes, s, z = O.quantize_keys_group(k16, 2)
+    kh = O.dequant_keys(codes, s, z, 2)
+    vc, vs, vz = O.quantize_values_tokens(v16, 2)
+    vh = O.dequant_values(vc, vs, vz, 2)
+    o_exact = O.attention_fp64(q, k16, vh)
+    o_quant = O.attention_fp64(q, kh, vh)
+    assert np.allclose(o_exact, vh[i], atol=1e-9)
+    assert np.allclose(o_quant, vh[i], atol=1e-9)
+
+
+# ---------------------------------------------------------------- error orderings
+
+def test_drift_exercise_per_token_beats_per_channel():
+    # KIVI notes exercise 4: V drifts (first half N(0,1), second half N(10,1));
+    # per-channel 2-bit scales taken from the first half (clamped) against
+    # per-token scales
+    rng = np.random.default_rng(11)
+    T, d, b = 1024, 128, 2
+    v = np.concatenate([rng.standard_normal((T // 2, d)), rng.standard_normal((T // 2, d)) + 10])
+    v = v.astype(np.float16)
+    first = v[: T // 2]
+    mn = first.min(axis=0)
+    s = O.asym_scale(mn, first.max(axis=0), b)
+    pc_codes = O.asym_codes(v, mn[None, :], s.astype(np.float32)[None, :], 2 ** b - 1)
+    pc = pc_codes * s.astype(np.float64)[None, :] + mn.astype(np.float64)[None, :]
+    tc, ts, tz = O.quantize_values_tokens(v, b)
+    pt = O.dequant_values(tc, ts, tz, b)
+    err_pc = np.abs(v.astype(np.float64) - pc).sum()
+    err_pt = np.abs(v.astype(np.float64) - pt).sum()
+    # expected: the stale grid clamps the second half near the first half's
+    # per-channel max (~3), ~7 per element on half the tokens; per token the
+    # 2-bit grid over N(.,1) (range ~5, s ~1.7) errs ~s/4 per element:
+    # ratio ~ (0.5*7 + 0.5*0.5) / 0.43 ~ 8.7
+    assert 6 < err_pc / err_pt < 12
+    assert err_pt / v.size < 0.5
+
+
+def test_table9_ordering_keys_per_channel_beat_per_token():
+    # KVTuner appendix (Table 9): at 2 bits, per-channel key error e_k is lower
+    # than per-token e_k when keys carry channel outliers
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    w = W.scaled(W.workload(2), batch=1, num_layers=1)
+    k, _ = W.gen_kv(w, 0, 0, 256)
+    k = k[0, 0].numpy()
+    ek_pc = []
+    for g in range(0, 256, 32):
+        c, s, z = O.quantize_keys_group(k[g:g + 32], 2)
+        ek_pc.append(O.dequant_keys(c, s, z, 2))
+    kh_pc = np.concatenate(ek_pc)
+    kh_pt = O.quantize_keys_per_token(k, 2)
+    assert O.rel_error(k, kh_pc) < O.rel_error(k, kh_pt)
+
+
+# ---------------------------------------------------------------- streaming state
+
+def test_flush_state_examples():
+    # R = G: a 4096-token prefill leaves every token quantized
+    assert O.flush_state(4096, 32, 32) == (4096, 0)
+    assert O.flush_state(4096 + 31, 32, 32) == (4096, 31)
+    assert O.flush_state(4096 + 32, 32, 32) == (4128, 0)
+    # per-layer windows of 800 and 384 tokens (G = 32)
+    assert O.flush_state(4096, 800, 32) == (3328, 768)
+    assert O.flush_state(4096, 384, 32) == (3744, 352)
+    assert O.flush_state(0, 64, 64) == (0, 0)
+
+
+def test_oracle_cache_streaming_matches_bulk():
+    # appending in pieces or in one call gives the same records and ring
+    rng = np.random.default_rng(12)
+    B, H, d, G, R = 1, 2, 64, 32, 96
+    k = rng.standard_normal((B, H, 300, d)).astype(np.float16)
+    v = rng.standard_normal((B, H, 300, d)).astype(np.float16)
+    a = O.OracleLayerCache(B, H, d, G, 4, 2, R)
+    a.append(k, v)
+    b = O.OracleLayerCache(B, H, d, G, 4, 2, R)
+    pos = 0
+    for n in (1, 7, 50, 33, 1, 1, 100, 107):
+        b.append(k[:, :, pos:pos + n], v[:, :, pos:pos + n])
+        pos += n
+    assert pos == 300
+    assert (a.n_q, a.r) == (b.n_q, b.r) == O.flush_state(300, R, G)
+    for u in range(B * H):
+        assert a.unit_records(u) == b.unit_records(u)
+        ka, va = a.residual_ring(u)
+        kb_, vb_ = b.residual_ring(u)
+        assert (ka == kb_).all() and (va == vb_).all()
+    # dequantized tokens: quantized groups are close, the residual is exact
+    kh, vh = a.dequantized(0)
+    assert kh.shape == (300, d)
+    assert (kh[a.n_q:] == k[0, 0, a.n_q:].astype(np.float64)).all()
+    assert np.abs(kh[: a.n_q] - k[0, 0, : a.n_q]).max() < 1.0
+
+
+def test_record_layout_sizes():
+    lay = O.record_layout(128, 32, 4, 2)
+    assert lay["wk"] == 16 and lay["wv"] == 8
+    assert lay["bytes"] == 32 * 64 + 32 * 32 + 4 * 128 + 4 * 32
+    lay3 = O.record_layout(128, 32, 4, 3)
+    assert lay3["wv"] == 12
+    for d in (64, 128):
+        for G in (32, 64, 128):
+            for kb in O.BITS_ALLOWED:
+                for vb in O.BITS_ALLOWED:
+                    assert O.record_layout(d, G, kb, vb)["bytes"] % 16 == 0
