@@ -47,7 +47,7 @@ Layout of the quantized cache (mirrored by the CUDA path):
 * per (batch, kv head) the cache is a sequence of group records, one per key
   group of G tokens:
   ``[K codes G x WK u32][V codes G x WV u32][K scale d f16][K zero d f16]
-  [V scale G f16][V zero G f16]``;
+  [V (scale, zero) G pairs of f16]`` (each token's value scale and zero adjacent);
 * the residual window is a ring of R_l slots; token i (absolute position) sits
   in slot i mod R_l; K rows then V rows, d fp16 each.
 """
@@ -297,9 +297,8 @@ def record_layout(d: int, group: int, k_bits: int, v_bits: int) -> Dict[str, int
     off["v_codes"] = off["k_codes"] + 4 * group * wk
     off["k_scale"] = off["v_codes"] + 4 * group * wv
     off["k_zero"] = off["k_scale"] + 2 * d
-    off["v_scale"] = off["k_zero"] + 2 * d
-    off["v_zero"] = off["v_scale"] + 2 * group
-    off["bytes"] = off["v_zero"] + 2 * group
+    off["v_scale"] = off["k_zero"] + 2 * d     # (scale, zero) pairs, one per token
+    off["bytes"] = off["v_scale"] + 4 * group
     off["wk"] = wk
     off["wv"] = wv
     return off
@@ -309,9 +308,9 @@ def build_group_record(k_grp: np.ndarray, v_grp: np.ndarray, k_bits: int, v_bits
     """Quantize one key group (k_grp, v_grp: [G, d] fp16) and lay out its record."""
     kc, ks, kz = quantize_keys_group(k_grp, k_bits)
     vc, vs, vz = quantize_values_tokens(v_grp, v_bits)
+    vsz = np.stack([vs.astype(F16), vz.astype(F16)], axis=1)  # [G, 2]
     parts = [pack_rows(kc, k_bits).tobytes(), pack_rows(vc, v_bits).tobytes(),
-             ks.astype(F16).tobytes(), kz.astype(F16).tobytes(),
-             vs.astype(F16).tobytes(), vz.astype(F16).tobytes()]
+             ks.astype(F16).tobytes(), kz.astype(F16).tobytes(), vsz.tobytes()]
     return b"".join(parts)
 
 
@@ -323,8 +322,8 @@ def parse_group_record(rec: bytes, d: int, group: int, k_bits: int, v_bits: int)
     vw = buf[lay["v_codes"]:lay["k_scale"]].view(np.uint32).reshape(group, lay["wv"])
     ks = buf[lay["k_scale"]:lay["k_zero"]].view(F16)
     kz = buf[lay["k_zero"]:lay["v_scale"]].view(F16)
-    vs = buf[lay["v_scale"]:lay["v_zero"]].view(F16)
-    vz = buf[lay["v_zero"]:lay["bytes"]].view(F16)
+    vsz = buf[lay["v_scale"]:lay["bytes"]].view(F16).reshape(group, 2)
+    vs, vz = vsz[:, 0], vsz[:, 1]
     k_hat = dequant_keys(unpack_rows(kw, k_bits, d), ks, kz, k_bits)
     v_hat = dequant_values(unpack_rows(vw, v_bits, d), vs, vz, v_bits)
     return k_hat, v_hat
