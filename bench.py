@@ -1,0 +1,484 @@
+"""Benchmark: mixed-precision KV decode attention on one GB300 (or N replicas).
+
+A step is one decode step of the whole hot path over every layer of the
+workload: append the new token (FP16 window; a group flush with quantize +
+pack every G steps) and run decode attention over the quantized cache plus
+the window.  The default workload is the Llama-3.1-8B-shaped decode: 32
+layers, 32 q / 8 kv heads, head_dim 128, batch 16, context 4096, G = R = 32,
+K8V4 on layers 0-1 and 29-31 and K4V2 elsewhere.
+
+Reported:
+  value       decode tokens/s (batch x ranks / step time), device-timed with
+              CUDA events around K replays of the step's CUDA graph
+  e2e         the same metric through KVQCache.decode_step with every step's
+              inputs copied from pinned host memory and its outputs read back
+  roofline    decode-attention kernel: algorithmic bytes per launch / average
+              launch duration (a second timed pass replaying a decode-only
+              graph of all layers) against the measured HBM copy bandwidth
+  cpu_baseline  the oracle timed on the host cores on a bounded sample
+
+--impl reference times the oracle (the plain CPU statement of the method) on
+the same workload, one bounded sample per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "mixed-precision KV decode-attn tokens/s; cache-read GB/s as % of HBM peak"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while it runs."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.samples = []
+        self.windows = []
+        self._proc = None
+        self._thr = None
+        self.gpu_index = gpu_index
+        self.interval_ms = interval_ms
+
+    def start(self):
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.interval_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self._proc = None
+            return
+        self._thr = threading.Thread(target=self._read, daemon=True)
+        self._thr.start()
+
+    def _read(self):
+        for line in self._proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self._proc is None:
+            return None
+        self._proc.terminate()
+        try:
+            self._proc.wait(timeout=5)
+        except Exception:
+            self._proc.kill()
+        if self._thr:
+            self._thr.join(timeout=2)
+        inside = [s for t, s in self.samples if any(a - 0.05 <= t <= b + 0.05 for a, b in self.windows)]
+        use = inside or [s for _, s in self.samples]
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for s in use:
+            f = [x.strip() for x in s.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "in_timed_region": bool(inside)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (bounded sample)
+# ----------------------------------------------------------------------------
+
+class OracleSampler:
+    """Times the oracle's decode step (append one token, then fp64 attention
+    over the dequantized cache) for one (batch, kv head) unit of each distinct
+    precision pair, at full context, and extrapolates to the whole step
+    (all units of all layers).  The oracle runs as it stands, single-threaded
+    numpy."""
+
+    def __init__(self, w):
+        from mixed_precision_quantized_quant_gb300 import workloads as W
+        from oracle import kvq_oracle as O
+        self.W, self.w = W, w
+        seen, self.layers = set(), []
+        for l, p in enumerate(w.layers):
+            if p not in seen:
+                seen.add(p)
+                self.layers.append(l)
+        self.unit_w = W.scaled(w, batch=1, num_kv_heads=1, num_q_heads=w.num_q_heads // w.num_kv_heads)
+        self.caches = {}
+        for l in self.layers:
+            kb, vb, R = w.layers[l]
+            ora = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R)
+            k, v = W.gen_kv(self.unit_w, l, 0, w.context)
+            ora.append(k.numpy(), v.numpy())
+            self.caches[l] = ora
+        self.pos = 0
+        U = w.batch * w.num_kv_heads
+        self.count = {l: sum(1 for p in w.layers if p == w.layers[l]) * U for l in self.layers}
+        self.desc = (f"oracle decode step (append 1 token + fp64 attention over the dequantized cache) "
+                     f"for 1 of {U} (batch, kv head) units on layers {self.layers} (one per distinct "
+                     f"precision pair) at context {w.context}; per-unit time x {U} units x "
+                     f"{w.num_layers} layers")
+
+    def step(self) -> float:
+        """Seconds one full decode step would take, from one timed unit-step
+        per distinct layer type."""
+        total = 0.0
+        for l in self.layers:
+            k1, v1 = self.W.gen_kv(self.unit_w, l, self.w.context + self.pos, 1)
+            q = self.W.gen_q(self.unit_w, l, self.pos).numpy()
+            t0 = time.perf_counter()
+            self.caches[l].append(k1.numpy(), v1.numpy())
+            self.caches[l].attend(q)
+            total += (time.perf_counter() - t0) * self.count[l]
+        self.pos += 1
+        return total
+
+
+def oracle_sample(w, budget_s: float = 12.0):
+    """(tokens/s, seconds per full step, description) from repeated sampled
+    steps until about budget_s seconds of oracle work."""
+    smp = OracleSampler(w)
+    t_start = time.perf_counter()
+    steps = []
+    while len(steps) < 3 or (time.perf_counter() - t_start < budget_s and len(steps) < 64):
+        steps.append(smp.step())
+    step_s = statistics.median(steps)
+    return w.batch / step_s, step_s, smp.desc + f"; median over {len(steps)} sampled steps"
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from mixed_precision_quantized_quant_gb300 import kvq as K
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K.load()
+    w = W.workload(args.workload)
+    L, B, Hq, Hkv, D = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    steps, warm = args.steps, args.warmup
+    cap = w.context + warm + steps
+    stream = torch.cuda.Stream(device=dev)
+
+    cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, cap, device=dev)
+
+    # ---- prefill (timed separately: append GB/s)
+    prefill_ms = 0.0
+    prefill_bytes = 0
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            k, v = W.gen_kv(w, l, 0, w.context, device=dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            cache.append(l, k, v, stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            prefill_ms += e0.elapsed_time(e1)
+            vw = cache.view(l)
+            U = B * Hkv
+            prefill_bytes += (k.numel() + v.numel()) * 2 + U * (vw["quantized_tokens"] // w.group_size) * \
+                vw["record_bytes"] + U * vw["residual_tokens"] * 4 * D
+            del k, v
+
+    # ---- per-step inputs, resident in HBM
+    nst = warm + steps
+    kin = torch.empty((nst, L, B, Hkv, 1, D), dtype=torch.float16, device=dev)
+    vin = torch.empty_like(kin)
+    qin = torch.empty((nst, L, B, Hq, D), dtype=torch.float16, device=dev)
+    for s in range(nst):
+        for l in range(L):
+            k1, v1 = W.gen_kv(w, l, w.context + s, 1, device=dev)
+            kin[s, l].copy_(k1)
+            vin[s, l].copy_(v1)
+            qin[s, l].copy_(W.gen_q(w, l, s, device=dev))
+    outs = torch.empty((L, B, Hq, D), dtype=torch.float32, device=dev)
+    # inputs are staged into fixed buffers so the step graph is captured once
+    k_cur = torch.empty((L, B, Hkv, 1, D), dtype=torch.float16, device=dev)
+    v_cur = torch.empty_like(k_cur)
+    q_cur = torch.empty((L, B, Hq, D), dtype=torch.float16, device=dev)
+    torch.cuda.synchronize()
+
+    def step_lists():
+        return ([k_cur[l] for l in range(L)], [v_cur[l] for l in range(L)], [q_cur[l] for l in range(L)],
+                [outs[l] for l in range(L)])
+
+    Ks, Vs, Qs, Os = step_lists()
+
+    def run_step(s):
+        k_cur.copy_(kin[s], non_blocking=True)
+        v_cur.copy_(vin[s], non_blocking=True)
+        q_cur.copy_(qin[s], non_blocking=True)
+        cache.decode_step(Ks, Vs, Qs, Os, stream=stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for s in range(warm):
+            run_step(s)
+        stream.synchronize()
+        _barrier(world)
+        torch.cuda.synchronize()
+        bytes_step = sum(cache.decode_bytes(l) for l in range(L))  # at the first timed step
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        ev0.record(stream)
+        for s in range(warm, warm + steps):
+            run_step(s)
+        ev1.record(stream)
+        stream.synchronize()
+        t1 = time.time()
+        sampler.mark(t0, t1)
+        torch.cuda.synchronize()
+        _barrier(world)
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total = _max_over_ranks(ms_total, world)
+    ms_step = ms_total / steps
+    tokens_per_s = world * B * steps / (ms_total / 1e3)
+    gpu_launches = steps * 2 * L
+
+    # ---- decode-attention roofline: replay a decode-only graph of all layers
+    dec_bytes = [cache.decode_bytes(l) for l in range(L)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for l in range(L):  # warm (and loads every instantiation before capture)
+            cache.decode_attn(l, q_cur[l], outs[l], stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                cache.decode_attn(l, q_cur[l], outs[l], stream=torch.cuda.current_stream())
+        for _ in range(3):
+            g.replay()
+        stream.synchronize()
+        reps = max(10, min(200, int(200 / max(ms_step, 0.05))))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+        sampler.mark(t0, time.time())
+    dec_ms_per_launch = e0.elapsed_time(e1) / reps / L
+    dec_bytes_per_launch = sum(dec_bytes) / L
+    clocks = sampler.stop()
+
+    # ---- end to end through the public API, pinned host copies every step
+    h_k = torch.empty((nst, L, B, Hkv, 1, D), dtype=torch.float16).pin_memory()
+    h_v = torch.empty_like(h_k).pin_memory()
+    h_q = torch.empty((nst, L, B, Hq, D), dtype=torch.float16).pin_memory()
+    h_k.copy_(kin.cpu())
+    h_v.copy_(vin.cpu())
+    h_q.copy_(qin.cpu())
+    h_out = torch.empty((L, B, Hq, D), dtype=torch.float32).pin_memory()
+    e2e_cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, cap, device=dev)
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            k, v = W.gen_kv(w, l, 0, w.context, device=dev)
+            e2e_cache.append(l, k, v, stream=stream)
+            del k, v
+        stream.synchronize()
+
+        def e2e_step(s):
+            k_cur.copy_(h_k[s], non_blocking=True)
+            v_cur.copy_(h_v[s], non_blocking=True)
+            q_cur.copy_(h_q[s], non_blocking=True)
+            e2e_cache.decode_step(Ks, Vs, Qs, Os, stream=stream)
+            h_out.copy_(outs, non_blocking=True)
+            stream.synchronize()
+
+        for s in range(warm):
+            e2e_step(s)
+        _barrier(world)
+        t0 = time.perf_counter()
+        for s in range(warm, warm + steps):
+            e2e_step(s)
+        t1 = time.perf_counter()
+        _barrier(world)
+    e2e_s = _max_over_ranks(t1 - t0, world)
+    e2e_tps = world * B * steps / e2e_s
+    h2d = L * (2 * B * Hkv * D * 2 + B * Hq * D * 2)
+    d2h = L * B * Hq * D * 4
+    err = cache.device_error(stream) | e2e_cache.device_error(stream)
+    if err:
+        raise RuntimeError(f"device error word {err}")
+
+    peak, peak_kind = _peaks()
+    achieved = dec_bytes_per_launch / (dec_ms_per_launch / 1e3) / 1e9
+    traffic = _ncu_traffic(args.workload)
+    result = {
+        "metric": METRIC,
+        "value": round(tokens_per_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 codes/fp32 accumulate",
+        "data": "synthetic (seeded: keys N(mu_c, sigma_c) with channel outliers, values with drifting mean)",
+        "config": {**w.describe(), "equivalent_bits": round(cache.equivalent_bits(), 5),
+                   "parallelism": f"replicas x{world} (independent (batch, kv head) units, no collective)",
+                   "l2": "inputs larger than L2: %.2f GB of cache read per step" % (bytes_step / 1e9)},
+        "cache_read_gbs": round(bytes_step / (ms_step / 1e3) / 1e9, 1),
+        "cache_read_frac_of_peak": round(bytes_step / (ms_step / 1e3) / 1e9 / peak, 4),
+        "append_prefill_gbs": round(prefill_bytes / (prefill_ms / 1e3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_kernel (all layers, decode-only graph replay)",
+                     "bytes_per_launch": int(dec_bytes_per_launch),
+                     "us_per_launch": round(dec_ms_per_launch * 1e3, 3),
+                     "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, step_s, desc = oracle_sample(w, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                  "sample": desc, "seconds_per_step": round(step_s, 2)}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def _ncu_traffic(widx):
+    """DRAM bytes per decode launch from a committed ncu summary, if one
+    matches this workload and the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(str(widx))
+        if not ent:
+            return None
+        import hashlib
+        src = os.path.join(ROOT, "mixed_precision_quantized_quant_gb300", "csrc", "kvq_decode.cuh")
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if ent.get("kernel_sha") != h:
+            return None
+        return ent.get("traffic_bytes_per_launch")
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the oracle
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    w = W.workload(args.workload)
+    smp = OracleSampler(w)
+    vals = []
+    for s in range(args.warmup + args.steps):
+        step_s = smp.step()
+        if s >= args.warmup:
+            vals.append(step_s)
+    step_s = statistics.median(vals)
+    v = w.batch / step_s
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC, "value": round(v, 6), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 quantizer / f64 attention",
+        "data": "synthetic", "config": w.describe(),
+        "cpu_baseline": {"value": round(v, 6), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": smp.desc + "; each step is one sampled unit-step per layer type"},
+        "e2e": {"value": round(v, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=120)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--workload", type=int, default=2, help="1..5; 2 is the Llama-3.1-8B-shaped decode")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

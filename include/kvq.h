@@ -1,0 +1,186 @@
+/*
+ * kvq.h -- layer-wise mixed-precision KV-cache quantization and decode
+ * attention over the quantized cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The method (sources are web pages, cited by title and section):
+ *   - every layer stores its cache at a static precision pair KxVy,
+ *     x, y in {2, 3, 4, 8}, chosen offline and loaded with no online cost
+ *     ("KVTuner: Sensitivity-Aware Layer-Wise Mixed-Precision KV Cache
+ *     Quantization ...", sections A1 and A2; "KVmix: Gradient-Based Layer
+ *     Importance-Aware Mixed-Precision Quantization for KV Cache", 关键设计 2 and 4);
+ *   - keys are quantized asymmetrically per channel over groups of G tokens,
+ *     values per token, with scale = (max - min)/(2^b - 1), zero = min and
+ *     code = clamp(rint((x - min)/scale), 0, 2^b - 1); codes are packed into
+ *     32-bit words, 3-bit words holding ten 3-bit fields and one 2-bit field
+ *     (KVTuner section A3 "KV缓存量化基础"; KVmix 关键设计 2; "LLM 量化精读笔记 · 08
+ *     KV Cache 量化：KIVI 与误差累积", sections 6.1 and 6.2);
+ *   - the most recent tokens stay in an FP16 residual window of R_l tokens;
+ *     when the window holds R_l or more tokens the oldest G are quantized as one
+ *     key group (KIVI notes section 6.2; KVmix 关键设计 3);
+ *   - decode attention a = softmax(q K^T / sqrt(d)), o = a V runs over the
+ *     quantized tokens (dequantized on the fly) and the FP16 window, after the
+ *     new token has been appended (KVTuner section A3 equation).
+ *
+ * Conventions shared by all entry points:
+ *   - The library allocates no device memory.  The caller allocates one device
+ *     buffer of kvq_cache_bytes() bytes and hands it to kvq_create(); the
+ *     library carves the per-layer caches, their state and its workspace out
+ *     of it.  The caller frees it after kvq_destroy().
+ *   - Device pointers passed to kvq_append() and kvq_decode_attn() must be
+ *     16-byte aligned and stay valid until the work queued on `stream` is done.
+ *   - Arguments are checked on the host before anything is launched; a failed
+ *     check returns a status and changes nothing.  KVQ_ERR_CUDA reports a
+ *     failed launch; the handle's host-side state is then undefined.
+ *   - Work is queued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and runs asynchronously.  One handle is driven by
+ *     one host thread at a time; calls on a handle are ordered by the caller.
+ *   - All sequences of a batch share one length.
+ *   - No kernel spins without bound and none traps: a device-side wait that
+ *     gives up sets an error word that kvq_device_error() reports.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_ARG = 1,      /* null pointer, bad dimension, layer out of range   */
+  KVQ_ERR_BITS = 2,     /* a bit width outside {2, 3, 4, 8}                  */
+  KVQ_ERR_ALIGN = 3,    /* a pointer that is not 16-byte aligned             */
+  KVQ_ERR_CAPACITY = 4, /* appending past max_tokens, or buffer too small    */
+  KVQ_ERR_CUDA = 5,     /* a CUDA runtime call failed                        */
+  KVQ_ERR_STATE = 6,    /* call not valid now (e.g. attention on empty layer)*/
+  KVQ_ERR_UNSUPPORTED = 7 /* a shape this build has no kernel for          */
+} kvq_status;
+
+/* One layer's static precision pair and FP16 residual window (tokens).
+ * k_bits, v_bits in {2, 3, 4, 8}; residual >= group_size and a multiple of it. */
+typedef struct {
+  uint8_t k_bits;
+  uint8_t v_bits;
+  uint16_t reserved; /* must be 0 */
+  int32_t residual;
+} kvq_layer_cfg;
+
+/* Shape of the cache.
+ *   num_q_heads % num_kv_heads == 0 and num_q_heads / num_kv_heads <= 8
+ *   head_dim in {64, 128}; group_size in {32, 64, 128}
+ *   max_tokens: capacity per sequence (all appended tokens, quantized or not)
+ *   layers: num_layers entries, read during kvq_create() only. */
+typedef struct {
+  int32_t num_layers;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t group_size;
+  int32_t max_tokens;
+  const kvq_layer_cfg* layers;
+} kvq_config;
+
+typedef struct kvq_handle kvq_handle;
+
+/* Device layout of one layer, for tests and for callers that snapshot the
+ * cache.  All pointers are device pointers into the buffer given to
+ * kvq_create(); counts are the host's view after the calls issued so far.
+ *
+ * Per (batch b, kv head h) "unit" u = b * num_kv_heads + h:
+ *   records + u * unit_record_stride is a sequence of group records, one per
+ *   quantized key group (group j covers tokens [j*G, (j+1)*G)), each
+ *   record_bytes long:
+ *     [K codes: G rows x k_words u32][V codes: G rows x v_words u32]
+ *     [K scale: head_dim f16][K zero: head_dim f16]
+ *     [V (scale, zero): G pairs of f16]
+ *   A code row is one token's head_dim codes, least significant field first:
+ *   for b in {2,4,8} field j of word w is channel w*32/b + j at bits [b*j, b*j+b);
+ *   for b = 3 word w holds channels 11w .. 11w+10, fields 0..9 3-bit at bit 3j
+ *   and field 10 2-bit at bits 30..31.
+ *   residual_k + u * residual_stride (and residual_v likewise) is a ring of
+ *   `residual` slots of head_dim fp16; token i sits in slot i % residual, and
+ *   the 16-byte chunk c of a slot s is stored at chunk position c ^ (s & 7). */
+typedef struct {
+  int32_t k_bits, v_bits, residual, group_size, head_dim;
+  int32_t k_words, v_words;          /* u32 words per code row                */
+  int64_t record_bytes;
+  int64_t unit_record_stride;        /* bytes between units' record arrays    */
+  int64_t residual_stride;           /* bytes between units' rings            */
+  int64_t tokens;                    /* tokens appended so far                */
+  int64_t quantized_tokens;          /* tokens held as quantized groups       */
+  int64_t residual_tokens;           /* tokens held in the FP16 ring          */
+  const void* records;
+  const void* residual_k;
+  const void* residual_v;
+} kvq_layer_view;
+
+/* Bytes of device memory the caller must provide for `cfg` (0 if cfg is
+ * invalid).  Includes every layer's cache sized for max_tokens, per-layer
+ * state and the decode workspace. */
+size_t kvq_cache_bytes(const kvq_config* cfg);
+
+/* Validate `cfg`, lay the caches out in `dev_buf` (device memory, 256-byte
+ * aligned, `bytes` >= kvq_cache_bytes(cfg)), zero it, and select the kernel
+ * instantiations for every layer's (k_bits, v_bits, head_dim, heads-per-kv)
+ * once, so that later calls dispatch with a table lookup.  Writes a new handle
+ * to *out.  Synchronizes the device once (the zeroing). */
+kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_handle** out);
+
+/* Append n_tokens (>= 0) new tokens to `layer`, oldest first.
+ * K, V: device, fp16, [batch][num_kv_heads][n_tokens][head_dim] contiguous,
+ * read-only, caller-owned.  New tokens enter the FP16 window; every time the
+ * window reaches the layer's `residual` the oldest group_size tokens are
+ * quantized (keys per channel, values per token), packed and stored as the
+ * next group record, all in the launched kernels.  Used for prefill
+ * (n_tokens = prompt length) and for decode (n_tokens = 1).
+ * KVQ_ERR_CAPACITY if tokens + n_tokens > max_tokens. */
+kvq_status kvq_append(kvq_handle* h, int layer, const void* K, const void* V, int n_tokens,
+                      void* stream);
+
+/* Decode attention of one query token per sequence over everything appended
+ * to `layer` so far.
+ * q: device fp16 [batch][num_q_heads][head_dim]; query head j reads kv head
+ *    j / (num_q_heads / num_kv_heads).
+ * out: device fp32 [batch][num_q_heads][head_dim], written entirely.
+ * Scores are scaled by 1/sqrt(head_dim).  KVQ_ERR_STATE if the layer is empty. */
+kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, void* stream);
+
+/* One decode step over every layer: for l = 0 .. num_layers-1,
+ * kvq_append(l, K[l], V[l], 1) then kvq_decode_attn(l, q[l], out[l]).
+ * K, V, q, out are host arrays of num_layers device pointers, with the shapes
+ * above (n_tokens = 1).  The launches of a step do not depend on the cache
+ * state, so after the first call with a given set of pointers the step is
+ * replayed from a CUDA graph the handle keeps (it is re-captured when the
+ * pointers change).  KVQ_ERR_CAPACITY if any layer is full. */
+kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V,
+                           const void* const* q, float* const* out, void* stream);
+
+/* Describe `layer` (see kvq_layer_view). */
+kvq_status kvq_layer_view_get(const kvq_handle* h, int layer, kvq_layer_view* v);
+
+/* f_m: mean over layers of (k_bits + v_bits) / 2 (KVTuner section A2). */
+double kvq_equivalent_bits(const kvq_handle* h);
+
+/* Algorithmic bytes one kvq_decode_attn(layer) call reads for the current
+ * state (packed codes, scales/zeros, FP16 window, q) and writes (out). */
+int64_t kvq_decode_bytes(const kvq_handle* h, int layer);
+
+/* Reads the device error word (a bounded wait that gave up, or an internal
+ * consistency check), clearing it.  Synchronizes `stream`.  0 means none. */
+kvq_status kvq_device_error(kvq_handle* h, int32_t* code, void* stream);
+
+/* Release the handle (host memory and any captured graph).  The device buffer
+ * stays the caller's. */
+kvq_status kvq_destroy(kvq_handle* h);
+
+const char* kvq_status_string(kvq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,405 @@
+// Host side of the C ABI declared in include/kvq.h: configuration checks,
+// cache layout inside the caller's buffer, the per-layer dispatch table, the
+// host mirror of the streaming state, launches and the graph-replayed decode
+// step.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/kvq.h"
+#include "kvq_kernels.h"
+
+namespace {
+
+using kvq::AppendParams;
+using kvq::DecodeParams;
+
+constexpr int kMaxGrid = 1024;       // decode CTAs per launch (bounds the partial buffer)
+constexpr int64_t kAlign = 256;
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+int words_per_row(int d, int b) { return b == 3 ? (d + 10) / 11 : d * b / 32; }
+bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 8; }
+
+struct LayerPlan {
+  int kb, vb, R;
+  int wk, wv;
+  int64_t rec_bytes;
+  int64_t max_groups;
+  int64_t unit_rec_stride;
+  int64_t off_records, off_res_k, off_res_v;
+  int64_t res_stride_elems;
+};
+
+struct Plan {
+  int L, B, Hq, Hkv, D, G, max_tokens, gqa, units;
+  std::vector<LayerPlan> layers;
+  int64_t off_ctrl, off_err, off_counters, off_partials, partial_floats;
+  int64_t total;
+};
+
+kvq_status make_plan(const kvq_config* cfg, Plan* P) {
+  if (!cfg || !cfg->layers) return KVQ_ERR_ARG;
+  if (cfg->num_layers < 1 || cfg->batch < 1 || cfg->num_q_heads < 1 || cfg->num_kv_heads < 1 ||
+      cfg->max_tokens < 1)
+    return KVQ_ERR_ARG;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return KVQ_ERR_ARG;
+  if (cfg->group_size != 32 && cfg->group_size != 64 && cfg->group_size != 128) return KVQ_ERR_ARG;
+  if (cfg->num_q_heads % cfg->num_kv_heads != 0) return KVQ_ERR_ARG;
+  const int gqa = cfg->num_q_heads / cfg->num_kv_heads;
+  if (gqa > 8) return KVQ_ERR_UNSUPPORTED;
+  P->L = cfg->num_layers;
+  P->B = cfg->batch;
+  P->Hq = cfg->num_q_heads;
+  P->Hkv = cfg->num_kv_heads;
+  P->D = cfg->head_dim;
+  P->G = cfg->group_size;
+  P->max_tokens = cfg->max_tokens;
+  P->gqa = gqa;
+  P->units = cfg->batch * cfg->num_kv_heads;
+  int64_t off = 0;
+  P->off_ctrl = off;
+  off += align_up(static_cast<int64_t>(P->L) * 64, kAlign);
+  P->off_err = off;
+  off += kAlign;
+  P->off_counters = off;
+  off += align_up(static_cast<int64_t>(P->units) * 4, kAlign);
+  P->partial_floats = static_cast<int64_t>(kMaxGrid + P->units) * gqa * (P->D + 2);
+  P->off_partials = off;
+  off += align_up(P->partial_floats * 4, kAlign);
+  P->layers.clear();
+  for (int l = 0; l < P->L; ++l) {
+    const kvq_layer_cfg& lc = cfg->layers[l];
+    if (lc.reserved != 0) return KVQ_ERR_ARG;
+    if (!bits_ok(lc.k_bits) || !bits_ok(lc.v_bits)) return KVQ_ERR_BITS;
+    if (lc.residual < P->G || lc.residual % P->G != 0) return KVQ_ERR_ARG;
+    LayerPlan lp;
+    lp.kb = lc.k_bits;
+    lp.vb = lc.v_bits;
+    lp.R = lc.residual;
+    lp.wk = words_per_row(P->D, lp.kb);
+    lp.wv = words_per_row(P->D, lp.vb);
+    lp.rec_bytes = 4LL * P->G * (lp.wk + lp.wv) + 4LL * P->D + 4LL * P->G;
+    lp.max_groups = P->max_tokens / P->G;
+    lp.unit_rec_stride = align_up(lp.max_groups * lp.rec_bytes, kAlign);
+    lp.off_records = off;
+    off += lp.unit_rec_stride * P->units;
+    lp.res_stride_elems = static_cast<int64_t>(lp.R) * P->D;
+    lp.off_res_k = off;
+    off += align_up(lp.res_stride_elems * 2 * P->units, kAlign);
+    lp.off_res_v = off;
+    off += align_up(lp.res_stride_elems * 2 * P->units, kAlign);
+    P->layers.push_back(lp);
+  }
+  P->total = off;
+  return KVQ_OK;
+}
+
+struct StepGraph {
+  std::vector<const void*> key;
+  cudaGraphExec_t exec = nullptr;
+};
+
+}  // namespace
+
+struct kvq_handle {
+  Plan plan;
+  uint8_t* base = nullptr;
+  std::vector<int64_t> tokens;  // host mirror of each layer's appended tokens
+  std::vector<kvq::DecodeKernel> dec;
+  std::vector<int> grid;
+  StepGraph graph;
+};
+
+namespace {
+
+int32_t* ctrl(kvq_handle* h, int layer) {
+  return reinterpret_cast<int32_t*>(h->base + h->plan.off_ctrl + static_cast<int64_t>(layer) * 64);
+}
+int32_t* errw(kvq_handle* h) { return reinterpret_cast<int32_t*>(h->base + h->plan.off_err); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V, int n, cudaStream_t s) {
+  const Plan& P = h->plan;
+  const LayerPlan& lp = P.layers[layer];
+  const int64_t T = h->tokens[layer];
+  const int64_t nq0 = kvq::quantized_after(T, lp.R, P.G);
+  const int64_t nq1 = kvq::quantized_after(T + n, lp.R, P.G);
+  const int64_t nflush = (nq1 - nq0) / P.G;
+  const int64_t first_res = T > nq1 ? T : nq1;
+  const int64_t nres = T + n - first_res;
+
+  AppendParams ap;
+  ap.K = static_cast<const __half*>(K);
+  ap.V = static_cast<const __half*>(V);
+  ap.n = n;
+  ap.units = P.units;
+  ap.G = P.G;
+  ap.R = lp.R;
+  ap.rec_bytes = static_cast<int>(lp.rec_bytes);
+  ap.unit_rec_stride = lp.unit_rec_stride;
+  ap.records = h->base + lp.off_records;
+  ap.res_k = reinterpret_cast<__half*>(h->base + lp.off_res_k);
+  ap.res_v = reinterpret_cast<__half*>(h->base + lp.off_res_v);
+  ap.res_stride = lp.res_stride_elems;
+  ap.tokens = ctrl(h, layer);
+  ap.done_ctr = ctrl(h, layer) + 1;
+  ap.err = errw(h);
+  const size_t smem = kvq::append_smem_bytes(lp.kb, lp.vb, P.D, P.G, static_cast<int>(lp.rec_bytes));
+  cudaError_t e = cudaSuccess;
+  if (n == 1) {
+    ap.mode = kvq::kFlush | kvq::kResidual | kvq::kUpdateState;
+    ap.ctas = P.units;
+    e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(1, P.units), smem, s);
+  } else {
+    if (nflush > 0) {
+      ap.mode = kvq::kFlush | (nres == 0 ? kvq::kUpdateState : 0);
+      ap.ctas = static_cast<int>(nflush * P.units);
+      e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(static_cast<unsigned>(nflush), P.units), smem, s);
+    }
+    if (e == cudaSuccess && nres > 0) {
+      const int64_t chunks = (nres + 15) / 16;
+      ap.mode = kvq::kResidual | kvq::kUpdateState;
+      ap.ctas = static_cast<int>(chunks * P.units);
+      e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(static_cast<unsigned>(chunks), P.units), 0, s);
+    }
+  }
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  h->tokens[layer] = T + n;
+  return KVQ_OK;
+}
+
+kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cudaStream_t s) {
+  const Plan& P = h->plan;
+  const LayerPlan& lp = P.layers[layer];
+  DecodeParams dp;
+  dp.q = static_cast<const __half*>(q);
+  dp.out = out;
+  dp.records = h->base + lp.off_records;
+  dp.unit_rec_stride = lp.unit_rec_stride;
+  dp.res_k = reinterpret_cast<const __half*>(h->base + lp.off_res_k);
+  dp.res_v = reinterpret_cast<const __half*>(h->base + lp.off_res_v);
+  dp.res_stride = lp.res_stride_elems;
+  dp.tokens = ctrl(h, layer);
+  dp.partials = reinterpret_cast<float*>(h->base + P.off_partials);
+  dp.counters = reinterpret_cast<int32_t*>(h->base + P.off_counters);
+  dp.err = errw(h);
+  dp.units = P.units;
+  dp.kv_heads = P.Hkv;
+  dp.gqa = P.gqa;
+  dp.G = P.G;
+  dp.R = lp.R;
+  dp.rec_bytes = static_cast<int>(lp.rec_bytes);
+  dp.grid = h->grid[layer];
+  dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
+  const kvq::DecodeKernel& k = h->dec[layer];
+  k.fn<<<h->grid[layer], kvq::kThreads, k.smem, s>>>(dp);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_cache_bytes(const kvq_config* cfg) {
+  Plan P;
+  if (make_plan(cfg, &P) != KVQ_OK) return 0;
+  return static_cast<size_t>(P.total);
+}
+
+kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_handle** out) {
+  if (!out) return KVQ_ERR_ARG;
+  *out = nullptr;
+  Plan P;
+  kvq_status st = make_plan(cfg, &P);
+  if (st != KVQ_OK) return st;
+  if (!dev_buf) return KVQ_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(dev_buf) & (kAlign - 1)) != 0) return KVQ_ERR_ALIGN;
+  if (bytes < static_cast<size_t>(P.total)) return KVQ_ERR_CAPACITY;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  kvq_handle* h = new (std::nothrow) kvq_handle;
+  if (!h) return KVQ_ERR_ARG;
+  h->plan = P;
+  h->base = static_cast<uint8_t*>(dev_buf);
+  h->tokens.assign(P.L, 0);
+  for (int l = 0; l < P.L; ++l) {
+    const LayerPlan& lp = P.layers[l];
+    kvq::DecodeKernel k =
+        kvq::decode_select(lp.kb, lp.vb, P.D, P.gqa, P.G, static_cast<int>(lp.rec_bytes));
+    if (!k.fn) {
+      delete h;
+      return KVQ_ERR_UNSUPPORTED;
+    }
+    h->dec.push_back(k);
+    int gsz = sms * k.ctas_per_sm;
+    if (gsz > kMaxGrid) gsz = kMaxGrid;
+    h->grid.push_back(gsz);
+  }
+  if (cudaMemset(dev_buf, 0, static_cast<size_t>(P.total)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    delete h;
+    return KVQ_ERR_CUDA;
+  }
+  *out = h;
+  return KVQ_OK;
+}
+
+kvq_status kvq_append(kvq_handle* h, int layer, const void* K, const void* V, int n_tokens, void* stream) {
+  if (!h || layer < 0 || layer >= h->plan.L || n_tokens < 0) return KVQ_ERR_ARG;
+  if (n_tokens == 0) return KVQ_OK;
+  if (!K || !V) return KVQ_ERR_ARG;
+  if (!aligned16(K) || !aligned16(V)) return KVQ_ERR_ALIGN;
+  if (h->tokens[layer] + n_tokens > h->plan.max_tokens) return KVQ_ERR_CAPACITY;
+  return launch_append(h, layer, K, V, n_tokens, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, void* stream) {
+  if (!h || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
+  if (!q || !out) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
+  if (h->tokens[layer] <= 0) return KVQ_ERR_STATE;
+  return launch_decode(h, layer, q, out, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V, const void* const* q,
+                           float* const* out, void* stream) {
+  if (!h || !K || !V || !q || !out) return KVQ_ERR_ARG;
+  const int L = h->plan.L;
+  for (int l = 0; l < L; ++l) {
+    if (!K[l] || !V[l] || !q[l] || !out[l]) return KVQ_ERR_ARG;
+    if (!aligned16(K[l]) || !aligned16(V[l]) || !aligned16(q[l]) || !aligned16(out[l])) return KVQ_ERR_ALIGN;
+    if (h->tokens[l] + 1 > h->plan.max_tokens) return KVQ_ERR_CAPACITY;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::vector<const void*> key;
+  key.reserve(4 * L);
+  for (int l = 0; l < L; ++l) {
+    key.push_back(K[l]);
+    key.push_back(V[l]);
+    key.push_back(q[l]);
+    key.push_back(out[l]);
+  }
+  if (s == nullptr) {  // the legacy stream cannot be captured: launch directly
+    for (int l = 0; l < L; ++l) {
+      kvq_status st = launch_append(h, l, K[l], V[l], 1, s);
+      if (st != KVQ_OK) return st;
+      st = launch_decode(h, l, q[l], out[l], s);
+      if (st != KVQ_OK) return st;
+    }
+    return KVQ_OK;
+  }
+  if (!h->graph.exec || h->graph.key != key) {
+    if (h->graph.exec) {
+      cudaGraphExecDestroy(h->graph.exec);
+      h->graph.exec = nullptr;
+    }
+    std::vector<int64_t> saved = h->tokens;
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return KVQ_ERR_CUDA;
+    kvq_status st = KVQ_OK;
+    for (int l = 0; l < L && st == KVQ_OK; ++l) {
+      st = launch_append(h, l, K[l], V[l], 1, s);
+      if (st == KVQ_OK) st = launch_decode(h, l, q[l], out[l], s);
+    }
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+    h->tokens = saved;
+    if (st != KVQ_OK || ec != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      return st != KVQ_OK ? st : KVQ_ERR_CUDA;
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&h->graph.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) {
+      h->graph.exec = nullptr;
+      return KVQ_ERR_CUDA;
+    }
+    h->graph.key = key;
+  }
+  if (cudaGraphLaunch(h->graph.exec, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  for (int l = 0; l < L; ++l) h->tokens[l] += 1;
+  return KVQ_OK;
+}
+
+kvq_status kvq_layer_view_get(const kvq_handle* h, int layer, kvq_layer_view* v) {
+  if (!h || !v || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
+  const Plan& P = h->plan;
+  const LayerPlan& lp = P.layers[layer];
+  std::memset(v, 0, sizeof(*v));
+  v->k_bits = lp.kb;
+  v->v_bits = lp.vb;
+  v->residual = lp.R;
+  v->group_size = P.G;
+  v->head_dim = P.D;
+  v->k_words = lp.wk;
+  v->v_words = lp.wv;
+  v->record_bytes = lp.rec_bytes;
+  v->unit_record_stride = lp.unit_rec_stride;
+  v->residual_stride = lp.res_stride_elems * 2;
+  v->tokens = h->tokens[layer];
+  v->quantized_tokens = kvq::quantized_after(h->tokens[layer], lp.R, P.G);
+  v->residual_tokens = v->tokens - v->quantized_tokens;
+  v->records = h->base + lp.off_records;
+  v->residual_k = h->base + lp.off_res_k;
+  v->residual_v = h->base + lp.off_res_v;
+  return KVQ_OK;
+}
+
+double kvq_equivalent_bits(const kvq_handle* h) {
+  if (!h) return 0.0;
+  double s = 0.0;
+  for (const LayerPlan& lp : h->plan.layers) s += 0.5 * (lp.kb + lp.vb);
+  return s / h->plan.L;
+}
+
+int64_t kvq_decode_bytes(const kvq_handle* h, int layer) {
+  if (!h || layer < 0 || layer >= h->plan.L) return -1;
+  const Plan& P = h->plan;
+  const LayerPlan& lp = P.layers[layer];
+  const int64_t T = h->tokens[layer];
+  const int64_t nq = kvq::quantized_after(T, lp.R, P.G);
+  const int64_t r = T - nq;
+  const int64_t per_unit = (nq / P.G) * lp.rec_bytes + r * 4LL * P.D;
+  return P.units * per_unit + static_cast<int64_t>(P.B) * P.Hq * P.D * (2 + 4);
+}
+
+kvq_status kvq_device_error(kvq_handle* h, int32_t* code, void* stream) {
+  if (!h || !code) return KVQ_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, errw(h), 4, cudaMemcpyDeviceToHost) != cudaSuccess) return KVQ_ERR_CUDA;
+  *code = v;
+  if (v != 0 && cudaMemset(errw(h), 0, 4) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_destroy(kvq_handle* h) {
+  if (!h) return KVQ_ERR_ARG;
+  if (h->graph.exec) cudaGraphExecDestroy(h->graph.exec);
+  delete h;
+  return KVQ_OK;
+}
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_ARG: return "invalid argument";
+    case KVQ_ERR_BITS: return "bit width outside {2,3,4,8}";
+    case KVQ_ERR_ALIGN: return "pointer not aligned";
+    case KVQ_ERR_CAPACITY: return "capacity exceeded";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_STATE: return "invalid state";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+// Device-side building blocks shared by the append and decode kernels:
+// inline-PTX wrappers (bulk TMA copies, mbarriers with bounded waits,
+// warp-level tensor-core MMA, ldmatrix), the streaming-state arithmetic and
+// the kernel parameter blocks.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kvq {
+
+// ---------------------------------------------------------------- constants
+
+constexpr int kThreads = 128;          // every kernel runs 4 warps per CTA
+constexpr int kWarps = kThreads / 32;
+constexpr int kResTile = 16;           // residual tokens per decode work item
+constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier waits
+
+// device error codes (written to the error word, never trapped)
+constexpr int32_t kErrWaitTimeout = 1;
+constexpr int32_t kErrBadState = 2;
+
+// ---------------------------------------------------------------- state
+
+// Tokens held after `total` appended tokens, with a residual window of R
+// tokens and key groups of G: whenever the window holds R or more tokens the
+// oldest G are quantized.  R is a multiple of G.
+__host__ __device__ __forceinline__ int64_t quantized_after(int64_t total, int R, int G) {
+  if (total < R) return 0;
+  return (int64_t)G * ((total - R) / G + 1);
+}
+
+// ---------------------------------------------------------------- params
+
+struct AppendParams {
+  const __half* K;        // [units][n][D]
+  const __half* V;
+  int n;                  // tokens appended by this call
+  int units;              // batch * kv heads
+  int G, R;
+  int rec_bytes;
+  int64_t unit_rec_stride;   // bytes
+  uint8_t* records;
+  __half* res_k;          // [units][R][D] ring (chunk-swizzled)
+  __half* res_v;
+  int64_t res_stride;     // elements between units' rings
+  int32_t* tokens;        // device state: tokens appended so far
+  int32_t* done_ctr;      // last-CTA counter of this launch
+  int32_t* err;
+  int mode;               // kFlush | kResidual | kUpdateState
+  int ctas;               // CTAs in this launch (for the last-CTA count)
+};
+constexpr int kFlush = 1, kResidual = 2, kUpdateState = 4;
+
+struct DecodeParams {
+  const __half* q;        // [B][Hq][D]
+  float* out;             // [B][Hq][D]
+  const uint8_t* records;
+  int64_t unit_rec_stride;
+  const __half* res_k;
+  const __half* res_v;
+  int64_t res_stride;     // elements
+  const int32_t* tokens;  // device state
+  float* partials;        // [slots][gqa][D + 2]
+  int32_t* counters;      // [units]
+  int32_t* err;
+  int units;
+  int kv_heads;
+  int gqa;                // query heads per kv head
+  int G, R;
+  int rec_bytes;
+  int grid;               // CTAs launched
+  float alpha;            // log2(e) / sqrt(D)
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// make generic-proxy shared-memory writes visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion signalled on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 1-D bulk copy shared -> global (bulk-group completion).
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Bounded wait on an mbarrier phase.  Returns false (and records the error)
+// if the phase did not complete within the iteration limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t* err) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(phase)
+        : "memory");
+    if (done) return true;
+  }
+  atomicExch(err, kErrWaitTimeout);
+  return false;
+}
+
+// D = A(16x16 f16, row) * B(16x8 f16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// (x & mask) | magic in one LOP3
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(magic));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// e holds two fp16 values 1024 + f*code (exact); returns the codes, exact:
+// e * (1/f) - 1024/f with one fma (f a power of two).
+__device__ __forceinline__ uint32_t magic_fix(uint32_t e, float inv_f) {
+  const __half2 s = __float2half2_rn(inv_f);
+  const __half2 o = __float2half2_rn(-1024.0f * inv_f);
+  return h2_as_u32(__hfma2(u32_as_h2(e), s, o));
+}
+
+constexpr uint32_t kMagic = 0x64006400u;  // fp16 1024.0 in both halves
+
+}  // namespace kvq

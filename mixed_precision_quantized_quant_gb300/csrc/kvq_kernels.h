@@ -1,0 +1,26 @@
+// Host-visible entry points of the CUDA kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "kvq_device.cuh"
+
+namespace kvq {
+
+// Fused quantize + pack + append, bit-width specialised.
+cudaError_t append_dispatch(int kb, int vb, int D, const AppendParams& p, dim3 grid, size_t smem,
+                            cudaStream_t s);
+size_t append_smem_bytes(int kb, int vb, int D, int G, int rec_bytes);
+
+// Decode attention, specialised on (k_bits, v_bits, head_dim, n-tiles).
+typedef void (*decode_kernel_t)(DecodeParams);
+struct DecodeKernel {
+  decode_kernel_t fn;
+  size_t smem;      // dynamic shared memory per CTA
+  int ctas_per_sm;  // occupancy at that smem
+};
+// Returns fn == nullptr if the combination has no instantiation.
+DecodeKernel decode_select(int kb, int vb, int D, int gqa, int G, int rec_bytes);
+size_t decode_smem_bytes(int D, int nt, int rec_bytes);
+
+}  // namespace kvq

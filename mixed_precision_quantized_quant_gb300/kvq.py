@@ -1,0 +1,255 @@
+"""Thin ctypes binding of libkvq.so (include/kvq.h).
+
+Argument marshalling only: every step of quantization and attention runs in
+the library's CUDA kernels.  PyTorch provides the device memory and streams.
+The functions keep the C names; ``KVQCache`` bundles them for convenience.
+There is no fallback: if the library is not built, loading it raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+STATUS = {
+    0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_BITS", 3: "KVQ_ERR_ALIGN", 4: "KVQ_ERR_CAPACITY",
+    5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_STATE", 7: "KVQ_ERR_UNSUPPORTED",
+}
+
+EXPORTS = (
+    "kvq_cache_bytes", "kvq_create", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
+    "kvq_layer_view_get", "kvq_equivalent_bits", "kvq_decode_bytes", "kvq_device_error",
+    "kvq_destroy", "kvq_status_string",
+)
+
+
+class KVQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class LayerCfg(ctypes.Structure):
+    _fields_ = [("k_bits", ctypes.c_uint8), ("v_bits", ctypes.c_uint8),
+                ("reserved", ctypes.c_uint16), ("residual", ctypes.c_int32)]
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32), ("layers", ctypes.POINTER(LayerCfg))]
+
+
+class LayerView(ctypes.Structure):
+    _fields_ = [("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32), ("residual", ctypes.c_int32),
+                ("group_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("k_words", ctypes.c_int32), ("v_words", ctypes.c_int32),
+                ("record_bytes", ctypes.c_int64), ("unit_record_stride", ctypes.c_int64),
+                ("residual_stride", ctypes.c_int64), ("tokens", ctypes.c_int64),
+                ("quantized_tokens", ctypes.c_int64), ("residual_tokens", ctypes.c_int64),
+                ("records", ctypes.c_void_p), ("residual_k", ctypes.c_void_p),
+                ("residual_v", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libkvq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"{path} is missing: build it with mixed_precision_quantized_quant_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.kvq_cache_bytes.argtypes = [ctypes.POINTER(Config)]
+    L.kvq_cache_bytes.restype = ctypes.c_size_t
+    L.kvq_create.argtypes = [ctypes.POINTER(Config), vp, ctypes.c_size_t, ctypes.POINTER(vp)]
+    L.kvq_create.restype = ctypes.c_int
+    L.kvq_append.argtypes = [vp, ctypes.c_int, vp, vp, ctypes.c_int, vp]
+    L.kvq_append.restype = ctypes.c_int
+    L.kvq_decode_attn.argtypes = [vp, ctypes.c_int, vp, vp, vp]
+    L.kvq_decode_attn.restype = ctypes.c_int
+    L.kvq_decode_step.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                  ctypes.POINTER(vp), vp]
+    L.kvq_decode_step.restype = ctypes.c_int
+    L.kvq_layer_view_get.argtypes = [vp, ctypes.c_int, ctypes.POINTER(LayerView)]
+    L.kvq_layer_view_get.restype = ctypes.c_int
+    L.kvq_equivalent_bits.argtypes = [vp]
+    L.kvq_equivalent_bits.restype = ctypes.c_double
+    L.kvq_decode_bytes.argtypes = [vp, ctypes.c_int]
+    L.kvq_decode_bytes.restype = i64
+    L.kvq_device_error.argtypes = [vp, ctypes.POINTER(i32), vp]
+    L.kvq_device_error.restype = ctypes.c_int
+    L.kvq_destroy.argtypes = [vp]
+    L.kvq_destroy.restype = ctypes.c_int
+    L.kvq_status_string.argtypes = [ctypes.c_int]
+    L.kvq_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(st: int, where: str) -> None:
+    if st != 0:
+        raise KVQError(st, where)
+
+
+def make_config(layers: Sequence[Tuple[int, int, int]], batch: int, num_q_heads: int, num_kv_heads: int,
+                head_dim: int, group_size: int, max_tokens: int):
+    arr = (LayerCfg * len(layers))()
+    for i, (kb, vb, r) in enumerate(layers):
+        arr[i].k_bits, arr[i].v_bits, arr[i].reserved, arr[i].residual = kb, vb, 0, r
+    cfg = Config(len(layers), batch, num_q_heads, num_kv_heads, head_dim, group_size, max_tokens,
+                 ctypes.cast(arr, ctypes.POINTER(LayerCfg)))
+    cfg._keep = arr  # keep the layer array alive with the struct
+    return cfg
+
+
+# ---------------------------------------------------------------- C names
+
+def kvq_cache_bytes(cfg: Config) -> int:
+    return int(load().kvq_cache_bytes(ctypes.byref(cfg)))
+
+
+def kvq_create(cfg: Config, dev_buf: int, nbytes: int) -> int:
+    h = ctypes.c_void_p()
+    _check(load().kvq_create(ctypes.byref(cfg), ctypes.c_void_p(dev_buf), nbytes, ctypes.byref(h)), "kvq_create")
+    return h.value
+
+
+def kvq_append(h: int, layer: int, K: int, V: int, n_tokens: int, stream: int) -> None:
+    _check(load().kvq_append(h, layer, K, V, n_tokens, stream), "kvq_append")
+
+
+def kvq_decode_attn(h: int, layer: int, q: int, out: int, stream: int) -> None:
+    _check(load().kvq_decode_attn(h, layer, q, out, stream), "kvq_decode_attn")
+
+
+def kvq_decode_step(h: int, K: Sequence[int], V: Sequence[int], q: Sequence[int], out: Sequence[int],
+                    stream: int) -> None:
+    n = len(K)
+    arr = [(ctypes.c_void_p * n)(*x) for x in (K, V, q, out)]
+    _check(load().kvq_decode_step(h, *arr, stream), "kvq_decode_step")
+
+
+def kvq_layer_view_get(h: int, layer: int) -> dict:
+    v = LayerView()
+    _check(load().kvq_layer_view_get(h, layer, ctypes.byref(v)), "kvq_layer_view_get")
+    return {name: getattr(v, name) for name, _ in LayerView._fields_}
+
+
+def kvq_equivalent_bits(h: int) -> float:
+    return float(load().kvq_equivalent_bits(h))
+
+
+def kvq_decode_bytes(h: int, layer: int) -> int:
+    return int(load().kvq_decode_bytes(h, layer))
+
+
+def kvq_device_error(h: int, stream: int) -> int:
+    code = ctypes.c_int32(0)
+    _check(load().kvq_device_error(h, ctypes.byref(code), stream), "kvq_device_error")
+    return code.value
+
+
+def kvq_destroy(h: int) -> None:
+    _check(load().kvq_destroy(h), "kvq_destroy")
+
+
+def kvq_status_string(s: int) -> str:
+    return load().kvq_status_string(s).decode()
+
+
+# ---------------------------------------------------------------- convenience
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dev_ptr(t, name: str, dtype, shape) -> int:
+    import torch
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return int(t.data_ptr())
+
+
+class KVQCache:
+    """A layer-wise mixed-precision KV cache living in one torch-allocated
+    device buffer."""
+
+    def __init__(self, layers: Sequence[Tuple[int, int, int]], batch: int, num_q_heads: int,
+                 num_kv_heads: int, head_dim: int, group_size: int, max_tokens: int, device="cuda"):
+        import torch
+        self.layers = [tuple(x) for x in layers]
+        self.B, self.Hq, self.Hkv, self.D, self.G = batch, num_q_heads, num_kv_heads, head_dim, group_size
+        self.max_tokens = max_tokens
+        self.cfg = make_config(self.layers, batch, num_q_heads, num_kv_heads, head_dim, group_size, max_tokens)
+        self.nbytes = kvq_cache_bytes(self.cfg)
+        if self.nbytes == 0:
+            raise KVQError(1, "kvq_cache_bytes")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.h = kvq_create(self.cfg, int(self.buf.data_ptr()), self.nbytes)
+
+    def append(self, layer: int, K, V, stream=None) -> None:
+        import torch
+        n = K.shape[2]
+        shp = (self.B, self.Hkv, n, self.D)
+        kvq_append(self.h, layer, _dev_ptr(K, "K", torch.float16, shp), _dev_ptr(V, "V", torch.float16, shp),
+                   n, _stream_ptr(stream))
+
+    def decode_attn(self, layer: int, q, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=q.device)
+        kvq_decode_attn(self.h, layer, _dev_ptr(q, "q", torch.float16, (self.B, self.Hq, self.D)),
+                        _dev_ptr(out, "out", torch.float32, (self.B, self.Hq, self.D)), _stream_ptr(stream))
+        return out
+
+    def decode_step(self, K: List, V: List, q: List, out: List, stream=None) -> None:
+        import torch
+        kv = (self.B, self.Hkv, 1, self.D)
+        qs = (self.B, self.Hq, self.D)
+        kvq_decode_step(self.h,
+                        [_dev_ptr(x, "K", torch.float16, kv) for x in K],
+                        [_dev_ptr(x, "V", torch.float16, kv) for x in V],
+                        [_dev_ptr(x, "q", torch.float16, qs) for x in q],
+                        [_dev_ptr(x, "out", torch.float32, qs) for x in out],
+                        _stream_ptr(stream))
+
+    def view(self, layer: int) -> dict:
+        return kvq_layer_view_get(self.h, layer)
+
+    def equivalent_bits(self) -> float:
+        return kvq_equivalent_bits(self.h)
+
+    def decode_bytes(self, layer: int) -> int:
+        return kvq_decode_bytes(self.h, layer)
+
+    def device_error(self, stream=None) -> int:
+        return kvq_device_error(self.h, _stream_ptr(stream))
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            kvq_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

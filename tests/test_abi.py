@@ -1,0 +1,92 @@
+"""The C-ABI library: it loads, exports every entry point include/kvq.h
+declares, and its host-only sizing logic behaves.  No GPU needed."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixed_precision_quantized_quant_gb300 import kvq as K
+from mixed_precision_quantized_quant_gb300 import workloads as W
+from oracle import kvq_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(K.LIB_PATH):
+        from mixed_precision_quantized_quant_gb300 import build
+        build.build()
+    return K.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(K.EXPORTS) == set(names), (set(K.EXPORTS) ^ set(names))
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert K.kvq_status_string(code)
+    assert K.kvq_status_string(0) == "ok"
+
+
+def _cfg(**kw):
+    base = dict(layers=[(4, 2, 32)], batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, group_size=32,
+                max_tokens=1024)
+    base.update(kw)
+    return K.make_config(base.pop("layers"), **base)
+
+
+def test_cache_bytes_rejects_bad_configs(lib):
+    assert K.kvq_cache_bytes(_cfg()) > 0
+    bad = [dict(head_dim=96), dict(group_size=48), dict(num_q_heads=6, num_kv_heads=4),
+           dict(num_q_heads=32, num_kv_heads=2), dict(layers=[(5, 2, 32)]), dict(layers=[(4, 2, 48)]),
+           dict(layers=[(4, 2, 16)]), dict(batch=0), dict(max_tokens=0)]
+    for b in bad:
+        assert K.kvq_cache_bytes(_cfg(**b)) == 0, b
+
+
+def test_cache_bytes_covers_layout(lib):
+    # the buffer holds at least the records for max_tokens and the windows
+    for idx in range(1, 6):
+        w = W.workload(idx)
+        cfg = K.make_config(w.layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.group_size,
+                            w.total_tokens)
+        nb = K.kvq_cache_bytes(cfg)
+        U = w.batch * w.num_kv_heads
+        need = 0
+        for kb, vb, R in w.layers:
+            rec = O.record_layout(w.head_dim, w.group_size, kb, vb)["bytes"]
+            need += U * (w.total_tokens // w.group_size) * rec + 2 * U * R * w.head_dim * 2
+        assert need <= nb <= need * 1.02 + (64 << 20), (idx, nb, need)
+
+
+def test_create_rejects_without_buffer(lib):
+    h = ctypes.c_void_p()
+    cfg = _cfg()
+    st = lib.kvq_create(ctypes.byref(cfg), None, 0, ctypes.byref(h))
+    assert st == 1 and not h.value
+    st = lib.kvq_create(ctypes.byref(cfg), ctypes.c_void_p(256), 16, ctypes.byref(h))
+    assert st == 4 and not h.value  # buffer too small: checked before any CUDA call
+    st = lib.kvq_create(ctypes.byref(cfg), ctypes.c_void_p(8), 1 << 40, ctypes.byref(h))
+    assert st == 3 and not h.value  # misaligned
+
+
+def test_null_handle_calls_are_rejected(lib):
+    assert lib.kvq_append(None, 0, None, None, 1, None) == 1
+    assert lib.kvq_decode_attn(None, 0, None, None, None) == 1
+    assert lib.kvq_destroy(None) == 1
+    assert lib.kvq_equivalent_bits(None) == 0.0
+    assert lib.kvq_decode_bytes(None, 0) == -1
