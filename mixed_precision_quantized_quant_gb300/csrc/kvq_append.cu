@@ -22,7 +22,6 @@ namespace {
 template <int B>
 struct BitsT {
   static constexpr int kQmax = (1 << B) - 1;
-  static constexpr int kWords128 = (B == 3) ? 12 : 128 * B / 32;
 };
 
 __host__ __device__ constexpr int words_per_row(int d, int b) { return b == 3 ? (d + 10) / 11 : d * b / 32; }

@@ -32,28 +32,39 @@
 
 namespace kvq {
 
-constexpr int kStages = 2;
+constexpr int kSlots = 4;   // copies in flight per warp (mbarrier slots)
+constexpr int kSlice = 32;  // tokens of a key group staged per work item
 
-__host__ __device__ constexpr int dec_stage_bytes(int D, int rec_bytes) {
-  return (((rec_bytes > kResTile * 4 * D) ? rec_bytes : kResTile * 4 * D) + 127) / 128 * 128;
+// Bytes of one staged 32-token slice of a group record:
+// [K rows][V rows][K scale][K zero][V (scale, zero) pairs].
+__host__ __device__ constexpr int slice_bytes(int D, int G, int rec_bytes) {
+  return (rec_bytes - 4 * D - 4 * G) / G * kSlice + 4 * D + 4 * kSlice;
+}
+
+// Per-warp ring of staged items: room for one residual tile plus one slice,
+// and at least two slices.
+__host__ __device__ constexpr int ring_bytes(int D, int G, int rec_bytes) {
+  const int sl = slice_bytes(D, G, rec_bytes), rt = kResTile * 4 * D;
+  const int need = (sl + rt > 2 * sl) ? sl + rt : 2 * sl;
+  return (need + 127) / 128 * 128;
 }
 
 struct DecodeSmem {
-  int stage_bytes;
-  int off_bars, off_qs, off_qp, off_qr, off_wm, off_wl, off_dm, off_flags, off_wo, off_dump, total;
+  int ring;
+  int off_bars, off_qs, off_qp, off_qr, off_wm, off_wl, off_dm, off_flags, off_wo, total;
 };
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int rec_bytes) {
+__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, int rec_bytes) {
   DecodeSmem s;
   const int H = 4 * NT;
-  s.stage_bytes = dec_stage_bytes(D, rec_bytes);
-  int off = kWarps * kStages * s.stage_bytes;
+  s.ring = ring_bytes(D, G, rec_bytes);
+  int off = kWarps * s.ring;
   s.off_bars = off;
-  off += kWarps * kStages * 8;
+  off += kWarps * kSlots * 8;
   s.off_qs = off;
   off += H * D * 2;
   s.off_qp = off;
-  off += 32 * (NT * D / 8 + 4) * 4;
+  off += 32 * (NT * 18 + 4) * 4;  // key-pair table (up to 18 pairs per thread)
   s.off_qr = off;
   off += 32 * (NT * D / 16 * 2 + 4) * 4;
   s.off_wm = off;
@@ -67,17 +78,82 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int rec_
   off = (off + 15) / 16 * 16;
   s.off_wo = off;
   off += kWarps * H * D * 4;
-  s.off_dump = off;
-  off += kWarps * H * D * 4;
   s.total = off;
   return s;
 }
 
 // ------------------------------------------------------------------ unpacking
 
-// Code pairs of one key word, in the order the query pairs are built:
-//  4-bit: (c0,c4) (c1,c5) (c2,c6) (c3,c7); 2-bit: (c_i, c_{8+i}), i = 0..7;
-//  8-bit: (c0,c2) (c1,c3).  Each pair is a half2 of exact integer codes.
+template <int N>
+__device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint32_t* p) {
+  if constexpr (N == 1) {
+    w[0] = p[0];
+  } else if constexpr (N == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(p + i);
+      w[i] = v.x;
+      w[i + 1] = v.y;
+      w[i + 2] = v.z;
+      w[i + 3] = v.w;
+    }
+  }
+}
+
+// Score k-steps (pairs of channels per thread per token row = 2 x this).
+// 3-bit keys: each thread owns 3 (d128) or 2 (d64) words of 11 fields.
+template <int KB, int D>
+struct KeyShape {
+  static constexpr int WK = (KB == 3) ? (D + 10) / 11 : D * KB / 32;  // words per token row
+  static constexpr int WT = (KB == 3) ? (D == 128 ? 3 : 2) : WK / 4;  // words per thread
+  static constexpr int KSK = (KB == 3) ? (D == 128 ? 9 : 6) : D / 16;
+  static constexpr int NPK = 2 * KSK;
+  static constexpr int PW = (KB == 3) ? 5 : 16 / KB;                  // pairs per word
+};
+
+// Value m-tiles in the quantized-path channel map (3-bit adds a tile for the
+// 2-bit fields of the 11-field words).
+template <int VB, int D>
+struct ValShape {
+  static constexpr int WV = (VB == 3) ? (D + 10) / 11 : D * VB / 32;
+  static constexpr int MT3 = (D == 128) ? 8 : 5;
+  static constexpr int MTV = (VB == 3) ? MT3 + 1 : D / 16;
+  static constexpr int VW = (VB == 3) ? 1 : ((D * VB / 256) > 0 ? (D * VB / 256) : 1);
+};
+
+// Channels (ca, cb) of key pair pi of thread tig (-1 for padding).
+//  4-bit: (c0,c4) (c1,c5) (c2,c6) (c3,c7) per word; 2-bit: (c_i, c_{8+i});
+//  8-bit: (c0,c2) (c1,c3); 3-bit: fields (i, i+5) of each word, then the
+//  2-bit fields of the thread's words paired two by two.
+template <int KB, int D>
+__device__ __forceinline__ void key_pair_channels(int tig, int pi, int& ca, int& cb) {
+  using S = KeyShape<KB, D>;
+  if constexpr (KB == 3) {
+    const int w0 = tig * S::WT;
+    if (pi < 5 * S::WT) {
+      const int base = 11 * (w0 + pi / 5);
+      ca = base + pi % 5;
+      cb = ca + 5;
+    } else {
+      const int k = pi - 5 * S::WT;
+      ca = (2 * k < S::WT) ? 11 * (w0 + 2 * k) + 10 : -1;
+      cb = (2 * k + 1 < S::WT) ? 11 * (w0 + 2 * k + 1) + 10 : -1;
+    }
+    if (ca >= D) ca = -1;
+    if (cb >= D) cb = -1;
+  } else {
+    const int wi = pi / S::PW, e = pi % S::PW;
+    const int cbase = tig * (D / 4) + wi * (32 / KB);
+    ca = cbase + e;
+    cb = cbase + e + (KB == 4 ? 4 : (KB == 2 ? 8 : 2));
+  }
+}
+
+// Code pairs of one 2/4/8-bit key word in key_pair_channels order.
 template <int KB>
 __device__ __forceinline__ void k_word_pairs(uint32_t w, uint32_t* e) {
   if constexpr (KB == 4) {
@@ -100,11 +176,56 @@ __device__ __forceinline__ void k_word_pairs(uint32_t w, uint32_t* e) {
   }
 }
 
-// Channel pair (ca, cb) of pair e of a key word starting at channel cbase.
-template <int KB>
-__device__ __forceinline__ void k_pair_channels(int cbase, int e, int& ca, int& cb) {
-  ca = cbase + e;
-  cb = cbase + e + (KB == 4 ? 4 : (KB == 2 ? 8 : 2));
+// Five 3-bit fields at bits 0,3,..,12 of the low halves of two words:
+// returns (field_i of a, field_i of b) for i = 0..4, exact.
+__device__ __forceinline__ void lo5(uint32_t a, uint32_t b, uint32_t* e) {
+  const uint32_t z = prmt(a, b, 0x5410u);
+  const uint32_t z9 = z >> 9;
+  e[0] = magic_fix(and_or(z, 0x00070007u, kMagic), 1.0f);
+  e[1] = magic_fix(and_or(z, 0x00380038u, kMagic), 1.0f / 8.0f);
+  e[2] = magic_fix(and_or(z, 0x01C001C0u, kMagic), 1.0f / 64.0f);
+  e[3] = magic_fix(and_or(z9, 0x00070007u, kMagic), 1.0f);
+  e[4] = magic_fix(and_or(z9, 0x00380038u, kMagic), 1.0f / 8.0f);
+}
+
+// 2-bit fields (bits 30..31) of two words as one pair.
+__device__ __forceinline__ uint32_t slot10_pair(uint32_t a, uint32_t b) {
+  return magic_fix(and_or(prmt(a >> 30, b >> 30, 0x5410u), 0x00030003u, kMagic), 1.0f);
+}
+
+// The thread's key pairs of one token row.
+template <int KB, int D>
+__device__ __forceinline__ void key_row_pairs(const uint32_t* row, int tig, uint32_t* E) {
+  using S = KeyShape<KB, D>;
+  if constexpr (KB == 3) {
+    uint32_t w[S::WT];
+#pragma unroll
+    for (int wi = 0; wi < S::WT; ++wi) {
+      const int wd = tig * S::WT + wi;
+      w[wi] = (wd < S::WK) ? row[wd] : 0u;
+    }
+#pragma unroll
+    for (int wi = 0; wi < S::WT; ++wi) {
+      // move fields 5..9 up one bit so field i and field i+5 sit 16 bits apart
+      const uint32_t x = (w[wi] & 0x7FFFu) | ((w[wi] << 1) & 0xFFFF0000u);
+      const uint32_t x9 = x >> 9;
+      E[5 * wi + 0] = magic_fix(and_or(x, 0x00070007u, kMagic), 1.0f);
+      E[5 * wi + 1] = magic_fix(and_or(x, 0x00380038u, kMagic), 1.0f / 8.0f);
+      E[5 * wi + 2] = magic_fix(and_or(x, 0x01C001C0u, kMagic), 1.0f / 64.0f);
+      E[5 * wi + 3] = magic_fix(and_or(x9, 0x00070007u, kMagic), 1.0f);
+      E[5 * wi + 4] = magic_fix(and_or(x9, 0x00380038u, kMagic), 1.0f / 8.0f);
+    }
+#pragma unroll
+    for (int k = 5 * S::WT; k < S::NPK; ++k) {
+      const int a = 2 * (k - 5 * S::WT), b = a + 1;
+      E[k] = (a < S::WT) ? slot10_pair(w[a], (b < S::WT) ? w[b] : 0u) : 0u;
+    }
+  } else {
+    uint32_t w[S::WT];
+    lds_words<S::WT>(w, row + tig * S::WT);
+#pragma unroll
+    for (int wi = 0; wi < S::WT; ++wi) k_word_pairs<KB>(w[wi], E + wi * S::PW);
+  }
 }
 
 // 2-bit field i (0..7) of both halves of x -> half2 of exact codes
@@ -123,7 +244,7 @@ __device__ __forceinline__ uint32_t f8(uint32_t z, int i) {
 }
 
 // Value code pairs for two tokens (a, b): H[c] = (code_a[c], code_b[c]) for the
-// D/8 channels this thread owns.  wa/wb hold the thread's slice of each row.
+// D/8 channels this thread owns (2/4/8-bit values).
 template <int VB, int D>
 __device__ __forceinline__ void v_pairs(const uint32_t* wa, const uint32_t* wb, uint32_t half_sel,
                                         uint32_t (&H)[D / 8]) {
@@ -162,23 +283,41 @@ __device__ __forceinline__ void v_pairs(const uint32_t* wa, const uint32_t* wb, 
   }
 }
 
-template <int N>
-__device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint32_t* p) {
-  if constexpr (N == 1) {
-    w[0] = p[0];
-  } else if constexpr (N == 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    w[0] = v.x;
-    w[1] = v.y;
+// Channel of row (g + 8*hi) of value m-tile mt in the quantized-path map, or -1.
+//  2/4/8-bit: thread g owns channels [g*D/8, (g+1)*D/8): row g -> g*D/8 + mt,
+//  row g+8 -> g*D/8 + D/16 + mt.
+//  3-bit, d128: thread g owns the 3-bit fields of word g (entries 0..9) and
+//  fields 5h..5h+4 of word 8 + g/2 (h = g & 1, entries 10..14); row g of tile
+//  mt is entry mt, row g+8 entry 8 + mt; tile 8 holds 2-bit fields (word g,
+//  and word 8 + g/2 for even g while that word has one).
+//  3-bit, d64: thread g < 6 owns the 3-bit fields of word g (entries 0..9);
+//  row g of tile mt is entry mt, row g+8 entry 5 + mt; tile 5 holds the 2-bit
+//  field of word g < 5 in row g.
+template <int VB, int D>
+__device__ __forceinline__ int vq_channel(int g, int mt, int hi) {
+  if constexpr (VB != 3) {
+    return g * (D / 8) + (hi ? D / 16 : 0) + mt;
   } else {
-#pragma unroll
-    for (int i = 0; i < N; i += 4) {
-      const uint4 v = *reinterpret_cast<const uint4*>(p + i);
-      w[i] = v.x;
-      w[i + 1] = v.y;
-      w[i + 2] = v.z;
-      w[i + 3] = v.w;
+    constexpr int MT3 = ValShape<VB, D>::MT3;
+    if (mt == MT3) {
+      if (!hi) return (D == 128 || g < 5) ? 11 * g + 10 : -1;
+      if (D == 128) {
+        const int wb = 8 + (g >> 1);
+        return ((g & 1) == 0 && wb <= 10) ? 11 * wb + 10 : -1;
+      }
+      return -1;
     }
+    const int e = hi ? MT3 + mt : mt;
+    int c;
+    if (D == 128) {
+      if (e < 10) c = 11 * g + e;
+      else if (e < 15) c = 11 * (8 + (g >> 1)) + 5 * (g & 1) + (e - 10);
+      else return -1;
+    } else {
+      if (g >= 6) return -1;
+      c = 11 * g + e;
+    }
+    return c < D ? c : -1;
   }
 }
 
@@ -189,23 +328,33 @@ __device__ __forceinline__ float reduce_over_g(float v) {
   return v;
 }
 
+// fp16 hi + lo split of two fp32 values, as (hi pair, lo pair)
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  hi = h2_as_u32(h);
+  lo = h2_as_u32(__floats2half2_rn(a - __low2float(h), b - __high2float(h)));
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int KB, int VB, int D, int NT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
-  constexpr int NP = D / 8;      // key pairs per token row per thread = value channels per thread
-  constexpr int KS = D / 16;     // k-steps of q.K^T = channel m-tiles of p.V
-  constexpr int WK = D * KB / 32;
-  constexpr int WT = WK / 4;     // key words per thread per row
-  constexpr int PW = 16 / KB;    // pairs per key word
-  constexpr int WV = D * VB / 32;
-  constexpr int VW = (D * VB / 256) > 0 ? (D * VB / 256) : 1;  // value words per thread per row
-  constexpr int H = 4 * NT;      // padded query heads
-  constexpr int QPS = NT * NP + 4;
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(DecodeParams p) {
+  using KS_ = KeyShape<KB, D>;
+  using VS_ = ValShape<VB, D>;
+  constexpr int KS = D / 16;            // residual k-steps / channel m-tiles
+  constexpr int KSK = KS_::KSK;         // quantized score k-steps
+  constexpr int NPK = KS_::NPK;         // key pairs per thread per row
+  constexpr int WK = KS_::WK;
+  constexpr int WV = VS_::WV;
+  constexpr int MTV = VS_::MTV;         // value m-tiles (quantized map)
+  constexpr int MTA = MTV > KS ? MTV : KS;
+  constexpr int NP = D / 8;
+  constexpr int H = 4 * NT;             // padded query heads
+  constexpr int QPS = NT * NPK + 4;
   constexpr int QRS = NT * KS * 2 + 4;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  const DecodeSmem L = decode_smem_layout(D, NT, p.rec_bytes);
+  const DecodeSmem L = decode_smem_layout(D, NT, p.G, p.rec_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
   __half* qs = reinterpret_cast<__half*>(smem + L.off_qs);
   uint32_t* qp_tab = reinterpret_cast<uint32_t*>(smem + L.off_qp);
@@ -215,94 +364,133 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   float* dm = reinterpret_cast<float*>(smem + L.off_dm);
   int* flags = reinterpret_cast<int*>(smem + L.off_flags);
   float* wo = reinterpret_cast<float*>(smem + L.off_wo);
-  float* dump = reinterpret_cast<float*>(smem + L.off_dump);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tig = lane & 3, part = g & 1;
 
   // ---------------- state and this CTA's share of the work
-  const int64_t T = __ldcg(p.tokens);
+  const int T = __ldcg(p.tokens);
   if (T <= 0) return;
-  const int64_t nq = quantized_after(T, p.R, p.G);
-  const int64_t r = T - nq;
-  const int64_t NG = nq / p.G;
-  const int64_t NRT = (r + kResTile - 1) / kResTile;
-  const int64_t NI = NG + NRT;
-  const int64_t cq = p.rec_bytes, cr = static_cast<int64_t>(kResTile) * 4 * D;
-  const int64_t Cu = NG * cq + NRT * cr;
+  const int nq = static_cast<int>(quantized_after(T, p.R, p.G));
+  const int r = T - nq;
+  const int NS = p.G / kSlice;            // slices per key group
+  const int NG = (nq / p.G) * NS;         // quantized work items (slices)
+  const int NRT = (r + kResTile - 1) / kResTile;
+  const int NI = NG + NRT;
+  const int cq = slice_bytes(D, p.G, p.rec_bytes), cr = kResTile * 4 * D;
+  const int64_t Cu = static_cast<int64_t>(NG) * cq + static_cast<int64_t>(NRT) * cr;
   const int64_t C = static_cast<int64_t>(p.units) * Cu;
   const int64_t maxc = (NRT > 0 && cr > cq) || NG == 0 ? cr : cq;
-  int64_t peff = C / maxc;
-  if (peff < 1) peff = 1;
-  if (peff > p.grid) peff = p.grid;
-  const int64_t pid = blockIdx.x;
+  int64_t peff64 = C / maxc;
+  if (peff64 < 1) peff64 = 1;
+  if (peff64 > p.grid) peff64 = p.grid;
+  const int peff = static_cast<int>(peff64);
+  const int pid = blockIdx.x;
   if (pid >= peff) return;
 
-  auto item_start = [&](int64_t f) -> int64_t {
-    const int64_t u = f / NI, i = f % NI;
-    return u * Cu + (i < NG ? i * cq : NG * cq + (i - NG) * cr);
+  auto item_start = [&](int f) -> int64_t {
+    const int u = f / NI, i = f - u * NI;
+    return u * Cu + (i < NG ? static_cast<int64_t>(i) * cq
+                            : static_cast<int64_t>(NG) * cq + static_cast<int64_t>(i - NG) * cr);
   };
-  auto first_item_at = [&](int64_t x) -> int64_t {  // first flat item starting at or after x
+  auto first_item_at = [&](int64_t x) -> int {  // first flat item starting at or after x
     const int64_t u = x / Cu, o = x - u * Cu;
     int64_t i;
     if (o == 0) {
       i = 0;
-    } else if (NG > 0 && o <= (NG - 1) * cq) {
+    } else if (NG > 0 && o <= static_cast<int64_t>(NG - 1) * cq) {
       i = (o + cq - 1) / cq;
-    } else if (o <= NG * cq) {
+    } else if (o <= static_cast<int64_t>(NG) * cq) {
       i = NG;
     } else {
-      i = NG + (o - NG * cq + cr - 1) / cr;
+      i = NG + (o - static_cast<int64_t>(NG) * cq + cr - 1) / cr;
     }
-    return u * NI + i;
+    return static_cast<int>(u * NI + i);
   };
-  auto owner = [&](int64_t f) -> int64_t { return (item_start(f) * peff) / C; };
-  const int64_t f0 = first_item_at((pid * C + peff - 1) / peff);
-  const int64_t f1 = first_item_at(((pid + 1) * C + peff - 1) / peff);
+  auto owner = [&](int f) -> int { return static_cast<int>((item_start(f) * peff) / C); };
+  const int f0 = first_item_at((static_cast<int64_t>(pid) * C + peff - 1) / peff);
+  const int f1 = first_item_at((static_cast<int64_t>(pid + 1) * C + peff - 1) / peff);
 
-  // ---------------- pipeline setup (warp-private stages)
-  uint8_t* stage_base = smem + warp * kStages * L.stage_bytes;
-  uint64_t* wbar = bars + warp * kStages;
+  // ---------------- per-warp ring of staged items (kSlots copies in flight)
+  uint8_t* ring = smem + warp * L.ring;
+  uint64_t* wbar = bars + warp * kSlots;
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&wbar[s], 1);
+    for (int s = 0; s < kSlots; ++s) mbar_init(&wbar[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
-
-  auto issue = [&](int64_t f, int st) {
-    const int64_t u = f / NI, i = f % NI;
-    uint8_t* dst = stage_base + st * L.stage_bytes;
-    fence_proxy_async_smem();
-    if (i < NG) {
-      mbar_arrive_expect_tx(&wbar[st], static_cast<uint32_t>(p.rec_bytes));
-      bulk_g2s(dst, p.records + u * p.unit_rec_stride + i * p.rec_bytes, static_cast<uint32_t>(p.rec_bytes),
-               &wbar[st]);
-    } else {
-      const int64_t k = i - NG;
-      const int64_t slot0 = (nq + k * kResTile) % p.R;
-      const uint32_t bytes = kResTile * D * 2;
-      mbar_arrive_expect_tx(&wbar[st], 2 * bytes);
-      bulk_g2s(dst, p.res_k + u * p.res_stride + slot0 * D, bytes, &wbar[st]);
-      bulk_g2s(dst + bytes, p.res_v + u * p.res_stride + slot0 * D, bytes, &wbar[st]);
+  // Ring bookkeeping runs identically in every lane; lane 0 issues the copies.
+  int rhead = 0, rtail = 0, rend = 0, nin = 0, kiss = 0, kcon = 0;
+  bool wrapped = false;
+  auto item_bytes = [&](int f) -> int { return (f - (f / NI) * NI) < NG ? cq : cr; };
+  auto try_issue = [&]() {
+    while (nin < kSlots) {
+      const int f = f0 + warp + 4 * kiss;
+      if (f >= f1) break;
+      const int sz = item_bytes(f);
+      int off;
+      if (nin == 0) {
+        rhead = rtail = 0;
+        wrapped = false;
+        off = 0;
+      } else if (!wrapped) {
+        if (rhead + sz <= L.ring) {
+          off = rhead;
+        } else if (sz <= rtail) {
+          rend = rhead;
+          wrapped = true;
+          off = 0;
+        } else {
+          break;
+        }
+      } else {
+        if (rhead + sz <= rtail) off = rhead;
+        else break;
+      }
+      rhead = off + sz;
+      if (lane == 0) {
+        const int st = kiss % kSlots;
+        const int u = f / NI, i = f - u * NI;
+        uint8_t* dst = ring + off;
+        fence_proxy_async_smem();
+        if (i < NG) {
+          const uint8_t* rec = p.records + u * p.unit_rec_stride + static_cast<int64_t>(i / NS) * p.rec_bytes;
+          if (NS == 1) {
+            mbar_arrive_expect_tx(&wbar[st], static_cast<uint32_t>(p.rec_bytes));
+            bulk_g2s(dst, rec, static_cast<uint32_t>(p.rec_bytes), &wbar[st]);
+          } else {
+            const int t0 = (i % NS) * kSlice;
+            const uint32_t kbytes = kSlice * WK * 4, vbytes = kSlice * WV * 4;
+            mbar_arrive_expect_tx(&wbar[st], static_cast<uint32_t>(cq));
+            bulk_g2s(dst, rec + t0 * WK * 4, kbytes, &wbar[st]);
+            bulk_g2s(dst + kbytes, rec + p.G * WK * 4 + t0 * WV * 4, vbytes, &wbar[st]);
+            bulk_g2s(dst + kbytes + vbytes, rec + p.G * (WK + WV) * 4, 4 * D, &wbar[st]);
+            bulk_g2s(dst + kbytes + vbytes + 4 * D, rec + p.G * (WK + WV) * 4 + 4 * D + t0 * 4, 4 * kSlice,
+                     &wbar[st]);
+          }
+        } else {
+          const int slot0 = (nq + (i - NG) * kResTile) % p.R;
+          const uint32_t bytes = kResTile * D * 2;
+          mbar_arrive_expect_tx(&wbar[st], 2 * bytes);
+          bulk_g2s(dst, p.res_k + u * p.res_stride + static_cast<int64_t>(slot0) * D, bytes, &wbar[st]);
+          bulk_g2s(dst + bytes, p.res_v + u * p.res_stride + static_cast<int64_t>(slot0) * D, bytes, &wbar[st]);
+        }
+      }
+      ++nin;
+      ++kiss;
     }
   };
-
-  int64_t k_item = 0;  // this warp's item counter
-  if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      const int64_t f = f0 + warp + 4 * s;
-      if (f < f1) issue(f, s);
-    }
-  }
+  try_issue();
 
   const __half2 negmask = part ? __float2half2_rn(-1.0f) : __float2half2_rn(0.0f);
   const float alpha = p.alpha;
   const uint32_t vhalf_sel = (g & 1) ? 0x7632u : 0x5410u;  // 2-bit values, D = 64
-  const int64_t u_first = f0 / NI, u_last = (f1 - 1) / NI;
+  const int u_first = f0 / NI, u_last = (f1 - 1) / NI;
+  bool failed = false;
 
-  for (int64_t u = u_first; u <= u_last; ++u) {
-    const int64_t seg_hi = ((u + 1) * NI < f1) ? (u + 1) * NI : f1;
-    const int b = static_cast<int>(u / p.kv_heads), kvh = static_cast<int>(u % p.kv_heads);
+  for (int u = u_first; u <= u_last; ++u) {
+    const int seg_hi = ((u + 1) * NI < f1) ? (u + 1) * NI : f1;
+    const int b = u / p.kv_heads, kvh = u - b * p.kv_heads;
 
     // ---------------- per-unit query tables
     for (int idx = tid; idx < H * D / 2; idx += kThreads) {
@@ -321,11 +509,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + (g >> 1);
         const bool live = h < p.gqa;
-        for (int pi = 0; pi < NP; ++pi) {
-          const int wi = pi / PW, e = pi % PW;
+        for (int pi = 0; pi < NPK; ++pi) {
           int ca, cb;
-          k_pair_channels<KB>(tig * (D / 4) + wi * (32 / KB), e, ca, cb);
-          qp[j * NP + pi] = live ? h2_as_u32(__halves2half2(qs[h * D + ca], qs[h * D + cb])) : 0u;
+          key_pair_channels<KB, D>(tig, pi, ca, cb);
+          const __half z0 = __float2half(0.0f);
+          const __half qa = (live && ca >= 0) ? qs[h * D + ca] : z0;
+          const __half qb = (live && cb >= 0) ? qs[h * D + cb] : z0;
+          qp[j * NPK + pi] = h2_as_u32(__halves2half2(qa, qb));
         }
         for (int kk = 0; kk < KS; ++kk) {
           for (int rr = 0; rr < 2; ++rr) {
@@ -340,26 +530,26 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
 
     // ---------------- warp state for this unit
     float m[NT], l[NT], vb[NT];
-    float acc[KS][NT][4];
+    float acc[MTA][NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       m[j] = -INFINITY;
       l[j] = 0.0f;
       vb[j] = 0.0f;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt)
+      for (int mt = 0; mt < MTA; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.0f;
     }
     bool has_q = false, in_res = false, dumped = false;
 
-    // online-softmax update for one tile of 16 tokens (scores already scaled)
-    auto softmax_tile = [&](float (&sa)[NT], float (&sb)[NT]) {
+    // online-softmax update: tmax = max of this tile's scaled scores per head
+    auto softmax_update = [&](const float (&tmax_in)[NT]) {
       float tmax[NT];
       bool need = false;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        float t = fmaxf(sa[j], sb[j]);
+        float t = tmax_in[j];
         t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 4));
         t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
         t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
@@ -375,193 +565,257 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
           l[j] *= f;
           vb[j] *= f;
 #pragma unroll
-          for (int mt = 0; mt < KS; ++mt)
+          for (int mt = 0; mt < MTA; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mt][j][e] *= f;
         }
       }
     };
 
-    while (true) {
-      const int64_t f = f0 + warp + 4 * k_item;
-      if (f >= seg_hi) break;
-      const int st = static_cast<int>(k_item % kStages);
-      const uint32_t ph = static_cast<uint32_t>((k_item / kStages) & 1);
-      if (!mbar_wait(&wbar[st], ph, p.err)) return;
-      const uint8_t* stg = stage_base + st * L.stage_bytes;
-      const int64_t i = f % NI;
+    // PV B fragments from (p~ of rows g, g+8) pairs: the thread's column is
+    // (head 4j + g/2, hi or lo); tokens come from lanes srcA and srcA + dB
+    auto pv_b = [&](uint32_t hi, uint32_t lo, int srcA, int dB, uint32_t& b01, uint32_t& b23) {
+      const uint32_t xh = __shfl_sync(0xffffffffu, hi, srcA);
+      const uint32_t yh = __shfl_sync(0xffffffffu, hi, srcA + dB);
+      const uint32_t xl = __shfl_sync(0xffffffffu, lo, srcA);
+      const uint32_t yl = __shfl_sync(0xffffffffu, lo, srcA + dB);
+      const uint32_t x = part ? xl : xh, y = part ? yl : yh;
+      b01 = prmt(x, y, 0x5410u);
+      b23 = prmt(x, y, 0x7632u);
+    };
 
-      if (i < NG) {
-        // ============ quantized group
+    while (true) {
+      const int f = f0 + warp + 4 * kcon;
+      if (f >= seg_hi) break;
+      const int st = kcon % kSlots;
+      const uint32_t ph = static_cast<uint32_t>((kcon / kSlots) & 1);
+      if (!failed && !mbar_wait(&wbar[st], ph, p.err)) failed = true;
+      const uint8_t* stg = ring + rtail;
+      const int i = f - (f / NI) * NI;
+
+      if (failed) {
+        // a copy never landed: skip the work, keep the control flow
+      } else if (i < NG) {
+        // ============ quantized slice of a key group (32 tokens)
         has_q = true;
         const uint32_t* Kc = reinterpret_cast<const uint32_t*>(stg);
-        const uint32_t* Vc = Kc + p.G * WK;
-        const __half* Ks = reinterpret_cast<const __half*>(Vc + p.G * WV);
+        const uint32_t* Vc = Kc + kSlice * WK;
+        const __half* Ks = reinterpret_cast<const __half*>(Vc + kSlice * WV);
         const __half* Kz = Ks + D;
         const __half2* Vsz = reinterpret_cast<const __half2*>(Kz + D);
 
-        uint32_t qp[NT][NP];
+        uint32_t qp[NT][NPK];
         {
           const uint32_t* src = qp_tab + lane * QPS;
 #pragma unroll
           for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int pi = 0; pi < NP; pi += 4) {
-              const uint4 v = *reinterpret_cast<const uint4*>(src + j * NP + pi);
+            for (int pi = 0; pi < NPK; pi += 2) {
+              const uint2 v = *reinterpret_cast<const uint2*>(src + j * NPK + pi);
               qp[j][pi] = v.x;
               qp[j][pi + 1] = v.y;
-              qp[j][pi + 2] = v.z;
-              qp[j][pi + 3] = v.w;
             }
         }
-        // zero pairs -> bias = sum_c q_c z_c, one MMA per k-step (zeros broadcast over rows)
-        float bias[NT];
-        {
-          uint32_t zn[NP];
+        // zero and scale pairs in key-pair order
+        uint32_t zp[NPK], sp[NPK];
+        if constexpr (KB == 3) {
+#pragma unroll
+          for (int pi = 0; pi < NPK; ++pi) {
+            int ca, cb;
+            key_pair_channels<KB, D>(tig, pi, ca, cb);
+            const __half h0 = __float2half(0.0f);
+            zp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Kz[ca] : h0, cb >= 0 ? Kz[cb] : h0));
+            sp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Ks[ca] : h0, cb >= 0 ? Ks[cb] : h0));
+          }
+        } else {
+          constexpr int PW = KS_::PW;
+          uint32_t zn[NPK], sn[NPK];
           const uint32_t* zsrc = reinterpret_cast<const uint32_t*>(Kz + tig * (D / 4));
-#pragma unroll
-          for (int pi = 0; pi < NP; pi += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(zsrc + pi);
-            zn[pi] = v.x;
-            zn[pi + 1] = v.y;
-            zn[pi + 2] = v.z;
-            zn[pi + 3] = v.w;
-          }
-          uint32_t zp[NP];
-#pragma unroll
-          for (int wi = 0; wi < WT; ++wi) {
-            const uint32_t* nn = zn + wi * PW;  // natural pairs of this word's channels
-            uint32_t* oo = zp + wi * PW;
-            if constexpr (KB == 4) {
-              oo[0] = prmt(nn[0], nn[2], 0x5410u);
-              oo[1] = prmt(nn[0], nn[2], 0x7632u);
-              oo[2] = prmt(nn[1], nn[3], 0x5410u);
-              oo[3] = prmt(nn[1], nn[3], 0x7632u);
-            } else if constexpr (KB == 2) {
-#pragma unroll
-              for (int kq = 0; kq < 4; ++kq) {
-                oo[2 * kq] = prmt(nn[kq], nn[kq + 4], 0x5410u);
-                oo[2 * kq + 1] = prmt(nn[kq], nn[kq + 4], 0x7632u);
-              }
-            } else {
-              oo[0] = prmt(nn[0], nn[1], 0x5410u);
-              oo[1] = prmt(nn[0], nn[1], 0x7632u);
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk)
-              mma_16816(c, zp[2 * kk], zp[2 * kk], zp[2 * kk + 1], zp[2 * kk + 1], qp[j][2 * kk], qp[j][2 * kk + 1]);
-            bias[j] = c[0];
-          }
-        }
-        // folded query q~ = q * s, hi part in even columns, lo part in odd ones
-        uint32_t bq[NT][NP];
-        {
-          uint32_t sn[NP];
           const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(Ks + tig * (D / 4));
 #pragma unroll
-          for (int pi = 0; pi < NP; pi += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(ssrc + pi);
-            sn[pi] = v.x;
-            sn[pi + 1] = v.y;
-            sn[pi + 2] = v.z;
-            sn[pi + 3] = v.w;
+          for (int pi = 0; pi < NPK; pi += 4) {
+            const uint4 vz = *reinterpret_cast<const uint4*>(zsrc + pi);
+            const uint4 vs = *reinterpret_cast<const uint4*>(ssrc + pi);
+            zn[pi] = vz.x; zn[pi + 1] = vz.y; zn[pi + 2] = vz.z; zn[pi + 3] = vz.w;
+            sn[pi] = vs.x; sn[pi + 1] = vs.y; sn[pi + 2] = vs.z; sn[pi + 3] = vs.w;
           }
 #pragma unroll
-          for (int wi = 0; wi < WT; ++wi) {
-            const uint32_t* nn = sn + wi * PW;
-            uint32_t sp[PW];
+          for (int wi = 0; wi < KS_::WT; ++wi) {
+            const uint32_t* nz = zn + wi * PW;
+            const uint32_t* ns = sn + wi * PW;
+            uint32_t* oz = zp + wi * PW;
+            uint32_t* os = sp + wi * PW;
             if constexpr (KB == 4) {
-              sp[0] = prmt(nn[0], nn[2], 0x5410u);
-              sp[1] = prmt(nn[0], nn[2], 0x7632u);
-              sp[2] = prmt(nn[1], nn[3], 0x5410u);
-              sp[3] = prmt(nn[1], nn[3], 0x7632u);
+              oz[0] = prmt(nz[0], nz[2], 0x5410u); oz[1] = prmt(nz[0], nz[2], 0x7632u);
+              oz[2] = prmt(nz[1], nz[3], 0x5410u); oz[3] = prmt(nz[1], nz[3], 0x7632u);
+              os[0] = prmt(ns[0], ns[2], 0x5410u); os[1] = prmt(ns[0], ns[2], 0x7632u);
+              os[2] = prmt(ns[1], ns[3], 0x5410u); os[3] = prmt(ns[1], ns[3], 0x7632u);
             } else if constexpr (KB == 2) {
 #pragma unroll
               for (int kq = 0; kq < 4; ++kq) {
-                sp[2 * kq] = prmt(nn[kq], nn[kq + 4], 0x5410u);
-                sp[2 * kq + 1] = prmt(nn[kq], nn[kq + 4], 0x7632u);
+                oz[2 * kq] = prmt(nz[kq], nz[kq + 4], 0x5410u);
+                oz[2 * kq + 1] = prmt(nz[kq], nz[kq + 4], 0x7632u);
+                os[2 * kq] = prmt(ns[kq], ns[kq + 4], 0x5410u);
+                os[2 * kq + 1] = prmt(ns[kq], ns[kq + 4], 0x7632u);
               }
             } else {
-              sp[0] = prmt(nn[0], nn[1], 0x5410u);
-              sp[1] = prmt(nn[0], nn[1], 0x7632u);
+              oz[0] = prmt(nz[0], nz[1], 0x5410u); oz[1] = prmt(nz[0], nz[1], 0x7632u);
+              os[0] = prmt(ns[0], ns[1], 0x5410u); os[1] = prmt(ns[0], ns[1], 0x7632u);
             }
+          }
+        }
+        // bias = sum_c q_c z_c: MMAs with the zeros broadcast over rows (two chains)
+        float bias[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < KSK; ++kk)
+            mma_16816((kk & 1) ? c1 : c0, zp[2 * kk], zp[2 * kk], zp[2 * kk + 1], zp[2 * kk + 1], qp[j][2 * kk],
+                      qp[j][2 * kk + 1]);
+          bias[j] = c0[0] + c1[0];
+        }
+        // folded query q~ = q * s: hi part in even columns, lo part in odd ones
+        uint32_t bq[NT][NPK];
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int pi = 0; pi < NPK; ++pi) {
+            if constexpr (KB == 3) {
+              // fp32 products: the 2-bit fields use s2 = (s*7)/3 (an fp32 value)
+              int ca, cb;
+              key_pair_channels<KB, D>(tig, pi, ca, cb);
+              const float2 qf = __half22float2(u32_as_h2(qp[j][pi]));
+              float2 sf = __half22float2(u32_as_h2(sp[pi]));
+              if (ca >= 0 && ca % 11 == 10) sf.x = __fdiv_rn(__fmul_rn(sf.x, 7.0f), 3.0f);
+              if (cb >= 0 && cb % 11 == 10) sf.y = __fdiv_rn(__fmul_rn(sf.y, 7.0f), 3.0f);
+              uint32_t hi, lo;
+              split_pair(qf.x * sf.x, qf.y * sf.y, hi, lo);
+              bq[j][pi] = part ? lo : hi;
+            } else {
+              const __half2 qq = u32_as_h2(qp[j][pi]);
+              const __half2 ss = u32_as_h2(sp[pi]);
+              const __half2 hi = __hmul2(qq, ss);
+              bq[j][pi] = h2_as_u32(__hfma2(qq, ss, __hmul2(hi, negmask)));
+            }
+          }
+
+        // ---- scores of the slice's 32 tokens: tiles 0 (tokens 0..15) and 1 (16..31);
+        // rows g and g+8 of each; two accumulator chains per tile
+        float sc[2][NT][4];
+        {
+          float sx[2][NT][4];
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              sc[t][j][0] = bias[j]; sc[t][j][1] = 0.0f; sc[t][j][2] = bias[j]; sc[t][j][3] = 0.0f;
+              sx[t][j][0] = 0.0f; sx[t][j][1] = 0.0f; sx[t][j][2] = 0.0f; sx[t][j][3] = 0.0f;
+            }
+          uint32_t e[4][NPK];
+#pragma unroll
+          for (int rw = 0; rw < 4; ++rw) key_row_pairs<KB, D>(Kc + (8 * rw + g) * WK, tig, e[rw]);
+#pragma unroll
+          for (int kk = 0; kk < KSK; ++kk)
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+              for (int j = 0; j < NT; ++j)
+                mma_16816((kk & 1) ? sx[t][j] : sc[t][j], e[2 * t][2 * kk], e[2 * t + 1][2 * kk],
+                          e[2 * t][2 * kk + 1], e[2 * t + 1][2 * kk + 1], bq[j][2 * kk], bq[j][2 * kk + 1]);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
-              for (int e = 0; e < PW; ++e) {
-                const __half2 qq = u32_as_h2(qp[j][wi * PW + e]);
-                const __half2 ss = u32_as_h2(sp[e]);
-                const __half2 hi = __hmul2(qq, ss);
-                bq[j][wi * PW + e] = h2_as_u32(__hfma2(qq, ss, __hmul2(hi, negmask)));
-              }
-          }
+              for (int q4 = 0; q4 < 4; ++q4) sc[t][j][q4] += sx[t][j][q4];
         }
-
-        for (int t0 = 0; t0 < p.G; t0 += 16) {
-          // ---- scores for tokens t0+g (row g) and t0+g+8 (row g+8)
-          float sc[NT][4];
+        // scaled scores: s[t][j][0] token 16t+g, [1] token 16t+g+8
+        float s[2][NT][2];
+        float tmax[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            s[t][j][0] = (sc[t][j][0] + sc[t][j][1]) * alpha;
+            s[t][j][1] = (sc[t][j][2] + sc[t][j][3]) * alpha;
+          }
+          tmax[j] = fmaxf(fmaxf(s[0][j][0], s[0][j][1]), fmaxf(s[1][j][0], s[1][j][1]));
+        }
+        softmax_update(tmax);
+        float2 sz[2][2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          sz[t][0] = __half22float2(Vsz[16 * t + g]);
+          sz[t][1] = __half22float2(Vsz[16 * t + g + 8]);
+        }
+        const int srcA = 4 * tig + (g >> 1);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint32_t b01[NT], b23[NT], c01[NT], c23[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            sc[j][0] = bias[j];
-            sc[j][1] = 0.0f;
-            sc[j][2] = bias[j];
-            sc[j][3] = 0.0f;
-          }
-          {
-            uint32_t k0[WT], k1[WT];
-            lds_words<WT>(k0, Kc + (t0 + g) * WK + tig * WT);
-            lds_words<WT>(k1, Kc + (t0 + g + 8) * WK + tig * WT);
-#pragma unroll
-            for (int wi = 0; wi < WT; ++wi) {
-              uint32_t e0[PW], e1[PW];
-              k_word_pairs<KB>(k0[wi], e0);
-              k_word_pairs<KB>(k1[wi], e1);
-#pragma unroll
-              for (int e = 0; e < PW; e += 2)
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-                  mma_16816(sc[j], e0[e], e1[e], e0[e + 1], e1[e + 1], bq[j][wi * PW + e], bq[j][wi * PW + e + 1]);
+            const float pa = exp2f(s[t][j][0] - m[j]), pb = exp2f(s[t][j][1] - m[j]);
+            l[j] += pa + pb;
+            vb[j] = fmaf(pa, sz[t][0].y, fmaf(pb, sz[t][1].y, vb[j]));
+            uint32_t hi, lo;
+            split_pair(pa * sz[t][0].x, pb * sz[t][1].x, hi, lo);
+            pv_b(hi, lo, srcA, 16, b01[j], b23[j]);  // tokens (tig, tig+4 | tig+8, tig+12)
+            if constexpr (VB == 3) {
+              const float s2a = __fdiv_rn(__fmul_rn(sz[t][0].x, 7.0f), 3.0f);
+              const float s2b = __fdiv_rn(__fmul_rn(sz[t][1].x, 7.0f), 3.0f);
+              split_pair(pa * s2a, pb * s2b, hi, lo);
+              pv_b(hi, lo, srcA, 16, c01[j], c23[j]);
             }
           }
-          float sa[NT], sb[NT];
+          // ---- p~.V over tokens 16t + (tig, tig+4 | tig+8, tig+12), rows = channels
+          const int tb = 16 * t;
+          if constexpr (VB == 3) {
+            constexpr int MT3 = VS_::MT3;
+            constexpr int NE = 2 * MT3;
+            uint32_t wa[4], wbw[4];
+            const int wA = (D == 128) ? g : (g < 6 ? g : 0);
+            const int wB = 8 + (g >> 1);
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            sa[j] = (sc[j][0] + sc[j][1]) * alpha;
-            sb[j] = (sc[j][2] + sc[j][3]) * alpha;
-          }
-          softmax_tile(sa, sb);
-          const float2 sza = __half22float2(Vsz[t0 + g]);
-          const float2 szb = __half22float2(Vsz[t0 + g + 8]);
-          uint32_t b01[NT], b23[NT];
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint32_t* row = Vc + (tb + tig + 4 * q4) * WV;
+              wa[q4] = (D == 128 || g < 6) ? row[wA] : 0u;
+              wbw[q4] = (D == 128) ? row[wB] : 0u;
+            }
+            const int hsh = 15 * (g & 1);
+            uint32_t h01[NE], h23[NE], t01[2], t23[2];
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const float pa = exp2f(sa[j] - m[j]), pb = exp2f(sb[j] - m[j]);
-            l[j] += pa + pb;
-            vb[j] = fmaf(pa, sza.y, fmaf(pb, szb.y, vb[j]));
-            const float ta = pa * sza.x, tb = pb * szb.x;
-            const __half2 hi = __floats2half2_rn(ta, tb);
-            const __half2 lo = __floats2half2_rn(ta - __low2float(hi), tb - __high2float(hi));
-            const int srcA = 4 * tig + (g >> 1), srcB = srcA + 16;
-            const uint32_t xh = __shfl_sync(0xffffffffu, h2_as_u32(hi), srcA);
-            const uint32_t yh = __shfl_sync(0xffffffffu, h2_as_u32(hi), srcB);
-            const uint32_t xl = __shfl_sync(0xffffffffu, h2_as_u32(lo), srcA);
-            const uint32_t yl = __shfl_sync(0xffffffffu, h2_as_u32(lo), srcB);
-            const uint32_t x = part ? xl : xh, y = part ? yl : yh;
-            b01[j] = prmt(x, y, 0x5410u);  // tokens tig, tig+4
-            b23[j] = prmt(x, y, 0x7632u);  // tokens tig+8, tig+12
-          }
-          // ---- p~.V over tokens (tig, tig+4 | tig+8, tig+12), rows = channels
-          {
+            for (int pr = 0; pr < 2; ++pr) {
+              uint32_t* Hh = pr ? h23 : h01;
+              uint32_t* T2 = pr ? t23 : t01;
+              const uint32_t a0 = wa[2 * pr], a1 = wa[2 * pr + 1];
+              lo5(a0, a1, Hh);
+              lo5(a0 >> 15, a1 >> 15, Hh + 5);
+              T2[0] = (D == 128 || g < 5) ? slot10_pair(a0, a1) : 0u;
+              if constexpr (D == 128) {
+                const uint32_t b0 = wbw[2 * pr], b1 = wbw[2 * pr + 1];
+                lo5(b0 >> hsh, b1 >> hsh, Hh + 10);
+                Hh[15] = 0u;
+                T2[1] = ((g & 1) == 0 && wB <= 10) ? slot10_pair(b0, b1) : 0u;
+              } else {
+                T2[1] = 0u;
+              }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT3; ++mt)
+#pragma unroll
+              for (int j = 0; j < NT; ++j)
+                mma_16816(acc[mt][j], h01[mt], h01[MT3 + mt], h23[mt], h23[MT3 + mt], b01[j], b23[j]);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) mma_16816(acc[MT3][j], t01[0], t01[1], t23[0], t23[1], c01[j], c23[j]);
+          } else {
+            constexpr int VW = VS_::VW;
             const int voff = (VB == 2 && D == 64) ? (g >> 1) : g * VW;
             uint32_t w0[VW], w1[VW], w2[VW], w3[VW];
-            lds_words<VW>(w0, Vc + (t0 + tig) * WV + voff);
-            lds_words<VW>(w1, Vc + (t0 + tig + 4) * WV + voff);
-            lds_words<VW>(w2, Vc + (t0 + tig + 8) * WV + voff);
-            lds_words<VW>(w3, Vc + (t0 + tig + 12) * WV + voff);
+            lds_words<VW>(w0, Vc + (tb + tig) * WV + voff);
+            lds_words<VW>(w1, Vc + (tb + tig + 4) * WV + voff);
+            lds_words<VW>(w2, Vc + (tb + tig + 8) * WV + voff);
+            lds_words<VW>(w3, Vc + (tb + tig + 12) * WV + voff);
             uint32_t h01[NP], h23[NP];
             v_pairs<VB, D>(w0, w1, vhalf_sel, h01);
             v_pairs<VB, D>(w2, w3, vhalf_sel, h23);
@@ -576,20 +830,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         // ============ residual tile: 16 FP16 tokens (chunk-swizzled rows)
         if (!in_res) {
           if (has_q) {
-            // park the quantized-token part (channel map of the quantized path)
+            // park the quantized-token part (quantized channel map) in wo
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
               const float vbt = reduce_over_g(vb[j]);
               vb[j] = 0.0f;
               const int h = 4 * j + tig;
-              float* dd = dump + (warp * H + h) * D;
+              float* dd = wo + (warp * H + h) * D;
 #pragma unroll
-              for (int mt = 0; mt < KS; ++mt) {
-                dd[g * NP + mt] = acc[mt][j][0] + acc[mt][j][1] + vbt;
-                dd[g * NP + KS + mt] = acc[mt][j][2] + acc[mt][j][3] + vbt;
+              for (int mt = 0; mt < MTV; ++mt) {
+                const int c0 = vq_channel<VB, D>(g, mt, 0), c1 = vq_channel<VB, D>(g, mt, 1);
+                if (c0 >= 0) dd[c0] = acc[mt][j][0] + acc[mt][j][1] + vbt;
+                if (c1 >= 0) dd[c1] = acc[mt][j][2] + acc[mt][j][3] + vbt;
+              }
+#pragma unroll
+              for (int mt = 0; mt < MTA; ++mt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.0f;
-              }
               if (g == 0) dm[warp * H + h] = m[j];
             }
             dumped = true;
@@ -598,15 +855,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         }
         const __half* Kr = reinterpret_cast<const __half*>(stg);
         const __half* Vr = Kr + kResTile * D;
-        const int64_t kt = i - NG;
-        const int64_t left = r - kt * kResTile;
-        const int vt = left < kResTile ? static_cast<int>(left) : kResTile;
+        const int left = r - (i - NG) * kResTile;
+        const int vt = left < kResTile ? left : kResTile;
 
-        float sc[NT][4];
+        float sc[NT][4], sx[NT][4];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[j][e] = 0.0f;
+          for (int e = 0; e < 4; ++e) {
+            sc[j][e] = 0.0f;
+            sx[j][e] = 0.0f;
+          }
         const uint32_t* qrs = qr_tab + lane * QRS;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
@@ -616,30 +875,25 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
           ldsm_x4(a, Kr + tok * D + ((ch ^ (tok & 7)) * 8));
 #pragma unroll
           for (int j = 0; j < NT; ++j)
-            mma_16816(sc[j], a[0], a[1], a[2], a[3], qrs[(j * KS + kk) * 2], qrs[(j * KS + kk) * 2 + 1]);
+            mma_16816((kk & 1) ? sx[j] : sc[j], a[0], a[1], a[2], a[3], qrs[(j * KS + kk) * 2],
+                      qrs[(j * KS + kk) * 2 + 1]);
         }
-        float sa[NT], sb[NT];
+        float sa[NT], sb[NT], tmax[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          sa[j] = (g < vt) ? (sc[j][0] + sc[j][1]) * alpha : -INFINITY;
-          sb[j] = (g + 8 < vt) ? (sc[j][2] + sc[j][3]) * alpha : -INFINITY;
+          sa[j] = (g < vt) ? (sc[j][0] + sx[j][0] + sc[j][1] + sx[j][1]) * alpha : -INFINITY;
+          sb[j] = (g + 8 < vt) ? (sc[j][2] + sx[j][2] + sc[j][3] + sx[j][3]) * alpha : -INFINITY;
+          tmax[j] = fmaxf(sa[j], sb[j]);
         }
-        softmax_tile(sa, sb);
+        softmax_update(tmax);
         uint32_t b01[NT], b23[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           const float pa = exp2f(sa[j] - m[j]), pb = exp2f(sb[j] - m[j]);
           l[j] += pa + pb;
-          const __half2 hi = __floats2half2_rn(pa, pb);
-          const __half2 lo = __floats2half2_rn(pa - __low2float(hi), pb - __high2float(hi));
-          const int srcA = 8 * tig + (g >> 1), srcB = srcA + 4;
-          const uint32_t xh = __shfl_sync(0xffffffffu, h2_as_u32(hi), srcA);
-          const uint32_t yh = __shfl_sync(0xffffffffu, h2_as_u32(hi), srcB);
-          const uint32_t xl = __shfl_sync(0xffffffffu, h2_as_u32(lo), srcA);
-          const uint32_t yl = __shfl_sync(0xffffffffu, h2_as_u32(lo), srcB);
-          const uint32_t x = part ? xl : xh, y = part ? yl : yh;
-          b01[j] = prmt(x, y, 0x5410u);  // tokens 2tig, 2tig+1
-          b23[j] = prmt(x, y, 0x7632u);  // tokens 2tig+8, 2tig+9
+          uint32_t hi, lo;
+          split_pair(pa, pb, hi, lo);
+          pv_b(hi, lo, 8 * tig + (g >> 1), 4, b01[j], b23[j]);  // tokens (2tig, 2tig+1 | +8, +9)
         }
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
@@ -653,15 +907,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         }
       }
 
+      // release the consumed item's ring space, then refill
       __syncwarp();
-      if (lane == 0) {
-        const int64_t fn = f + 4 * kStages;
-        if (fn < f1) issue(fn, st);
+      {
+        const int sz = item_bytes(f);
+        --nin;
+        rtail += sz;
+        if (wrapped && rtail == rend) {
+          rtail = 0;
+          wrapped = false;
+        }
       }
-      ++k_item;
+      ++kcon;
+      try_issue();
     }
 
     // ---------------- warp -> shared memory
+    // (a parked quantized part, already in wo, is rescaled to the final max)
+    if (dumped) __syncwarp();
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const float lt = reduce_over_g(l[j]);
@@ -672,26 +935,31 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         wl[warp * H + h] = lt;
       }
       float* oo = wo + (warp * H + h) * D;
+      const float fd = dumped ? exp2f(dm[warp * H + h] - m[j]) : 0.0f;
+      if (in_res) {
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        if (in_res) {
-          oo[16 * mt + g] = acc[mt][j][0] + acc[mt][j][1];
-          oo[16 * mt + 8 + g] = acc[mt][j][2] + acc[mt][j][3];
-        } else {
-          oo[g * NP + mt] = acc[mt][j][0] + acc[mt][j][1] + vbt;
-          oo[g * NP + KS + mt] = acc[mt][j][2] + acc[mt][j][3] + vbt;
+        for (int mt = 0; mt < KS; ++mt) {
+          const float o0 = acc[mt][j][0] + acc[mt][j][1], o1 = acc[mt][j][2] + acc[mt][j][3];
+          oo[16 * mt + g] = dumped ? fmaf(oo[16 * mt + g], fd, o0) : o0;
+          oo[16 * mt + 8 + g] = dumped ? fmaf(oo[16 * mt + 8 + g], fd, o1) : o1;
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < MTV; ++mt) {
+          const int c0 = vq_channel<VB, D>(g, mt, 0), c1 = vq_channel<VB, D>(g, mt, 1);
+          if (c0 >= 0) oo[c0] = acc[mt][j][0] + acc[mt][j][1] + vbt;
+          if (c1 >= 0) oo[c1] = acc[mt][j][2] + acc[mt][j][3] + vbt;
         }
       }
     }
-    if (lane == 0) flags[warp] = dumped ? 1 : 0;
     __syncthreads();
 
     // ---------------- CTA merge of the warps, then output or partial
-    const int64_t pf = owner(u * NI), pl = owner(u * NI + NI - 1);
-    const int nparts = static_cast<int>(pl - pf + 1);
+    const int pf = owner(u * NI), pl = owner(u * NI + NI - 1);
+    const int nparts = pl - pf + 1;
     const int64_t qrow = (static_cast<int64_t>(b) * p.kv_heads + kvh) * p.gqa;  // first query head row
     const int stride_slot = p.gqa * (D + 2);
-    float* slot = p.partials + (pid + u) * stride_slot;
+    float* slot = p.partials + static_cast<int64_t>(pid + u) * stride_slot;
     for (int idx = tid; idx < p.gqa * D; idx += kThreads) {
       const int h = idx / D, c = idx % D;
       float M = -INFINITY;
@@ -703,9 +971,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         const float mw = wm[w * H + h];
         if (mw == -INFINITY) continue;
         const float f = exp2f(mw - M);
-        float o = wo[(w * H + h) * D + c];
-        if (flags[w]) o += dump[(w * H + h) * D + c] * exp2f(dm[w * H + h] - mw);
-        O += o * f;
+        O += wo[(w * H + h) * D + c] * f;
         Lsum += wl[w * H + h] * f;
       }
       if (nparts == 1) {
@@ -731,10 +997,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         for (int idx = tid; idx < p.gqa * D; idx += kThreads) {
           const int h = idx / D, c = idx % D;
           float M = -INFINITY;
-          for (int64_t s = pf; s <= pl; ++s) M = fmaxf(M, __ldcg(p.partials + (s + u) * stride_slot + p.gqa * D + 2 * h));
+          for (int sidx = pf; sidx <= pl; ++sidx)
+            M = fmaxf(M, __ldcg(p.partials + static_cast<int64_t>(sidx + u) * stride_slot + p.gqa * D + 2 * h));
           float O = 0.0f, Lsum = 0.0f;
-          for (int64_t s = pf; s <= pl; ++s) {
-            const float* ps = p.partials + (s + u) * stride_slot;
+          for (int sidx = pf; sidx <= pl; ++sidx) {
+            const float* ps = p.partials + static_cast<int64_t>(sidx + u) * stride_slot;
             const float f = exp2f(__ldcg(ps + p.gqa * D + 2 * h) - M);
             O += __ldcg(ps + h * D + c) * f;
             Lsum += __ldcg(ps + p.gqa * D + 2 * h + 1) * f;

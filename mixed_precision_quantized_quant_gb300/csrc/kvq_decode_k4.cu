@@ -16,12 +16,12 @@ static DecodeKernel make() {
 
 DecodeKernel decode_get_k4(int vb, int D, int nt) {
   DecodeKernel none{nullptr, 0, 0};
-#define E(VB)                                                       \
-  if (vb == VB) {                                                   \
+#define E(VB)                                                               \
+  if (vb == VB) {                                                           \
     if (D == 128) return nt == 1 ? make<VB, 128, 1>() : make<VB, 128, 2>(); \
-    return nt == 1 ? make<VB, 64, 1>() : make<VB, 64, 2>();         \
+    return nt == 1 ? make<VB, 64, 1>() : make<VB, 64, 2>();                 \
   }
-  E(2) E(4) E(8)
+  E(2) E(3) E(4) E(8)
 #undef E
   return none;
 }

@@ -6,23 +6,24 @@
 namespace kvq {
 
 DecodeKernel decode_get_k2(int vb, int D, int nt);
+DecodeKernel decode_get_k3(int vb, int D, int nt);
 DecodeKernel decode_get_k4(int vb, int D, int nt);
 DecodeKernel decode_get_k8(int vb, int D, int nt);
 
-size_t decode_smem_bytes(int D, int nt, int rec_bytes) {
-  return static_cast<size_t>(decode_smem_layout(D, nt, rec_bytes).total);
+size_t decode_smem_bytes(int D, int nt, int G, int rec_bytes) {
+  return static_cast<size_t>(decode_smem_layout(D, nt, G, rec_bytes).total);
 }
 
 DecodeKernel decode_select(int kb, int vb, int D, int gqa, int G, int rec_bytes) {
-  (void)G;
   DecodeKernel k{nullptr, 0, 0};
   if (gqa < 1 || gqa > 8) return k;
   const int nt = gqa <= 4 ? 1 : 2;
   if (kb == 2) k = decode_get_k2(vb, D, nt);
+  else if (kb == 3) k = decode_get_k3(vb, D, nt);
   else if (kb == 4) k = decode_get_k4(vb, D, nt);
   else if (kb == 8) k = decode_get_k8(vb, D, nt);
   if (!k.fn) return k;
-  k.smem = decode_smem_bytes(D, nt, rec_bytes);
+  k.smem = decode_smem_bytes(D, nt, G, rec_bytes);
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(k.smem)) != cudaSuccess) {
     k.fn = nullptr;

@@ -21,6 +21,6 @@ struct DecodeKernel {
 };
 // Returns fn == nullptr if the combination has no instantiation.
 DecodeKernel decode_select(int kb, int vb, int D, int gqa, int G, int rec_bytes);
-size_t decode_smem_bytes(int D, int nt, int rec_bytes);
+size_t decode_smem_bytes(int D, int nt, int G, int rec_bytes);
 
 }  // namespace kvq

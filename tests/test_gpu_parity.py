@@ -58,7 +58,7 @@ def _run_stream(kb, vb, D, G, R, gqa, schedule, B=2, Hkv=2, attn_every=1, seed=0
     cache.close()
 
 
-PAIRS = [(2, 2), (2, 4), (2, 8), (4, 2), (4, 4), (4, 8), (8, 2), (8, 4), (8, 8)]
+PAIRS = [(kb, vb) for kb in (2, 3, 4, 8) for vb in (2, 3, 4, 8)]
 
 
 @pytest.mark.parametrize("kb,vb", PAIRS)
@@ -193,7 +193,7 @@ def _layers_to_check(w):
     return out
 
 
-@pytest.mark.parametrize("idx", [2, 3, 5])
+@pytest.mark.parametrize("idx", [2, 3, 4, 5])
 def test_workload_full_size_sampled(idx):
     """Full-size shapes in the benchmark's launch configuration, one layer per
     distinct precision pair; codes and attention checked on sampled units."""
