@@ -158,21 +158,21 @@ template <int KB>
 __device__ __forceinline__ void k_word_pairs(uint32_t w, uint32_t* e) {
   if constexpr (KB == 4) {
     const uint32_t t = w >> 8;
-    e[0] = magic_fix(and_or(w, 0x000F000Fu, kMagic), 1.0f);
-    e[1] = magic_fix(and_or(w, 0x00F000F0u, kMagic), 1.0f / 16.0f);
-    e[2] = magic_fix(and_or(t, 0x000F000Fu, kMagic), 1.0f);
-    e[3] = magic_fix(and_or(t, 0x00F000F0u, kMagic), 1.0f / 16.0f);
+    e[0] = magic_fix(and_or(w, 0x000F000Fu, kMagic), 0);
+    e[1] = magic_fix(and_or(w, 0x00F000F0u, kMagic), 4);
+    e[2] = magic_fix(and_or(t, 0x000F000Fu, kMagic), 0);
+    e[3] = magic_fix(and_or(t, 0x00F000F0u, kMagic), 4);
   } else if constexpr (KB == 2) {
     const uint32_t t = w >> 10;
 #pragma unroll
     for (int i = 0; i < 5; ++i)
-      e[i] = magic_fix(and_or(w, 0x00030003u << (2 * i), kMagic), 1.0f / static_cast<float>(1 << (2 * i)));
+      e[i] = magic_fix(and_or(w, 0x00030003u << (2 * i), kMagic), 2 * i);
 #pragma unroll
     for (int i = 0; i < 3; ++i)
-      e[5 + i] = magic_fix(and_or(t, 0x00030003u << (2 * i), kMagic), 1.0f / static_cast<float>(1 << (2 * i)));
+      e[5 + i] = magic_fix(and_or(t, 0x00030003u << (2 * i), kMagic), 2 * i);
   } else {  // 8-bit
-    e[0] = magic_fix(prmt(w, 0x64646464u, 0x4240u), 1.0f);
-    e[1] = magic_fix(prmt(w, 0x64646464u, 0x4341u), 1.0f);
+    e[0] = magic_fix(prmt(w, 0x64646464u, 0x4240u), 0);
+    e[1] = magic_fix(prmt(w, 0x64646464u, 0x4341u), 0);
   }
 }
 
@@ -181,16 +181,16 @@ __device__ __forceinline__ void k_word_pairs(uint32_t w, uint32_t* e) {
 __device__ __forceinline__ void lo5(uint32_t a, uint32_t b, uint32_t* e) {
   const uint32_t z = prmt(a, b, 0x5410u);
   const uint32_t z9 = z >> 9;
-  e[0] = magic_fix(and_or(z, 0x00070007u, kMagic), 1.0f);
-  e[1] = magic_fix(and_or(z, 0x00380038u, kMagic), 1.0f / 8.0f);
-  e[2] = magic_fix(and_or(z, 0x01C001C0u, kMagic), 1.0f / 64.0f);
-  e[3] = magic_fix(and_or(z9, 0x00070007u, kMagic), 1.0f);
-  e[4] = magic_fix(and_or(z9, 0x00380038u, kMagic), 1.0f / 8.0f);
+  e[0] = magic_fix(and_or(z, 0x00070007u, kMagic), 0);
+  e[1] = magic_fix(and_or(z, 0x00380038u, kMagic), 3);
+  e[2] = magic_fix(and_or(z, 0x01C001C0u, kMagic), 6);
+  e[3] = magic_fix(and_or(z9, 0x00070007u, kMagic), 0);
+  e[4] = magic_fix(and_or(z9, 0x00380038u, kMagic), 3);
 }
 
 // 2-bit fields (bits 30..31) of two words as one pair.
 __device__ __forceinline__ uint32_t slot10_pair(uint32_t a, uint32_t b) {
-  return magic_fix(and_or(prmt(a >> 30, b >> 30, 0x5410u), 0x00030003u, kMagic), 1.0f);
+  return magic_fix(and_or(prmt(a >> 30, b >> 30, 0x5410u), 0x00030003u, kMagic), 0);
 }
 
 // The thread's key pairs of one token row.
@@ -209,11 +209,11 @@ __device__ __forceinline__ void key_row_pairs(const uint32_t* row, int tig, uint
       // move fields 5..9 up one bit so field i and field i+5 sit 16 bits apart
       const uint32_t x = (w[wi] & 0x7FFFu) | ((w[wi] << 1) & 0xFFFF0000u);
       const uint32_t x9 = x >> 9;
-      E[5 * wi + 0] = magic_fix(and_or(x, 0x00070007u, kMagic), 1.0f);
-      E[5 * wi + 1] = magic_fix(and_or(x, 0x00380038u, kMagic), 1.0f / 8.0f);
-      E[5 * wi + 2] = magic_fix(and_or(x, 0x01C001C0u, kMagic), 1.0f / 64.0f);
-      E[5 * wi + 3] = magic_fix(and_or(x9, 0x00070007u, kMagic), 1.0f);
-      E[5 * wi + 4] = magic_fix(and_or(x9, 0x00380038u, kMagic), 1.0f / 8.0f);
+      E[5 * wi + 0] = magic_fix(and_or(x, 0x00070007u, kMagic), 0);
+      E[5 * wi + 1] = magic_fix(and_or(x, 0x00380038u, kMagic), 3);
+      E[5 * wi + 2] = magic_fix(and_or(x, 0x01C001C0u, kMagic), 6);
+      E[5 * wi + 3] = magic_fix(and_or(x9, 0x00070007u, kMagic), 0);
+      E[5 * wi + 4] = magic_fix(and_or(x9, 0x00380038u, kMagic), 3);
     }
 #pragma unroll
     for (int k = 5 * S::WT; k < S::NPK; ++k) {
@@ -230,17 +230,15 @@ __device__ __forceinline__ void key_row_pairs(const uint32_t* row, int tig, uint
 
 // 2-bit field i (0..7) of both halves of x -> half2 of exact codes
 __device__ __forceinline__ uint32_t f2(uint32_t x, int i) {
-  if (i < 5) return magic_fix(and_or(x, 0x00030003u << (2 * i), kMagic), 1.0f / static_cast<float>(1 << (2 * i)));
-  return magic_fix(and_or(x >> 10, 0x00030003u << (2 * (i - 5)), kMagic),
-                   1.0f / static_cast<float>(1 << (2 * (i - 5))));
+  if (i < 5) return magic_fix(and_or(x, 0x00030003u << (2 * i), kMagic), 2 * i);
+  return magic_fix(and_or(x >> 10, 0x00030003u << (2 * (i - 5)), kMagic), 2 * (i - 5));
 }
 __device__ __forceinline__ uint32_t f4(uint32_t x, int f) {
   const uint32_t y = (f >= 2) ? (x >> 8) : x;
-  return (f & 1) ? magic_fix(and_or(y, 0x00F000F0u, kMagic), 1.0f / 16.0f)
-                 : magic_fix(and_or(y, 0x000F000Fu, kMagic), 1.0f);
+  return (f & 1) ? magic_fix(and_or(y, 0x00F000F0u, kMagic), 4) : magic_fix(and_or(y, 0x000F000Fu, kMagic), 0);
 }
 __device__ __forceinline__ uint32_t f8(uint32_t z, int i) {
-  return magic_fix(and_or(i ? (z >> 8) : z, 0x00FF00FFu, kMagic), 1.0f);
+  return magic_fix(and_or(i ? (z >> 8) : z, 0x00FF00FFu, kMagic), 0);
 }
 
 // Value code pairs for two tokens (a, b): H[c] = (code_a[c], code_b[c]) for the
@@ -422,12 +420,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   // Ring bookkeeping runs identically in every lane; lane 0 issues the copies.
   int rhead = 0, rtail = 0, rend = 0, nin = 0, kiss = 0, kcon = 0;
   bool wrapped = false;
-  auto item_bytes = [&](int f) -> int { return (f - (f / NI) * NI) < NG ? cq : cr; };
+  // (unit, item) of the next item to issue / to consume, advanced without division
+  int iu = (f0 + warp) / NI, ii = (f0 + warp) - ((f0 + warp) / NI) * NI;
+  int cu = iu, ci = ii;
   auto try_issue = [&]() {
     while (nin < kSlots) {
       const int f = f0 + warp + 4 * kiss;
       if (f >= f1) break;
-      const int sz = item_bytes(f);
+      const int sz = ii < NG ? cq : cr;
       int off;
       if (nin == 0) {
         rhead = rtail = 0;
@@ -449,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       }
       rhead = off + sz;
       if (lane == 0) {
-        const int st = kiss % kSlots;
-        const int u = f / NI, i = f - u * NI;
+        const int st = kiss & (kSlots - 1);
+        const int u = iu, i = ii;
         uint8_t* dst = ring + off;
         fence_proxy_async_smem();
         if (i < NG) {
@@ -478,6 +478,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       }
       ++nin;
       ++kiss;
+      ii += 4;
+      while (ii >= NI) {
+        ii -= NI;
+        ++iu;
+      }
     }
   };
   try_issue();
@@ -502,14 +507,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       reinterpret_cast<__half2*>(qs)[idx] = v;
     }
     __syncthreads();
-    if (warp == 0) {
+    {
+      // every warp fills a quarter of the per-lane tables (lane = tid & 31)
       uint32_t* qp = qp_tab + lane * QPS;
       uint32_t* qr = qr_tab + lane * QRS;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + (g >> 1);
         const bool live = h < p.gqa;
-        for (int pi = 0; pi < NPK; ++pi) {
+        for (int pi = warp; pi < NPK; pi += kWarps) {
           int ca, cb;
           key_pair_channels<KB, D>(tig, pi, ca, cb);
           const __half z0 = __float2half(0.0f);
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           const __half qb = (live && cb >= 0) ? qs[h * D + cb] : z0;
           qp[j * NPK + pi] = h2_as_u32(__halves2half2(qa, qb));
         }
-        for (int kk = 0; kk < KS; ++kk) {
+        for (int kk = warp; kk < KS; kk += kWarps) {
           for (int rr = 0; rr < 2; ++rr) {
             const int c = 16 * kk + 8 * rr + 2 * tig;
             qr[(j * KS + kk) * 2 + rr] =
@@ -560,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           const float mn = fmaxf(m[j], tmax[j]);
-          const float f = (mn == -INFINITY) ? 1.0f : exp2f(m[j] - mn);
+          const float f = (mn == -INFINITY) ? 1.0f : ex2(m[j] - mn);
           m[j] = mn;
           l[j] *= f;
           vb[j] *= f;
@@ -587,11 +593,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
     while (true) {
       const int f = f0 + warp + 4 * kcon;
       if (f >= seg_hi) break;
-      const int st = kcon % kSlots;
-      const uint32_t ph = static_cast<uint32_t>((kcon / kSlots) & 1);
+      const int st = kcon & (kSlots - 1);
+      const uint32_t ph = static_cast<uint32_t>((kcon >> 2) & 1);
       if (!failed && !mbar_wait(&wbar[st], ph, p.err)) failed = true;
       const uint8_t* stg = ring + rtail;
-      const int i = f - (f / NI) * NI;
+      const int i = ci;
 
       if (failed) {
         // a copy never landed: skip the work, keep the control flow
@@ -730,17 +736,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) sc[t][j][q4] += sx[t][j][q4];
         }
-        // scaled scores: s[t][j][0] token 16t+g, [1] token 16t+g+8
+        // raw scores: s[t][j][0] token 16t+g, [1] token 16t+g+8; m is kept in
+        // units of alpha * raw (log2 domain), p = 2^(alpha*raw - m)
         float s[2][NT][2];
         float tmax[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            s[t][j][0] = (sc[t][j][0] + sc[t][j][1]) * alpha;
-            s[t][j][1] = (sc[t][j][2] + sc[t][j][3]) * alpha;
+            s[t][j][0] = sc[t][j][0] + sc[t][j][1];
+            s[t][j][1] = sc[t][j][2] + sc[t][j][3];
           }
-          tmax[j] = fmaxf(fmaxf(s[0][j][0], s[0][j][1]), fmaxf(s[1][j][0], s[1][j][1]));
+          tmax[j] = alpha * fmaxf(fmaxf(s[0][j][0], s[0][j][1]), fmaxf(s[1][j][0], s[1][j][1]));
         }
         softmax_update(tmax);
         float2 sz[2][2];
@@ -755,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           uint32_t b01[NT], b23[NT], c01[NT], c23[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            const float pa = exp2f(s[t][j][0] - m[j]), pb = exp2f(s[t][j][1] - m[j]);
+            const float pa = ex2(fmaf(s[t][j][0], alpha, -m[j])), pb = ex2(fmaf(s[t][j][1], alpha, -m[j]));
             l[j] += pa + pb;
             vb[j] = fmaf(pa, sz[t][0].y, fmaf(pb, sz[t][1].y, vb[j]));
             uint32_t hi, lo;
@@ -881,15 +888,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
         float sa[NT], sb[NT], tmax[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          sa[j] = (g < vt) ? (sc[j][0] + sx[j][0] + sc[j][1] + sx[j][1]) * alpha : -INFINITY;
-          sb[j] = (g + 8 < vt) ? (sc[j][2] + sx[j][2] + sc[j][3] + sx[j][3]) * alpha : -INFINITY;
-          tmax[j] = fmaxf(sa[j], sb[j]);
+          sa[j] = (g < vt) ? (sc[j][0] + sx[j][0]) + (sc[j][1] + sx[j][1]) : -INFINITY;
+          sb[j] = (g + 8 < vt) ? (sc[j][2] + sx[j][2]) + (sc[j][3] + sx[j][3]) : -INFINITY;
+          tmax[j] = alpha * fmaxf(sa[j], sb[j]);
         }
         softmax_update(tmax);
         uint32_t b01[NT], b23[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          const float pa = exp2f(sa[j] - m[j]), pb = exp2f(sb[j] - m[j]);
+          const float pa = ex2(fmaf(sa[j], alpha, -m[j])), pb = ex2(fmaf(sb[j], alpha, -m[j]));
           l[j] += pa + pb;
           uint32_t hi, lo;
           split_pair(pa, pb, hi, lo);
@@ -910,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       // release the consumed item's ring space, then refill
       __syncwarp();
       {
-        const int sz = item_bytes(f);
+        const int sz = ci < NG ? cq : cr;
         --nin;
         rtail += sz;
         if (wrapped && rtail == rend) {
@@ -919,6 +926,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
         }
       }
       ++kcon;
+      ci += 4;
+      while (ci >= NI) {
+        ci -= NI;
+        ++cu;
+      }
       try_issue();
     }
 
@@ -935,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
         wl[warp * H + h] = lt;
       }
       float* oo = wo + (warp * H + h) * D;
-      const float fd = dumped ? exp2f(dm[warp * H + h] - m[j]) : 0.0f;
+      const float fd = dumped ? ex2(dm[warp * H + h] - m[j]) : 0.0f;
       if (in_res) {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
@@ -970,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       for (int w = 0; w < kWarps; ++w) {
         const float mw = wm[w * H + h];
         if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
+        const float f = ex2(mw - M);
         O += wo[(w * H + h) * D + c] * f;
         Lsum += wl[w * H + h] * f;
       }
@@ -1002,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           float O = 0.0f, Lsum = 0.0f;
           for (int sidx = pf; sidx <= pl; ++sidx) {
             const float* ps = p.partials + static_cast<int64_t>(sidx + u) * stride_slot;
-            const float f = exp2f(__ldcg(ps + p.gqa * D + 2 * h) - M);
+            const float f = ex2(__ldcg(ps + p.gqa * D + 2 * h) - M);
             O += __ldcg(ps + h * D + c) * f;
             Lsum += __ldcg(ps + p.gqa * D + 2 * h + 1) * f;
           }

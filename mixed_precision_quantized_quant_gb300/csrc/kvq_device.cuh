@@ -173,12 +173,20 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t m
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// e holds two fp16 values 1024 + f*code (exact); returns the codes, exact:
-// e * (1/f) - 1024/f with one fma (f a power of two).
-__device__ __forceinline__ uint32_t magic_fix(uint32_t e, float inv_f) {
-  const __half2 s = __float2half2_rn(inv_f);
-  const __half2 o = __float2half2_rn(-1024.0f * inv_f);
-  return h2_as_u32(__hfma2(u32_as_h2(e), s, o));
+// e holds two fp16 values 1024 + 2^k * code (exact); returns the codes, exact:
+// e * 2^-k - 1024 * 2^-k with one fma.  The constants are built from their
+// fp16 bit patterns so they fold at compile time.
+__device__ __forceinline__ uint32_t magic_fix(uint32_t e, int k) {
+  const uint32_t sc = static_cast<uint32_t>(15 - k) << 10;                // 2^-k
+  const uint32_t of = 0x8000u | (static_cast<uint32_t>(25 - k) << 10);   // -1024 * 2^-k
+  return h2_as_u32(__hfma2(u32_as_h2(e), u32_as_h2(sc | (sc << 16)), u32_as_h2(of | (of << 16))));
+}
+
+// 2^x for x <= 0 (probabilities and rescale factors), one MUFU op
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 constexpr uint32_t kMagic = 0x64006400u;  // fp16 1024.0 in both halves
