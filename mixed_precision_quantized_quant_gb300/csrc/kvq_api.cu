@@ -85,6 +85,14 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
     lp.wv = words_per_row(P->D, lp.vb);
     lp.rec_bytes = 4LL * P->G * (lp.wk + lp.wv) + 4LL * P->D + 4LL * P->G;
     lp.max_groups = P->max_tokens / P->G;
+    {
+      // the decode kernel splits a layer's work in 32-bit byte-cost units
+      const int64_t slice = 4LL * 32 * (lp.wk + lp.wv) + 4LL * P->D + 128;
+      const int64_t tile = 16LL * 4 * P->D;
+      const int64_t setup = 4 * (slice > 2048 ? slice : 2048);
+      const int64_t per_unit = setup + lp.max_groups * (P->G / 32) * slice + ((lp.R + 15) / 16) * tile;
+      if (per_unit * P->units >= (1LL << 32)) return KVQ_ERR_UNSUPPORTED;
+    }
     lp.unit_rec_stride = align_up(lp.max_groups * lp.rec_bytes, kAlign);
     lp.off_records = off;
     off += lp.unit_rec_stride * P->units;

@@ -51,7 +51,7 @@ __host__ __device__ constexpr int ring_bytes(int D, int G, int rec_bytes) {
 
 struct DecodeSmem {
   int ring;
-  int off_bars, off_qs, off_qp, off_qr, off_wm, off_wl, off_dm, off_flags, off_wo, total;
+  int off_bars, off_qs, off_qp, off_qps, off_qr, off_wm, off_wl, off_dm, off_flags, off_wo, total;
 };
 
 __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, int rec_bytes) {
@@ -60,13 +60,16 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, i
   s.ring = ring_bytes(D, G, rec_bytes);
   int off = kWarps * s.ring;
   s.off_bars = off;
-  off += kWarps * kSlots * 8;
+  off += (kWarps * kSlots + 2) * 8;  // ring slots, then the two query buffers
   s.off_qs = off;
-  off += H * D * 2;
+  off += 2 * H * D * 2;              // double-buffered query rows of a unit
+  // per-lane query tables, lane-interleaved in 8-byte pairs (conflict-free)
   s.off_qp = off;
-  off += 32 * (NT * 18 + 4) * 4;  // key-pair table (up to 18 pairs per thread)
+  off += 32 * NT * 18 * 4;           // key-pair query table (up to 18 pairs per thread)
+  s.off_qps = off;
+  off += 32 * NT * 18 * 4;           // same, scaled by 2^(Pmax - pos) per pair
   s.off_qr = off;
-  off += 32 * (NT * D / 16 * 2 + 4) * 4;
+  off += 32 * NT * D / 16 * 2 * 4;   // residual (fp16 key) query table
   s.off_wm = off;
   off += kWarps * H * 4;
   s.off_wl = off;
@@ -125,6 +128,14 @@ struct ValShape {
   static constexpr int VW = (VB == 3) ? 1 : ((D * VB / 256) > 0 ? (D * VB / 256) : 1);
 };
 
+// Codes enter the tensor cores as exact fp16 subnormals: a field masked in
+// place at bit position pos (pos + width <= 10) is the fp16 value
+// code * 2^(pos - 24).  The power-of-two factor is removed outside the MMA:
+// for keys it is folded into the query column of that k-slot (q scaled by
+// 2^(Pmax - pos), so every product carries 2^(Pmax - 24)); for values every
+// row of a value m-tile shares one position and the fp32 accumulator of that
+// tile is rescaled once at the end.
+
 // Channels (ca, cb) of key pair pi of thread tig (-1 for padding).
 //  4-bit: (c0,c4) (c1,c5) (c2,c6) (c3,c7) per word; 2-bit: (c_i, c_{8+i});
 //  8-bit: (c0,c2) (c1,c3); 3-bit: fields (i, i+5) of each word, then the
@@ -153,45 +164,55 @@ __device__ __forceinline__ void key_pair_channels(int tig, int pi, int& ca, int&
   }
 }
 
+// Bit position of key pair pi inside its 16-bit half, and the largest one.
+template <int KB, int D>
+__host__ __device__ constexpr int key_pos(int pi) {
+  if (KB == 4) return 4 * (pi & 1);
+  if (KB == 2) return 2 * (pi & 1);
+  if (KB == 8) return 0;
+  return (pi < 5 * KeyShape<KB, D>::WT) ? ((pi % 5) % 3) * 3 : 0;  // 3-bit: 0,3,6,0,3
+}
+template <int KB>
+__host__ __device__ constexpr int key_pos_max() {
+  return KB == 4 ? 4 : (KB == 2 ? 2 : (KB == 8 ? 0 : 6));
+}
+
 // Code pairs of one 2/4/8-bit key word in key_pair_channels order.
 template <int KB>
 __device__ __forceinline__ void k_word_pairs(uint32_t w, uint32_t* e) {
   if constexpr (KB == 4) {
     const uint32_t t = w >> 8;
-    e[0] = magic_fix(and_or(w, 0x000F000Fu, kMagic), 0);
-    e[1] = magic_fix(and_or(w, 0x00F000F0u, kMagic), 4);
-    e[2] = magic_fix(and_or(t, 0x000F000Fu, kMagic), 0);
-    e[3] = magic_fix(and_or(t, 0x00F000F0u, kMagic), 4);
+    e[0] = w & 0x000F000Fu;
+    e[1] = w & 0x00F000F0u;
+    e[2] = t & 0x000F000Fu;
+    e[3] = t & 0x00F000F0u;
   } else if constexpr (KB == 2) {
-    const uint32_t t = w >> 10;
 #pragma unroll
-    for (int i = 0; i < 5; ++i)
-      e[i] = magic_fix(and_or(w, 0x00030003u << (2 * i), kMagic), 2 * i);
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-      e[5 + i] = magic_fix(and_or(t, 0x00030003u << (2 * i), kMagic), 2 * i);
+    for (int i = 0; i < 8; i += 2) {
+      const uint32_t t = w >> (2 * i);
+      e[i] = t & 0x00030003u;
+      e[i + 1] = t & 0x000C000Cu;
+    }
   } else {  // 8-bit
-    e[0] = magic_fix(prmt(w, 0x64646464u, 0x4240u), 0);
-    e[1] = magic_fix(prmt(w, 0x64646464u, 0x4341u), 0);
+    e[0] = prmt(w, 0u, 0x4240u);
+    e[1] = prmt(w, 0u, 0x4341u);
   }
 }
 
-// Five 3-bit fields at bits 0,3,..,12 of the low halves of two words:
-// returns (field_i of a, field_i of b) for i = 0..4, exact.
+// Five 3-bit fields at bits 0,3,..,12 of the low halves of two words, as
+// (field_i of a, field_i of b) subnormal pairs at positions 0,3,6,0,3.
 __device__ __forceinline__ void lo5(uint32_t a, uint32_t b, uint32_t* e) {
   const uint32_t z = prmt(a, b, 0x5410u);
   const uint32_t z9 = z >> 9;
-  e[0] = magic_fix(and_or(z, 0x00070007u, kMagic), 0);
-  e[1] = magic_fix(and_or(z, 0x00380038u, kMagic), 3);
-  e[2] = magic_fix(and_or(z, 0x01C001C0u, kMagic), 6);
-  e[3] = magic_fix(and_or(z9, 0x00070007u, kMagic), 0);
-  e[4] = magic_fix(and_or(z9, 0x00380038u, kMagic), 3);
+  e[0] = z & 0x00070007u;
+  e[1] = z & 0x00380038u;
+  e[2] = z & 0x01C001C0u;
+  e[3] = z9 & 0x00070007u;
+  e[4] = z9 & 0x00380038u;
 }
 
-// 2-bit fields (bits 30..31) of two words as one pair.
-__device__ __forceinline__ uint32_t slot10_pair(uint32_t a, uint32_t b) {
-  return magic_fix(and_or(prmt(a >> 30, b >> 30, 0x5410u), 0x00030003u, kMagic), 0);
-}
+// 2-bit fields (bits 30..31) of two words as one pair at position 0.
+__device__ __forceinline__ uint32_t slot10_pair(uint32_t a, uint32_t b) { return prmt(a >> 30, b >> 30, 0x5410u); }
 
 // The thread's key pairs of one token row.
 template <int KB, int D>
@@ -209,11 +230,11 @@ __device__ __forceinline__ void key_row_pairs(const uint32_t* row, int tig, uint
       // move fields 5..9 up one bit so field i and field i+5 sit 16 bits apart
       const uint32_t x = (w[wi] & 0x7FFFu) | ((w[wi] << 1) & 0xFFFF0000u);
       const uint32_t x9 = x >> 9;
-      E[5 * wi + 0] = magic_fix(and_or(x, 0x00070007u, kMagic), 0);
-      E[5 * wi + 1] = magic_fix(and_or(x, 0x00380038u, kMagic), 3);
-      E[5 * wi + 2] = magic_fix(and_or(x, 0x01C001C0u, kMagic), 6);
-      E[5 * wi + 3] = magic_fix(and_or(x9, 0x00070007u, kMagic), 0);
-      E[5 * wi + 4] = magic_fix(and_or(x9, 0x00380038u, kMagic), 3);
+      E[5 * wi + 0] = x & 0x00070007u;
+      E[5 * wi + 1] = x & 0x00380038u;
+      E[5 * wi + 2] = x & 0x01C001C0u;
+      E[5 * wi + 3] = x9 & 0x00070007u;
+      E[5 * wi + 4] = x9 & 0x00380038u;
     }
 #pragma unroll
     for (int k = 5 * S::WT; k < S::NPK; ++k) {
@@ -228,69 +249,84 @@ __device__ __forceinline__ void key_row_pairs(const uint32_t* row, int tig, uint
   }
 }
 
-// 2-bit field i (0..7) of both halves of x -> half2 of exact codes
-__device__ __forceinline__ uint32_t f2(uint32_t x, int i) {
-  if (i < 5) return magic_fix(and_or(x, 0x00030003u << (2 * i), kMagic), 2 * i);
-  return magic_fix(and_or(x >> 10, 0x00030003u << (2 * (i - 5)), kMagic), 2 * (i - 5));
-}
-__device__ __forceinline__ uint32_t f4(uint32_t x, int f) {
-  const uint32_t y = (f >= 2) ? (x >> 8) : x;
-  return (f & 1) ? magic_fix(and_or(y, 0x00F000F0u, kMagic), 4) : magic_fix(and_or(y, 0x000F000Fu, kMagic), 0);
-}
-__device__ __forceinline__ uint32_t f8(uint32_t z, int i) {
-  return magic_fix(and_or(i ? (z >> 8) : z, 0x00FF00FFu, kMagic), 0);
-}
-
 // Value code pairs for two tokens (a, b): H[c] = (code_a[c], code_b[c]) for the
-// D/8 channels this thread owns (2/4/8-bit values).
+// D/8 channels this thread owns (2/4/8-bit values), as subnormals at the
+// positions value_pos gives for the m-tile that uses them.
 template <int VB, int D>
 __device__ __forceinline__ void v_pairs(const uint32_t* wa, const uint32_t* wb, uint32_t half_sel,
                                         uint32_t (&H)[D / 8]) {
   if constexpr (VB == 2) {
     if constexpr (D == 128) {
       const uint32_t x = prmt(wa[0], wb[0], 0x5410u), y = prmt(wa[0], wb[0], 0x7632u);
+      const uint32_t x10 = x >> 10, y10 = y >> 10;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        H[i] = f2(x, i);
-        H[8 + i] = f2(y, i);
+      for (int i = 0; i < 5; ++i) {
+        H[i] = x & (0x00030003u << (2 * i));
+        H[8 + i] = y & (0x00030003u << (2 * i));
+      }
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        H[5 + i] = x10 & (0x00030003u << (2 * i));
+        H[13 + i] = y10 & (0x00030003u << (2 * i));
       }
     } else {
       const uint32_t x = prmt(wa[0], wb[0], half_sel);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) H[i] = f2(x, i);
+      for (int i = 0; i < 8; i += 2) {
+        const uint32_t t = x >> (2 * i);
+        H[i] = t & 0x00030003u;
+        H[i + 1] = t & 0x000C000Cu;
+      }
     }
   } else if constexpr (VB == 4) {
 #pragma unroll
     for (int k = 0; k < D / 64; ++k) {
       const uint32_t x = prmt(wa[k], wb[k], 0x5410u), y = prmt(wa[k], wb[k], 0x7632u);
-#pragma unroll
-      for (int f = 0; f < 4; ++f) {
-        H[8 * k + f] = f4(x, f);
-        H[8 * k + 4 + f] = f4(y, f);
-      }
+      const uint32_t x8 = x >> 8, y8 = y >> 8;
+      H[8 * k + 0] = x & 0x000F000Fu;
+      H[8 * k + 1] = x & 0x00F000F0u;
+      H[8 * k + 2] = x8 & 0x000F000Fu;
+      H[8 * k + 3] = x8 & 0x00F000F0u;
+      H[8 * k + 4] = y & 0x000F000Fu;
+      H[8 * k + 5] = y & 0x00F000F0u;
+      H[8 * k + 6] = y8 & 0x000F000Fu;
+      H[8 * k + 7] = y8 & 0x00F000F0u;
     }
   } else {  // 8-bit
 #pragma unroll
     for (int k = 0; k < D / 32; ++k) {
       const uint32_t z = prmt(wa[k], wb[k], 0x5410u), y = prmt(wa[k], wb[k], 0x7632u);
-      H[4 * k] = f8(z, 0);
-      H[4 * k + 1] = f8(z, 1);
-      H[4 * k + 2] = f8(y, 0);
-      H[4 * k + 3] = f8(y, 1);
+      H[4 * k] = z & 0x00FF00FFu;
+      H[4 * k + 1] = (z >> 8) & 0x00FF00FFu;
+      H[4 * k + 2] = y & 0x00FF00FFu;
+      H[4 * k + 3] = (y >> 8) & 0x00FF00FFu;
     }
   }
+}
+
+// Bit position shared by both rows of value m-tile mt (quantized channel map).
+template <int VB, int D>
+__host__ __device__ constexpr int value_pos(int mt) {
+  if (VB == 2) return D == 128 ? 2 * (mt < 5 ? mt : mt - 5) : 2 * (mt & 1);
+  if (VB == 4) return 4 * (mt & 1);
+  if (VB == 8) return 0;
+  // 3-bit: d128 tiles hold positions 0,0,0,3,3,3,6,6 then the 2-bit tile (0);
+  // d64 tiles 0,3,6,0,3 then the 2-bit tile (0)
+  if (D == 128) return mt < 3 ? 0 : (mt < 6 ? 3 : (mt < 8 ? 6 : 0));
+  return mt < 5 ? ((mt % 5) % 3) * 3 : 0;
 }
 
 // Channel of row (g + 8*hi) of value m-tile mt in the quantized-path map, or -1.
 //  2/4/8-bit: thread g owns channels [g*D/8, (g+1)*D/8): row g -> g*D/8 + mt,
 //  row g+8 -> g*D/8 + D/16 + mt.
-//  3-bit, d128: thread g owns the 3-bit fields of word g (entries 0..9) and
-//  fields 5h..5h+4 of word 8 + g/2 (h = g & 1, entries 10..14); row g of tile
-//  mt is entry mt, row g+8 entry 8 + mt; tile 8 holds 2-bit fields (word g,
-//  and word 8 + g/2 for even g while that word has one).
-//  3-bit, d64: thread g < 6 owns the 3-bit fields of word g (entries 0..9);
-//  row g of tile mt is entry mt, row g+8 entry 5 + mt; tile 5 holds the 2-bit
-//  field of word g < 5 in row g.
+//  3-bit, d128: thread g owns the 3-bit fields of word g and fields
+//  5h..5h+4 of word 8 + g/2 (h = g & 1).  With A = fields 0..4 of word g,
+//  A' = fields 5..9 of word g and B = the owned fields of word 8 + g/2, the
+//  tiles hold (row g / row g+8): A0/A3, A'0/A'3, B0/B3, A1/A4, A'1/A'4,
+//  B1/B4, A2/A'2, B2/-; tile 8 holds 2-bit fields (word g, and word 8 + g/2
+//  for even g while that word has one).
+//  3-bit, d64: thread g < 6 owns word g: tile mt holds field mt / field 5+mt
+//  (mt < 5); tile 5 holds the 2-bit field of word g < 5 in row g.
 template <int VB, int D>
 __device__ __forceinline__ int vq_channel(int g, int mt, int hi) {
   if constexpr (VB != 3) {
@@ -305,15 +341,19 @@ __device__ __forceinline__ int vq_channel(int g, int mt, int hi) {
       }
       return -1;
     }
-    const int e = hi ? MT3 + mt : mt;
     int c;
     if (D == 128) {
-      if (e < 10) c = 11 * g + e;
-      else if (e < 15) c = 11 * (8 + (g >> 1)) + 5 * (g & 1) + (e - 10);
-      else return -1;
+      // (source, field) of each tile row: source 0 = A, 1 = A', 2 = B
+      const int src_lo[8] = {0, 1, 2, 0, 1, 2, 0, 2}, fld_lo[8] = {0, 0, 0, 1, 1, 1, 2, 2};
+      const int src_hi[8] = {0, 1, 2, 0, 1, 2, 1, -1}, fld_hi[8] = {3, 3, 3, 4, 4, 4, 2, 0};
+      const int src = hi ? src_hi[mt] : src_lo[mt], fld = hi ? fld_hi[mt] : fld_lo[mt];
+      if (src < 0) return -1;
+      if (src == 0) c = 11 * g + fld;
+      else if (src == 1) c = 11 * g + 5 + fld;
+      else c = 11 * (8 + (g >> 1)) + 5 * (g & 1) + fld;
     } else {
       if (g >= 6) return -1;
-      c = 11 * g + e;
+      c = 11 * g + (hi ? 5 + mt : mt);
     }
     return c < D ? c : -1;
   }
@@ -348,14 +388,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   constexpr int MTA = MTV > KS ? MTV : KS;
   constexpr int NP = D / 8;
   constexpr int H = 4 * NT;             // padded query heads
-  constexpr int QPS = NT * NPK + 4;
-  constexpr int QRS = NT * KS * 2 + 4;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const DecodeSmem L = decode_smem_layout(D, NT, p.G, p.rec_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
   __half* qs = reinterpret_cast<__half*>(smem + L.off_qs);
   uint32_t* qp_tab = reinterpret_cast<uint32_t*>(smem + L.off_qp);
+  uint32_t* qps_tab = reinterpret_cast<uint32_t*>(smem + L.off_qps);
   uint32_t* qr_tab = reinterpret_cast<uint32_t*>(smem + L.off_qr);
   float* wm = reinterpret_cast<float*>(smem + L.off_wm);
   float* wl = reinterpret_cast<float*>(smem + L.off_wl);
@@ -365,8 +404,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tig = lane & 3, part = g & 1;
+  // table entry (j, pi) of lane l sits at u32 ((j*NPK + pi)/2 * 32 + l) * 2 + (pi & 1)
+  auto kt_idx = [](int j, int pi, int l) { return (((j * NPK + pi) >> 1) * 32 + l) * 2 + (pi & 1); };
+  auto rt_idx = [](int j, int kk, int l) { return ((j * KS + kk) * 32 + l) * 2; };
 
   // ---------------- state and this CTA's share of the work
+  // The flat list of items (per unit: its slices, then its residual tiles)
+  // is cut into P near-equal cost ranges, x(p) = p*floor(C/P) + min(p, C mod P);
+  // each unit also carries a fixed cost for its setup and merge, so CTAs that
+  // span two units get fewer bytes.  An item belongs to the CTA whose range
+  // holds its start.  All of it is 32-bit arithmetic (the host keeps a
+  // layer's decode bytes below 2^32), computed by every thread, no barrier.
   const int T = __ldcg(p.tokens);
   if (T <= 0) return;
   const int nq = static_cast<int>(quantized_after(T, p.R, p.G));
@@ -375,39 +423,48 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   const int NG = (nq / p.G) * NS;         // quantized work items (slices)
   const int NRT = (r + kResTile - 1) / kResTile;
   const int NI = NG + NRT;
-  const int cq = slice_bytes(D, p.G, p.rec_bytes), cr = kResTile * 4 * D;
-  const int64_t Cu = static_cast<int64_t>(NG) * cq + static_cast<int64_t>(NRT) * cr;
-  const int64_t C = static_cast<int64_t>(p.units) * Cu;
-  const int64_t maxc = (NRT > 0 && cr > cq) || NG == 0 ? cr : cq;
-  int64_t peff64 = C / maxc;
-  if (peff64 < 1) peff64 = 1;
-  if (peff64 > p.grid) peff64 = p.grid;
-  const int peff = static_cast<int>(peff64);
+  const uint32_t cq = slice_bytes(D, p.G, p.rec_bytes), cr = kResTile * 4 * D;
+  const uint32_t csu = 4u * (cq > 2048u ? cq : 2048u);  // per-unit setup cost
+  const uint32_t Cu = csu + static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(NRT) * cr;
+  const uint32_t C = static_cast<uint32_t>(p.units) * Cu;
+  // a CTA range must hold at least one item start: range >= largest item + setup
+  const uint32_t maxc = csu + ((NRT > 0 && cr > cq) || NG == 0 ? cr : cq);
+  uint32_t peff_u = C / maxc;
+  if (peff_u < 1) peff_u = 1;
+  if (peff_u > static_cast<uint32_t>(p.grid)) peff_u = p.grid;
+  const int peff = static_cast<int>(peff_u);
   const int pid = blockIdx.x;
   if (pid >= peff) return;
-
-  auto item_start = [&](int f) -> int64_t {
+  const uint32_t CQ = C / peff_u, CR = C - CQ * peff_u;
+  auto range_start = [&](uint32_t pp) -> uint32_t { return pp * CQ + (pp < CR ? pp : CR); };
+  auto item_start = [&](int f) -> uint32_t {
     const int u = f / NI, i = f - u * NI;
-    return u * Cu + (i < NG ? static_cast<int64_t>(i) * cq
-                            : static_cast<int64_t>(NG) * cq + static_cast<int64_t>(i - NG) * cr);
+    return static_cast<uint32_t>(u) * Cu + csu +
+           (i < NG ? static_cast<uint32_t>(i) * cq
+                   : static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(i - NG) * cr);
   };
-  auto first_item_at = [&](int64_t x) -> int {  // first flat item starting at or after x
-    const int64_t u = x / Cu, o = x - u * Cu;
-    int64_t i;
-    if (o == 0) {
+  auto first_item_at = [&](uint32_t x) -> int {  // first flat item starting at or after x
+    const uint32_t u = x / Cu;
+    const uint32_t ox = x - u * Cu;
+    int i;
+    if (ox <= csu) {
       i = 0;
-    } else if (NG > 0 && o <= static_cast<int64_t>(NG - 1) * cq) {
-      i = (o + cq - 1) / cq;
-    } else if (o <= static_cast<int64_t>(NG) * cq) {
-      i = NG;
     } else {
-      i = NG + (o - static_cast<int64_t>(NG) * cq + cr - 1) / cr;
+      const uint32_t o = ox - csu;
+      if (NG > 0 && o <= static_cast<uint32_t>(NG - 1) * cq) i = static_cast<int>((o + cq - 1) / cq);
+      else if (o <= static_cast<uint32_t>(NG) * cq) i = NG;
+      else i = NG + static_cast<int>((o - static_cast<uint32_t>(NG) * cq + cr - 1) / cr);
     }
-    return static_cast<int>(u * NI + i);
+    return static_cast<int>(u) * NI + i;
   };
-  auto owner = [&](int f) -> int { return static_cast<int>((item_start(f) * peff) / C); };
-  const int f0 = first_item_at((static_cast<int64_t>(pid) * C + peff - 1) / peff);
-  const int f1 = first_item_at((static_cast<int64_t>(pid + 1) * C + peff - 1) / peff);
+  auto owner = [&](int f) -> int {  // CTA whose range holds item f's start
+    const uint32_t x = item_start(f);
+    const uint32_t big = CR * (CQ + 1);
+    return x < big ? static_cast<int>(x / (CQ + 1)) : static_cast<int>(CR + (x - big) / CQ);
+  };
+  const int f0 = first_item_at(range_start(pid));
+  const int f1 = first_item_at(range_start(pid + 1));
+  const int u_first = f0 / NI, u_last = (f1 - 1) / NI;
 
   // ---------------- per-warp ring of staged items (kSlots copies in flight)
   uint8_t* ring = smem + warp * L.ring;
@@ -422,21 +479,21 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   bool wrapped = false;
   // (unit, item) of the next item to issue / to consume, advanced without division
   int iu = (f0 + warp) / NI, ii = (f0 + warp) - ((f0 + warp) / NI) * NI;
-  int cu = iu, ci = ii;
+  int ci = ii;
   auto try_issue = [&]() {
     while (nin < kSlots) {
       const int f = f0 + warp + 4 * kiss;
       if (f >= f1) break;
-      const int sz = ii < NG ? cq : cr;
+      const uint32_t sz = ii < NG ? cq : cr;
       int off;
       if (nin == 0) {
         rhead = rtail = 0;
         wrapped = false;
         off = 0;
       } else if (!wrapped) {
-        if (rhead + sz <= L.ring) {
+        if (rhead + static_cast<int>(sz) <= L.ring) {
           off = rhead;
-        } else if (sz <= rtail) {
+        } else if (static_cast<int>(sz) <= rtail) {
           rend = rhead;
           wrapped = true;
           off = 0;
@@ -444,15 +501,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           break;
         }
       } else {
-        if (rhead + sz <= rtail) off = rhead;
+        if (rhead + static_cast<int>(sz) <= rtail) off = rhead;
         else break;
       }
-      rhead = off + sz;
+      rhead = off + static_cast<int>(sz);
       if (lane == 0) {
         const int st = kiss & (kSlots - 1);
         const int u = iu, i = ii;
         uint8_t* dst = ring + off;
-        fence_proxy_async_smem();
         if (i < NG) {
           const uint8_t* rec = p.records + u * p.unit_rec_stride + static_cast<int64_t>(i / NS) * p.rec_bytes;
           if (NS == 1) {
@@ -461,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           } else {
             const int t0 = (i % NS) * kSlice;
             const uint32_t kbytes = kSlice * WK * 4, vbytes = kSlice * WV * 4;
-            mbar_arrive_expect_tx(&wbar[st], static_cast<uint32_t>(cq));
+            mbar_arrive_expect_tx(&wbar[st], cq);
             bulk_g2s(dst, rec + t0 * WK * 4, kbytes, &wbar[st]);
             bulk_g2s(dst + kbytes, rec + p.G * WK * 4 + t0 * WV * 4, vbytes, &wbar[st]);
             bulk_g2s(dst + kbytes + vbytes, rec + p.G * (WK + WV) * 4, 4 * D, &wbar[st]);
@@ -487,30 +543,40 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   };
   try_issue();
 
+  // ---------------- query rows of a unit, double-buffered bulk copies
+  // (rows past gqa are never read: the tables test h < gqa)
+  uint64_t* qbar = bars + kWarps * kSlots;
+  const uint32_t qbytes = static_cast<uint32_t>(p.gqa * D * 2);
+  auto issue_q = [&](int u, int buf) {
+    mbar_arrive_expect_tx(&qbar[buf], qbytes);
+    bulk_g2s(qs + buf * H * D, p.q + static_cast<int64_t>(u) * p.gqa * D, qbytes, &qbar[buf]);
+  };
+  if (tid == 0) {
+    mbar_init(&qbar[0], 1);
+    mbar_init(&qbar[1], 1);
+    fence_mbar_init();
+    issue_q(u_first, 0);
+    if (u_first + 1 <= u_last) issue_q(u_first + 1, 1);
+  }
+  __syncthreads();  // query barriers initialised before anyone waits on them
+
   const __half2 negmask = part ? __float2half2_rn(-1.0f) : __float2half2_rn(0.0f);
-  const float alpha = p.alpha;
+  const float alpha = p.alpha;  // residual scores (fp16 keys)
+  // quantized scores carry 2^(Pmax - 24) (subnormal codes, scaled query)
+  const float alpha_q = p.alpha * (16777216.0f / static_cast<float>(1 << key_pos_max<KB>()));
   const uint32_t vhalf_sel = (g & 1) ? 0x7632u : 0x5410u;  // 2-bit values, D = 64
-  const int u_first = f0 / NI, u_last = (f1 - 1) / NI;
   bool failed = false;
 
   for (int u = u_first; u <= u_last; ++u) {
     const int seg_hi = ((u + 1) * NI < f1) ? (u + 1) * NI : f1;
     const int b = u / p.kv_heads, kvh = u - b * p.kv_heads;
 
-    // ---------------- per-unit query tables
-    for (int idx = tid; idx < H * D / 2; idx += kThreads) {
-      const int h = idx / (D / 2), c2 = idx % (D / 2);
-      __half2 v = __float2half2_rn(0.0f);
-      if (h < p.gqa)
-        v = reinterpret_cast<const __half2*>(p.q + (static_cast<int64_t>(b) * p.kv_heads * p.gqa +
-                                                    static_cast<int64_t>(kvh) * p.gqa + h) * D)[c2];
-      reinterpret_cast<__half2*>(qs)[idx] = v;
-    }
-    __syncthreads();
+    // ---------------- per-unit query tables (from the prefetched query rows)
+    const int seg = u - u_first;
+    const __half* qu = qs + (seg & 1) * H * D;
+    if (!failed && !mbar_wait(&qbar[seg & 1], static_cast<uint32_t>((seg >> 1) & 1), p.err)) failed = true;
     {
       // every warp fills a quarter of the per-lane tables (lane = tid & 31)
-      uint32_t* qp = qp_tab + lane * QPS;
-      uint32_t* qr = qr_tab + lane * QRS;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + (g >> 1);
@@ -519,20 +585,24 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           int ca, cb;
           key_pair_channels<KB, D>(tig, pi, ca, cb);
           const __half z0 = __float2half(0.0f);
-          const __half qa = (live && ca >= 0) ? qs[h * D + ca] : z0;
-          const __half qb = (live && cb >= 0) ? qs[h * D + cb] : z0;
-          qp[j * NPK + pi] = h2_as_u32(__halves2half2(qa, qb));
+          const __half qa = (live && ca >= 0) ? qu[h * D + ca] : z0;
+          const __half qb = (live && cb >= 0) ? qu[h * D + cb] : z0;
+          const __half2 q2 = __halves2half2(qa, qb);
+          qp_tab[kt_idx(j, pi, lane)] = h2_as_u32(q2);
+          const float f = static_cast<float>(1 << (key_pos_max<KB>() - key_pos<KB, D>(pi)));
+          qps_tab[kt_idx(j, pi, lane)] = h2_as_u32(__hmul2(q2, __float2half2_rn(f)));
         }
         for (int kk = warp; kk < KS; kk += kWarps) {
           for (int rr = 0; rr < 2; ++rr) {
             const int c = 16 * kk + 8 * rr + 2 * tig;
-            qr[(j * KS + kk) * 2 + rr] =
-                (live && !part) ? h2_as_u32(__halves2half2(qs[h * D + c], qs[h * D + c + 1])) : 0u;
+            qr_tab[rt_idx(j, kk, lane) + rr] =
+                (live && !part) ? h2_as_u32(__halves2half2(qu[h * D + c], qu[h * D + c + 1])) : 0u;
           }
         }
       }
     }
     __syncthreads();
+    if (tid == 0 && u + 2 <= u_last) issue_q(u + 2, seg & 1);
 
     // ---------------- warp state for this unit
     float m[NT], l[NT], vb[NT];
@@ -611,17 +681,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
         const __half2* Vsz = reinterpret_cast<const __half2*>(Kz + D);
 
         uint32_t qp[NT][NPK];
-        {
-          const uint32_t* src = qp_tab + lane * QPS;
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
+        for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int pi = 0; pi < NPK; pi += 2) {
-              const uint2 v = *reinterpret_cast<const uint2*>(src + j * NPK + pi);
-              qp[j][pi] = v.x;
-              qp[j][pi + 1] = v.y;
-            }
-        }
+          for (int pi = 0; pi < NPK; pi += 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(qp_tab + kt_idx(j, pi, lane));
+            qp[j][pi] = v.x;
+            qp[j][pi + 1] = v.y;
+          }
+        // key codes arrive as code * 2^(pos - 24): the scaled query carries
+        // 2^(Pmax - pos), so every score product is scaled by 2^(Pmax - 24)
+        constexpr float kScoreScale = static_cast<float>(1 << key_pos_max<KB>()) / 16777216.0f;
         // zero and scale pairs in key-pair order
         uint32_t zp[NPK], sp[NPK];
         if constexpr (KB == 3) {
@@ -679,45 +749,54 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           for (int kk = 0; kk < KSK; ++kk)
             mma_16816((kk & 1) ? c1 : c0, zp[2 * kk], zp[2 * kk], zp[2 * kk + 1], zp[2 * kk + 1], qp[j][2 * kk],
                       qp[j][2 * kk + 1]);
-          bias[j] = c0[0] + c1[0];
+          bias[j] = (c0[0] + c1[0]) * kScoreScale;  // in the scaled score domain
         }
-        // folded query q~ = q * s: hi part in even columns, lo part in odd ones
+        // folded query q~ = q * s (scaled): hi part in even columns, lo part in odd ones
         uint32_t bq[NT][NPK];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int pi = 0; pi < NPK; ++pi) {
-            if constexpr (KB == 3) {
-              // fp32 products: the 2-bit fields use s2 = (s*7)/3 (an fp32 value)
-              int ca, cb;
-              key_pair_channels<KB, D>(tig, pi, ca, cb);
-              const float2 qf = __half22float2(u32_as_h2(qp[j][pi]));
-              float2 sf = __half22float2(u32_as_h2(sp[pi]));
-              if (ca >= 0 && ca % 11 == 10) sf.x = __fdiv_rn(__fmul_rn(sf.x, 7.0f), 3.0f);
-              if (cb >= 0 && cb % 11 == 10) sf.y = __fdiv_rn(__fmul_rn(sf.y, 7.0f), 3.0f);
-              uint32_t hi, lo;
-              split_pair(qf.x * sf.x, qf.y * sf.y, hi, lo);
-              bq[j][pi] = part ? lo : hi;
-            } else {
-              const __half2 qq = u32_as_h2(qp[j][pi]);
-              const __half2 ss = u32_as_h2(sp[pi]);
-              const __half2 hi = __hmul2(qq, ss);
-              bq[j][pi] = h2_as_u32(__hfma2(qq, ss, __hmul2(hi, negmask)));
+          for (int pi = 0; pi < NPK; pi += 2) {
+            const uint2 q2 = *reinterpret_cast<const uint2*>(qps_tab + kt_idx(j, pi, lane));
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t qsc = h2 ? q2.y : q2.x;
+              const int pj = pi + h2;
+              if constexpr (KB == 3) {
+                // fp32 products: the 2-bit fields use s2 = (s*7)/3 (an fp32 value)
+                int ca, cb;
+                key_pair_channels<KB, D>(tig, pj, ca, cb);
+                const float2 qf = __half22float2(u32_as_h2(qsc));
+                float2 sf = __half22float2(u32_as_h2(sp[pj]));
+                if (ca >= 0 && ca % 11 == 10) sf.x = __fdiv_rn(__fmul_rn(sf.x, 7.0f), 3.0f);
+                if (cb >= 0 && cb % 11 == 10) sf.y = __fdiv_rn(__fmul_rn(sf.y, 7.0f), 3.0f);
+                uint32_t hi, lo;
+                split_pair(qf.x * sf.x, qf.y * sf.y, hi, lo);
+                bq[j][pj] = part ? lo : hi;
+              } else {
+                const __half2 qq = u32_as_h2(qsc);
+                const __half2 ss = u32_as_h2(sp[pj]);
+                const __half2 hi = __hmul2(qq, ss);
+                bq[j][pj] = h2_as_u32(__hfma2(qq, ss, __hmul2(hi, negmask)));
+              }
             }
           }
 
         // ---- scores of the slice's 32 tokens: tiles 0 (tokens 0..15) and 1 (16..31);
-        // rows g and g+8 of each; two accumulator chains per tile
+        // rows g and g+8 of each; two accumulator chains per tile (the bias is
+        // added afterwards, so these chains do not wait for the bias MMAs)
         float sc[2][NT][4];
         {
           float sx[2][NT][4];
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              sc[t][j][0] = bias[j]; sc[t][j][1] = 0.0f; sc[t][j][2] = bias[j]; sc[t][j][3] = 0.0f;
-              sx[t][j][0] = 0.0f; sx[t][j][1] = 0.0f; sx[t][j][2] = 0.0f; sx[t][j][3] = 0.0f;
-            }
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                sc[t][j][q4] = 0.0f;
+                sx[t][j][q4] = 0.0f;
+              }
           uint32_t e[4][NPK];
 #pragma unroll
           for (int rw = 0; rw < 4; ++rw) key_row_pairs<KB, D>(Kc + (8 * rw + g) * WK, tig, e[rw]);
@@ -736,6 +815,54 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) sc[t][j][q4] += sx[t][j][q4];
         }
+
+        // ---- value code pairs of both tiles (independent of the softmax)
+        constexpr int NE = (VB == 3) ? 2 * VS_::MT3 : NP;
+        uint32_t hv[2][2][NE];   // [tile][token pair (tig,tig+4) | (tig+8,tig+12)][entry]
+        uint32_t h2v[2][2][2];   // 3-bit values: 2-bit-field tile entries
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int tb = 16 * t;
+          if constexpr (VB == 3) {
+            uint32_t wa[4], wbw[4];
+            const int wA = (D == 128) ? g : (g < 6 ? g : 0);
+            const int wB = 8 + (g >> 1);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint32_t* row = Vc + (tb + tig + 4 * q4) * WV;
+              wa[q4] = (D == 128 || g < 6) ? row[wA] : 0u;
+              wbw[q4] = (D == 128) ? row[wB] : 0u;
+            }
+            const int hsh = 15 * (g & 1);
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+              uint32_t* Hh = hv[t][pr];
+              const uint32_t a0 = wa[2 * pr], a1 = wa[2 * pr + 1];
+              lo5(a0, a1, Hh);
+              lo5(a0 >> 15, a1 >> 15, Hh + 5);
+              h2v[t][pr][0] = (D == 128 || g < 5) ? slot10_pair(a0, a1) : 0u;
+              if constexpr (D == 128) {
+                const uint32_t b0 = wbw[2 * pr], b1 = wbw[2 * pr + 1];
+                lo5(b0 >> hsh, b1 >> hsh, Hh + 10);
+                Hh[15] = 0u;
+                h2v[t][pr][1] = ((g & 1) == 0 && wB <= 10) ? slot10_pair(b0, b1) : 0u;
+              } else {
+                h2v[t][pr][1] = 0u;
+              }
+            }
+          } else {
+            constexpr int VW = VS_::VW;
+            const int voff = (VB == 2 && D == 64) ? (g >> 1) : g * VW;
+            uint32_t w0[VW], w1[VW], w2[VW], w3[VW];
+            lds_words<VW>(w0, Vc + (tb + tig) * WV + voff);
+            lds_words<VW>(w1, Vc + (tb + tig + 4) * WV + voff);
+            lds_words<VW>(w2, Vc + (tb + tig + 8) * WV + voff);
+            lds_words<VW>(w3, Vc + (tb + tig + 12) * WV + voff);
+            v_pairs<VB, D>(w0, w1, vhalf_sel, hv[t][0]);
+            v_pairs<VB, D>(w2, w3, vhalf_sel, hv[t][1]);
+          }
+        }
+
         // raw scores: s[t][j][0] token 16t+g, [1] token 16t+g+8; m is kept in
         // units of alpha * raw (log2 domain), p = 2^(alpha*raw - m)
         float s[2][NT][2];
@@ -744,10 +871,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
         for (int j = 0; j < NT; ++j) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            s[t][j][0] = sc[t][j][0] + sc[t][j][1];
-            s[t][j][1] = sc[t][j][2] + sc[t][j][3];
+            s[t][j][0] = (sc[t][j][0] + sc[t][j][1]) + bias[j];
+            s[t][j][1] = (sc[t][j][2] + sc[t][j][3]) + bias[j];
           }
-          tmax[j] = alpha * fmaxf(fmaxf(s[0][j][0], s[0][j][1]), fmaxf(s[1][j][0], s[1][j][1]));
+          tmax[j] = alpha_q * fmaxf(fmaxf(s[0][j][0], s[0][j][1]), fmaxf(s[1][j][0], s[1][j][1]));
         }
         softmax_update(tmax);
         float2 sz[2][2];
@@ -762,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           uint32_t b01[NT], b23[NT], c01[NT], c23[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            const float pa = ex2(fmaf(s[t][j][0], alpha, -m[j])), pb = ex2(fmaf(s[t][j][1], alpha, -m[j]));
+            const float pa = ex2(fmaf(s[t][j][0], alpha_q, -m[j])), pb = ex2(fmaf(s[t][j][1], alpha_q, -m[j]));
             l[j] += pa + pb;
             vb[j] = fmaf(pa, sz[t][0].y, fmaf(pb, sz[t][1].y, vb[j]));
             uint32_t hi, lo;
@@ -776,61 +903,28 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
             }
           }
           // ---- p~.V over tokens 16t + (tig, tig+4 | tig+8, tig+12), rows = channels
-          const int tb = 16 * t;
           if constexpr (VB == 3) {
             constexpr int MT3 = VS_::MT3;
-            constexpr int NE = 2 * MT3;
-            uint32_t wa[4], wbw[4];
-            const int wA = (D == 128) ? g : (g < 6 ? g : 0);
-            const int wB = 8 + (g >> 1);
+            // rows g / g+8 of tile mt (see vq_channel): d128 pairs entries of equal
+            // bit position, d64 takes fields mt / 5 + mt of the same word
+            constexpr int lo128[8] = {0, 5, 10, 1, 6, 11, 2, 12}, hi128[8] = {3, 8, 13, 4, 9, 14, 7, 15};
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const uint32_t* row = Vc + (tb + tig + 4 * q4) * WV;
-              wa[q4] = (D == 128 || g < 6) ? row[wA] : 0u;
-              wbw[q4] = (D == 128) ? row[wB] : 0u;
-            }
-            const int hsh = 15 * (g & 1);
-            uint32_t h01[NE], h23[NE], t01[2], t23[2];
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-              uint32_t* Hh = pr ? h23 : h01;
-              uint32_t* T2 = pr ? t23 : t01;
-              const uint32_t a0 = wa[2 * pr], a1 = wa[2 * pr + 1];
-              lo5(a0, a1, Hh);
-              lo5(a0 >> 15, a1 >> 15, Hh + 5);
-              T2[0] = (D == 128 || g < 5) ? slot10_pair(a0, a1) : 0u;
-              if constexpr (D == 128) {
-                const uint32_t b0 = wbw[2 * pr], b1 = wbw[2 * pr + 1];
-                lo5(b0 >> hsh, b1 >> hsh, Hh + 10);
-                Hh[15] = 0u;
-                T2[1] = ((g & 1) == 0 && wB <= 10) ? slot10_pair(b0, b1) : 0u;
-              } else {
-                T2[1] = 0u;
-              }
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT3; ++mt)
+            for (int mt = 0; mt < MT3; ++mt) {
+              const int el = (D == 128) ? lo128[mt] : mt, eh = (D == 128) ? hi128[mt] : MT3 + mt;
 #pragma unroll
               for (int j = 0; j < NT; ++j)
-                mma_16816(acc[mt][j], h01[mt], h01[MT3 + mt], h23[mt], h23[MT3 + mt], b01[j], b23[j]);
+                mma_16816(acc[mt][j], hv[t][0][el], hv[t][0][eh], hv[t][1][el], hv[t][1][eh], b01[j], b23[j]);
+            }
 #pragma unroll
-            for (int j = 0; j < NT; ++j) mma_16816(acc[MT3][j], t01[0], t01[1], t23[0], t23[1], c01[j], c23[j]);
+            for (int j = 0; j < NT; ++j)
+              mma_16816(acc[MT3][j], h2v[t][0][0], h2v[t][0][1], h2v[t][1][0], h2v[t][1][1], c01[j], c23[j]);
           } else {
-            constexpr int VW = VS_::VW;
-            const int voff = (VB == 2 && D == 64) ? (g >> 1) : g * VW;
-            uint32_t w0[VW], w1[VW], w2[VW], w3[VW];
-            lds_words<VW>(w0, Vc + (tb + tig) * WV + voff);
-            lds_words<VW>(w1, Vc + (tb + tig + 4) * WV + voff);
-            lds_words<VW>(w2, Vc + (tb + tig + 8) * WV + voff);
-            lds_words<VW>(w3, Vc + (tb + tig + 12) * WV + voff);
-            uint32_t h01[NP], h23[NP];
-            v_pairs<VB, D>(w0, w1, vhalf_sel, h01);
-            v_pairs<VB, D>(w2, w3, vhalf_sel, h23);
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
               for (int j = 0; j < NT; ++j)
-                mma_16816(acc[mt][j], h01[mt], h01[KS + mt], h23[mt], h23[KS + mt], b01[j], b23[j]);
+                mma_16816(acc[mt][j], hv[t][0][mt], hv[t][0][KS + mt], hv[t][1][mt], hv[t][1][KS + mt], b01[j],
+                          b23[j]);
           }
         }
       } else {
@@ -846,9 +940,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
               float* dd = wo + (warp * H + h) * D;
 #pragma unroll
               for (int mt = 0; mt < MTV; ++mt) {
+                const float fs = 16777216.0f / static_cast<float>(1 << value_pos<VB, D>(mt));
                 const int c0 = vq_channel<VB, D>(g, mt, 0), c1 = vq_channel<VB, D>(g, mt, 1);
-                if (c0 >= 0) dd[c0] = acc[mt][j][0] + acc[mt][j][1] + vbt;
-                if (c1 >= 0) dd[c1] = acc[mt][j][2] + acc[mt][j][3] + vbt;
+                if (c0 >= 0) dd[c0] = fmaf(acc[mt][j][0] + acc[mt][j][1], fs, vbt);
+                if (c1 >= 0) dd[c1] = fmaf(acc[mt][j][2] + acc[mt][j][3], fs, vbt);
               }
 #pragma unroll
               for (int mt = 0; mt < MTA; ++mt)
@@ -873,7 +968,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
             sc[j][e] = 0.0f;
             sx[j][e] = 0.0f;
           }
-        const uint32_t* qrs = qr_tab + lane * QRS;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -881,9 +975,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           uint32_t a[4];
           ldsm_x4(a, Kr + tok * D + ((ch ^ (tok & 7)) * 8));
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-            mma_16816((kk & 1) ? sx[j] : sc[j], a[0], a[1], a[2], a[3], qrs[(j * KS + kk) * 2],
-                      qrs[(j * KS + kk) * 2 + 1]);
+          for (int j = 0; j < NT; ++j) {
+            const uint2 bq2 = *reinterpret_cast<const uint2*>(qr_tab + rt_idx(j, kk, lane));
+            mma_16816((kk & 1) ? sx[j] : sc[j], a[0], a[1], a[2], a[3], bq2.x, bq2.y);
+          }
         }
         float sa[NT], sb[NT], tmax[NT];
 #pragma unroll
@@ -917,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       // release the consumed item's ring space, then refill
       __syncwarp();
       {
-        const int sz = ci < NG ? cq : cr;
+        const int sz = static_cast<int>(ci < NG ? cq : cr);
         --nin;
         rtail += sz;
         if (wrapped && rtail == rend) {
@@ -927,10 +1022,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       }
       ++kcon;
       ci += 4;
-      while (ci >= NI) {
-        ci -= NI;
-        ++cu;
-      }
+      while (ci >= NI) ci -= NI;
       try_issue();
     }
 
@@ -958,9 +1050,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       } else {
 #pragma unroll
         for (int mt = 0; mt < MTV; ++mt) {
+          const float fs = 16777216.0f / static_cast<float>(1 << value_pos<VB, D>(mt));
           const int c0 = vq_channel<VB, D>(g, mt, 0), c1 = vq_channel<VB, D>(g, mt, 1);
-          if (c0 >= 0) oo[c0] = acc[mt][j][0] + acc[mt][j][1] + vbt;
-          if (c1 >= 0) oo[c1] = acc[mt][j][2] + acc[mt][j][3] + vbt;
+          if (c0 >= 0) oo[c0] = fmaf(acc[mt][j][0] + acc[mt][j][1], fs, vbt);
+          if (c1 >= 0) oo[c1] = fmaf(acc[mt][j][2] + acc[mt][j][3], fs, vbt);
         }
       }
     }
