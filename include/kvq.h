@@ -159,6 +159,38 @@ kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, 
 kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V,
                            const void* const* q, float* const* out, void* stream);
 
+/* Size of the library's own device scratch for kvq_decode_attn_noalloc():
+ * 4 MiB, a file-scope device array that every GPU which loads the library
+ * keeps until the process exits. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* kvq_decode_attn() for callers that may not allocate device memory at all.
+ *
+ * The papers have no counterpart to this entry point; it exists for callers
+ * such as plugins hosted by another runtime that owns every device
+ * allocation, or code on a latency path where cudaMalloc (which synchronises
+ * the device) is not allowed.  Such a caller may hold a cache whose buffer it
+ * cannot grow, and cannot hand the library extra workspace.
+ *
+ * Same arguments, result and errors as kvq_decode_attn(), except that the
+ * split-merge workspace (per-split partial results and one arrival counter
+ * per (batch, kv head) unit) comes from the library's static device array of
+ * KVQ_NOALLOC_SCRATCH_BYTES instead of the handle's buffer, and nothing is
+ * allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Needs align256(units * 4) + (grid + units) * gqa * (head_dim + 2) * 4
+ *     bytes, where units = batch * num_kv_heads and grid is the layer's
+ *     launch width (at most 1024 CTAs); a layer needing more returns
+ *     KVQ_ERR_CAPACITY and launches nothing.
+ *   - The first call on a device (the device current at the call) looks up the
+ *     array's device address with cudaGetSymbolAddress and keeps it; make that
+ *     first call before any stream capture.  KVQ_ERR_CUDA if the lookup fails.
+ *   - Each call clears the counters on `stream` (an asynchronous memset of
+ *     units * 4 bytes) before it launches the kernel.
+ *   - Every call on a device shares the one array: calls that overlap on the
+ *     GPU (other streams, or other handles, without ordering between them)
+ *     race on it and give wrong results.  Order them on one stream. */
+kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const void* q, float* out, void* stream);
+
 /* Describe `layer` (see kvq_layer_view). */
 kvq_status kvq_layer_view_get(const kvq_handle* h, int layer, kvq_layer_view* v);
 

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -411,3 +412,77 @@ const char* kvq_status_string(kvq_status s) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------- allocation-free decode
+//
+// kvq_decode_attn_noalloc(): the decode kernel with its split-merge workspace
+// in a static device array instead of the caller's cache buffer.  Host code
+// only sees a stand-in symbol for the array, so each device's real address is
+// looked up once with cudaGetSymbolAddress and kept.
+
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
+
+kvq_status noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const void* q, float* out,
+                                              void* stream) {
+  if (!h || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
+  if (!q || !out) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
+  if (h->tokens[layer] <= 0) return KVQ_ERR_STATE;
+  const Plan& P = h->plan;
+  const LayerPlan& lp = P.layers[layer];
+  const int grid = h->grid[layer];
+  const int64_t counter_bytes = align_up(static_cast<int64_t>(P.units) * 4, 256);
+  const int64_t partial_bytes = static_cast<int64_t>(grid + P.units) * P.gqa * (P.D + 2) * 4;
+  if (counter_bytes + partial_bytes > static_cast<int64_t>(KVQ_NOALLOC_SCRATCH_BYTES)) return KVQ_ERR_CAPACITY;
+  uint8_t* scratch = nullptr;
+  const kvq_status st = noalloc_scratch(&scratch);
+  if (st != KVQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* counters = reinterpret_cast<int32_t*>(scratch);
+  if (cudaMemsetAsync(counters, 0, static_cast<size_t>(P.units) * 4, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  DecodeParams dp;
+  dp.q = static_cast<const __half*>(q);
+  dp.out = out;
+  dp.records = h->base + lp.off_records;
+  dp.unit_rec_stride = lp.unit_rec_stride;
+  dp.res_k = reinterpret_cast<const __half*>(h->base + lp.off_res_k);
+  dp.res_v = reinterpret_cast<const __half*>(h->base + lp.off_res_v);
+  dp.res_stride = lp.res_stride_elems;
+  dp.tokens = ctrl(h, layer);
+  dp.partials = reinterpret_cast<float*>(scratch + counter_bytes);
+  dp.counters = counters;
+  dp.err = errw(h);
+  dp.units = P.units;
+  dp.kv_heads = P.Hkv;
+  dp.gqa = P.gqa;
+  dp.G = P.G;
+  dp.R = lp.R;
+  dp.rec_bytes = static_cast<int>(lp.rec_bytes);
+  dp.grid = grid;
+  dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
+  const kvq::DecodeKernel& k = h->dec[layer];
+  k.fn<<<grid, kvq::kThreads, k.smem, s>>>(dp);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}

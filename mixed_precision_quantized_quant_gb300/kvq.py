@@ -23,7 +23,7 @@ STATUS = {
 EXPORTS = (
     "kvq_cache_bytes", "kvq_create", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
     "kvq_layer_view_get", "kvq_equivalent_bits", "kvq_decode_bytes", "kvq_device_error",
-    "kvq_destroy", "kvq_status_string",
+    "kvq_destroy", "kvq_status_string", "kvq_decode_attn_noalloc",
 )
 
 
@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.kvq_append.restype = ctypes.c_int
     L.kvq_decode_attn.argtypes = [vp, ctypes.c_int, vp, vp, vp]
     L.kvq_decode_attn.restype = ctypes.c_int
+    L.kvq_decode_attn_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, vp]
+    L.kvq_decode_attn_noalloc.restype = ctypes.c_int
     L.kvq_decode_step.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                   ctypes.POINTER(vp), vp]
     L.kvq_decode_step.restype = ctypes.c_int
@@ -129,6 +131,12 @@ def kvq_append(h: int, layer: int, K: int, V: int, n_tokens: int, stream: int) -
 
 def kvq_decode_attn(h: int, layer: int, q: int, out: int, stream: int) -> None:
     _check(load().kvq_decode_attn(h, layer, q, out, stream), "kvq_decode_attn")
+
+
+def kvq_decode_attn_noalloc(h: int, layer: int, q: int, out: int, stream: int) -> None:
+    """kvq_decode_attn with the library's static device scratch: for callers
+    that may not allocate device memory (see include/kvq.h)."""
+    _check(load().kvq_decode_attn_noalloc(h, layer, q, out, stream), "kvq_decode_attn_noalloc")
 
 
 def kvq_decode_step(h: int, K: Sequence[int], V: Sequence[int], q: Sequence[int], out: Sequence[int],
