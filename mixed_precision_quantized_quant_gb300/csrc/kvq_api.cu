@@ -207,7 +207,7 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   dp.grid = h->grid[layer];
   dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
   const kvq::DecodeKernel& k = h->dec[layer];
-  k.fn<<<h->grid[layer], kvq::kThreads, k.smem, s>>>(dp);
+  k.fn<<<h->grid[layer], kvq::kDecThreads, k.smem, s>>>(dp);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
@@ -482,7 +482,7 @@ extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const vo
   dp.grid = grid;
   dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
   const kvq::DecodeKernel& k = h->dec[layer];
-  k.fn<<<grid, kvq::kThreads, k.smem, s>>>(dp);
+  k.fn<<<grid, kvq::kDecThreads, k.smem, s>>>(dp);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

@@ -41,11 +41,13 @@ __host__ __device__ constexpr int slice_bytes(int D, int G, int rec_bytes) {
   return (rec_bytes - 4 * D - 4 * G) / G * kSlice + 4 * D + 4 * kSlice;
 }
 
-// Per-warp ring of staged items: room for one residual tile plus one slice,
-// and at least two slices.
+// Per-warp ring of staged items: at least two slices, and at least one
+// residual tile (a tile waits for the ring to drain when it does not fit
+// beside the slices in flight; tiles are few, and a smaller ring fits more
+// CTAs on an SM).
 __host__ __device__ constexpr int ring_bytes(int D, int G, int rec_bytes) {
   const int sl = slice_bytes(D, G, rec_bytes), rt = kResTile * 4 * D;
-  const int need = (sl + rt > 2 * sl) ? sl + rt : 2 * sl;
+  const int need = (rt > 2 * sl) ? rt : 2 * sl;
   return (need + 127) / 128 * 128;
 }
 
@@ -58,9 +60,9 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, i
   DecodeSmem s;
   const int H = 4 * NT;
   s.ring = ring_bytes(D, G, rec_bytes);
-  int off = kWarps * s.ring;
+  int off = kDecWarps * s.ring;
   s.off_bars = off;
-  off += (kWarps * kSlots + 2) * 8;  // ring slots, then the two query buffers
+  off += (kDecWarps * kSlots + 2) * 8;  // ring slots, then the two query buffers
   s.off_qs = off;
   off += 2 * H * D * 2;              // double-buffered query rows of a unit
   // per-lane query tables, lane-interleaved in 8-byte pairs (conflict-free)
@@ -71,16 +73,16 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, i
   s.off_qr = off;
   off += 32 * NT * D / 16 * 2 * 4;   // residual (fp16 key) query table
   s.off_wm = off;
-  off += kWarps * H * 4;
+  off += kDecWarps * H * 4;
   s.off_wl = off;
-  off += kWarps * H * 4;
+  off += kDecWarps * H * 4;
   s.off_dm = off;
-  off += kWarps * H * 4;
+  off += kDecWarps * H * 4;
   s.off_flags = off;
   off += 64;
   off = (off + 15) / 16 * 16;
   s.off_wo = off;
-  off += kWarps * H * D * 4;
+  off += kDecWarps * H * D * 4;
   s.total = off;
   return s;
 }
@@ -376,7 +378,7 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
 // ------------------------------------------------------------------ kernel
 
 template <int KB, int VB, int D, int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(DecodeParams p) {
   using KS_ = KeyShape<KB, D>;
   using VS_ = ValShape<VB, D>;
   constexpr int KS = D / 16;            // residual k-steps / channel m-tiles
@@ -417,14 +419,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   // layer's decode bytes below 2^32), computed by every thread, no barrier.
   const int T = __ldcg(p.tokens);
   if (T <= 0) return;
-  const int nq = static_cast<int>(quantized_after(T, p.R, p.G));
+  const int lgG = 31 - __clz(p.G);        // G is 32, 64 or 128
+  const int nq = T < p.R ? 0 : (((T - p.R) >> lgG) + 1) << lgG;  // tokens in key groups
   const int r = T - nq;
-  const int NS = p.G / kSlice;            // slices per key group
-  const int NG = (nq / p.G) * NS;         // quantized work items (slices)
+  const int NS = p.G / kSlice;            // slices per key group (1, 2 or 4)
+  const int lgNS = NS == 4 ? 2 : NS - 1;
+  const int NG = nq / kSlice;             // quantized work items (slices)
   const int NRT = (r + kResTile - 1) / kResTile;
   const int NI = NG + NRT;
-  const uint32_t cq = slice_bytes(D, p.G, p.rec_bytes), cr = kResTile * 4 * D;
-  const uint32_t csu = 4u * (cq > 2048u ? cq : 2048u);  // per-unit setup cost
+  constexpr uint32_t cq = kSlice * 4 * (WK + WV) + 4 * D + 4 * kSlice;  // staged slice bytes
+  constexpr uint32_t cr = kResTile * 4 * D;                             // residual tile bytes
+  constexpr uint32_t csu = 4u * (cq > 2048u ? cq : 2048u);              // per-unit setup cost
   const uint32_t Cu = csu + static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(NRT) * cr;
   const uint32_t C = static_cast<uint32_t>(p.units) * Cu;
   // a CTA range must hold at least one item start: range >= largest item + setup
@@ -437,13 +442,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   if (pid >= peff) return;
   const uint32_t CQ = C / peff_u, CR = C - CQ * peff_u;
   auto range_start = [&](uint32_t pp) -> uint32_t { return pp * CQ + (pp < CR ? pp : CR); };
-  auto item_start = [&](int f) -> uint32_t {
-    const int u = f / NI, i = f - u * NI;
+  // start of item i of unit u in the cost order
+  auto item_start = [&](int u, int i) -> uint32_t {
     return static_cast<uint32_t>(u) * Cu + csu +
            (i < NG ? static_cast<uint32_t>(i) * cq
                    : static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(i - NG) * cr);
   };
-  auto first_item_at = [&](uint32_t x) -> int {  // first flat item starting at or after x
+  // first item starting at or after x, as (unit, item) with item < NI
+  auto first_item_at = [&](uint32_t x, int& u_out, int& i_out) {
     const uint32_t u = x / Cu;
     const uint32_t ox = x - u * Cu;
     int i;
@@ -455,16 +461,41 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       else if (o <= static_cast<uint32_t>(NG) * cq) i = NG;
       else i = NG + static_cast<int>((o - static_cast<uint32_t>(NG) * cq + cr - 1) / cr);
     }
-    return static_cast<int>(u) * NI + i;
+    u_out = static_cast<int>(u);
+    i_out = i;
+    if (i_out >= NI) {
+      ++u_out;
+      i_out = 0;
+    }
   };
-  auto owner = [&](int f) -> int {  // CTA whose range holds item f's start
-    const uint32_t x = item_start(f);
+  auto owner_of = [&](uint32_t x) -> int {  // CTA whose range holds cost offset x
     const uint32_t big = CR * (CQ + 1);
     return x < big ? static_cast<int>(x / (CQ + 1)) : static_cast<int>(CR + (x - big) / CQ);
   };
-  const int f0 = first_item_at(range_start(pid));
-  const int f1 = first_item_at(range_start(pid + 1));
-  const int u_first = f0 / NI, u_last = (f1 - 1) / NI;
+  int u0, i0, u1, i1;
+  first_item_at(range_start(pid), u0, i0);
+  first_item_at(range_start(pid + 1), u1, i1);
+  // flat item indices f = u*NI + i stay below 2^31: every item costs more
+  // than 1024 of the fewer than 2^32 cost units
+  const int f0 = u0 * NI + i0, f1 = u1 * NI + i1;
+  const int u_first = u0, u_last = i1 == 0 ? u1 - 1 : u1;
+
+  // ---------------- query rows of a unit, double-buffered bulk copies
+  // (issued before the ring copies: the query tables gate every item;
+  // rows past gqa are never read, the tables test h < gqa)
+  uint64_t* qbar = bars + kDecWarps * kSlots;
+  const uint32_t qbytes = static_cast<uint32_t>(p.gqa * D * 2);
+  auto issue_q = [&](int u, int buf) {
+    mbar_arrive_expect_tx(&qbar[buf], qbytes);
+    bulk_g2s(qs + buf * H * D, p.q + static_cast<int64_t>(u) * p.gqa * D, qbytes, &qbar[buf]);
+  };
+  if (tid == 0) {
+    mbar_init(&qbar[0], 1);
+    mbar_init(&qbar[1], 1);
+    fence_mbar_init();
+    issue_q(u_first, 0);
+    if (u_first + 1 <= u_last) issue_q(u_first + 1, 1);
+  }
 
   // ---------------- per-warp ring of staged items (kSlots copies in flight)
   uint8_t* ring = smem + warp * L.ring;
@@ -478,11 +509,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
   int rhead = 0, rtail = 0, rend = 0, nin = 0, kiss = 0, kcon = 0;
   bool wrapped = false;
   // (unit, item) of the next item to issue / to consume, advanced without division
-  int iu = (f0 + warp) / NI, ii = (f0 + warp) - ((f0 + warp) / NI) * NI;
+  int iu = u0, ii = i0 + warp;
+  while (ii >= NI) {
+    ii -= NI;
+    ++iu;
+  }
   int ci = ii;
   auto try_issue = [&]() {
     while (nin < kSlots) {
-      const int f = f0 + warp + 4 * kiss;
+      const int f = f0 + warp + kDecWarps * kiss;
       if (f >= f1) break;
       const uint32_t sz = ii < NG ? cq : cr;
       int off;
@@ -510,12 +545,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
         const int u = iu, i = ii;
         uint8_t* dst = ring + off;
         if (i < NG) {
-          const uint8_t* rec = p.records + u * p.unit_rec_stride + static_cast<int64_t>(i / NS) * p.rec_bytes;
+          const uint8_t* rec = p.records + u * p.unit_rec_stride + static_cast<int64_t>(i >> lgNS) * p.rec_bytes;
           if (NS == 1) {
             mbar_arrive_expect_tx(&wbar[st], static_cast<uint32_t>(p.rec_bytes));
             bulk_g2s(dst, rec, static_cast<uint32_t>(p.rec_bytes), &wbar[st]);
           } else {
-            const int t0 = (i % NS) * kSlice;
+            const int t0 = (i & (NS - 1)) * kSlice;
             const uint32_t kbytes = kSlice * WK * 4, vbytes = kSlice * WV * 4;
             mbar_arrive_expect_tx(&wbar[st], cq);
             bulk_g2s(dst, rec + t0 * WK * 4, kbytes, &wbar[st]);
@@ -534,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       }
       ++nin;
       ++kiss;
-      ii += 4;
+      ii += kDecWarps;
       while (ii >= NI) {
         ii -= NI;
         ++iu;
@@ -542,22 +577,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
     }
   };
   try_issue();
-
-  // ---------------- query rows of a unit, double-buffered bulk copies
-  // (rows past gqa are never read: the tables test h < gqa)
-  uint64_t* qbar = bars + kWarps * kSlots;
-  const uint32_t qbytes = static_cast<uint32_t>(p.gqa * D * 2);
-  auto issue_q = [&](int u, int buf) {
-    mbar_arrive_expect_tx(&qbar[buf], qbytes);
-    bulk_g2s(qs + buf * H * D, p.q + static_cast<int64_t>(u) * p.gqa * D, qbytes, &qbar[buf]);
-  };
-  if (tid == 0) {
-    mbar_init(&qbar[0], 1);
-    mbar_init(&qbar[1], 1);
-    fence_mbar_init();
-    issue_q(u_first, 0);
-    if (u_first + 1 <= u_last) issue_q(u_first + 1, 1);
-  }
   __syncthreads();  // query barriers initialised before anyone waits on them
 
   const __half2 negmask = part ? __float2half2_rn(-1.0f) : __float2half2_rn(0.0f);
@@ -581,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + (g >> 1);
         const bool live = h < p.gqa;
-        for (int pi = warp; pi < NPK; pi += kWarps) {
+        for (int pi = warp; pi < NPK; pi += kDecWarps) {
           int ca, cb;
           key_pair_channels<KB, D>(tig, pi, ca, cb);
           const __half z0 = __float2half(0.0f);
@@ -592,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
           const float f = static_cast<float>(1 << (key_pos_max<KB>() - key_pos<KB, D>(pi)));
           qps_tab[kt_idx(j, pi, lane)] = h2_as_u32(__hmul2(q2, __float2half2_rn(f)));
         }
-        for (int kk = warp; kk < KS; kk += kWarps) {
+        for (int kk = warp; kk < KS; kk += kDecWarps) {
           for (int rr = 0; rr < 2; ++rr) {
             const int c = 16 * kk + 8 * rr + 2 * tig;
             qr_tab[rt_idx(j, kk, lane) + rr] =
@@ -621,21 +640,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
 
     // online-softmax update: tmax = max of this tile's scaled scores per head
     auto softmax_update = [&](const float (&tmax_in)[NT]) {
-      float tmax[NT];
+      // m only moves when some lane's own maximum passes it by more than 8
+      // (log2 units); the lanes of a head reduce their maxima only then
       bool need = false;
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        float t = tmax_in[j];
-        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 4));
-        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
-        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
-        tmax[j] = t;
-        need |= t > m[j] + 8.0f;
-      }
+      for (int j = 0; j < NT; ++j) need |= tmax_in[j] > m[j] + 8.0f;
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          const float mn = fmaxf(m[j], tmax[j]);
+          float t = tmax_in[j];
+          t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 4));
+          t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
+          t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
+          const float mn = fmaxf(m[j], t);
           const float f = (mn == -INFINITY) ? 1.0f : ex2(m[j] - mn);
           m[j] = mn;
           l[j] *= f;
@@ -661,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
     };
 
     while (true) {
-      const int f = f0 + warp + 4 * kcon;
+      const int f = f0 + warp + kDecWarps * kcon;
       if (f >= seg_hi) break;
       const int st = kcon & (kSlots - 1);
       const uint32_t ph = static_cast<uint32_t>((kcon >> 2) & 1);
@@ -1021,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
         }
       }
       ++kcon;
-      ci += 4;
+      ci += kDecWarps;
       while (ci >= NI) ci -= NI;
       try_issue();
     }
@@ -1060,19 +1077,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
     __syncthreads();
 
     // ---------------- CTA merge of the warps, then output or partial
-    const int pf = owner(u * NI), pl = owner(u * NI + NI - 1);
+    const int pf = owner_of(item_start(u, 0)), pl = owner_of(item_start(u, NI - 1));
     const int nparts = pl - pf + 1;
     const int64_t qrow = (static_cast<int64_t>(b) * p.kv_heads + kvh) * p.gqa;  // first query head row
     const int stride_slot = p.gqa * (D + 2);
     float* slot = p.partials + static_cast<int64_t>(pid + u) * stride_slot;
-    for (int idx = tid; idx < p.gqa * D; idx += kThreads) {
+    for (int idx = tid; idx < p.gqa * D; idx += kDecThreads) {
       const int h = idx / D, c = idx % D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * H + h]);
+      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w * H + h]);
       float O = 0.0f, Lsum = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < kDecWarps; ++w) {
         const float mw = wm[w * H + h];
         if (mw == -INFINITY) continue;
         const float f = ex2(mw - M);
@@ -1090,28 +1107,48 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_kernel(Decod
       }
     }
     if (nparts > 1) {
-      __threadfence();
+      // the last CTA of the unit to arrive merges every split's partial
       __syncthreads();
       if (tid == 0) {
-        const int prev = atomicAdd(p.counters + u, 1);
+        const int prev = atomic_add_acq_rel(p.counters + u, 1);
         flags[8] = (prev == nparts - 1) ? 1 : 0;
       }
       __syncthreads();
       if (flags[8]) {
-        __threadfence();
-        for (int idx = tid; idx < p.gqa * D; idx += kThreads) {
-          const int h = idx / D, c = idx % D;
-          float M = -INFINITY;
-          for (int sidx = pf; sidx <= pl; ++sidx)
-            M = fmaxf(M, __ldcg(p.partials + static_cast<int64_t>(sidx + u) * stride_slot + p.gqa * D + 2 * h));
-          float O = 0.0f, Lsum = 0.0f;
-          for (int sidx = pf; sidx <= pl; ++sidx) {
-            const float* ps = p.partials + static_cast<int64_t>(sidx + u) * stride_slot;
-            const float f = ex2(__ldcg(ps + p.gqa * D + 2 * h) - M);
-            O += __ldcg(ps + h * D + c) * f;
-            Lsum += __ldcg(ps + p.gqa * D + 2 * h + 1) * f;
+        // one pass over the splits with a running (max, sum, output) per
+        // element; a split's loads do not depend on the running values, so
+        // the loads of several splits are in flight together
+        constexpr int PER = H * D / kDecThreads;
+        const int nout = p.gqa * D;
+        float Mr[PER], Lr[PER], Or[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+          Mr[k] = -INFINITY;
+          Lr[k] = 0.0f;
+          Or[k] = 0.0f;
+        }
+#pragma unroll 4
+        for (int sidx = pf; sidx <= pl; ++sidx) {
+          const float* ps = p.partials + static_cast<int64_t>(sidx + u) * stride_slot;
+#pragma unroll
+          for (int k = 0; k < PER; ++k) {
+            const int idx = tid + k * kDecThreads;
+            if (idx < nout) {
+              const int h = idx / D;
+              const float ms = __ldcg(ps + nout + 2 * h), ls = __ldcg(ps + nout + 2 * h + 1);
+              const float os = __ldcg(ps + idx);
+              const float mn = fmaxf(Mr[k], ms);
+              const float fa = ex2(Mr[k] - mn), fb = ex2(ms - mn);
+              Or[k] = fmaf(Or[k], fa, os * fb);
+              Lr[k] = fmaf(Lr[k], fa, ls * fb);
+              Mr[k] = mn;
+            }
           }
-          p.out[(qrow + h) * D + c] = O / Lsum;
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+          const int idx = tid + k * kDecThreads;
+          if (idx < nout) p.out[qrow * D + idx] = Or[k] / Lr[k];
         }
         if (tid == 0) p.counters[u] = 0;
       }

@@ -30,7 +30,7 @@ DecodeKernel decode_select(int kb, int vb, int D, int gqa, int G, int rec_bytes)
     return k;
   }
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(k.fn), kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(k.fn), kDecThreads,
                                                     k.smem) != cudaSuccess || occ < 1) {
     k.fn = nullptr;
     return k;

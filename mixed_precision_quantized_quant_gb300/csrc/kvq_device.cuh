@@ -11,8 +11,10 @@ namespace kvq {
 
 // ---------------------------------------------------------------- constants
 
-constexpr int kThreads = 128;          // every kernel runs 4 warps per CTA
+constexpr int kThreads = 128;          // append kernels run 4 warps per CTA
 constexpr int kWarps = kThreads / 32;
+constexpr int kDecWarps = 4;                 // warps per decode-attention CTA
+constexpr int kDecThreads = 32 * kDecWarps;
 constexpr int kResTile = 16;           // residual tokens per decode work item
 constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier waits
 
@@ -77,6 +79,15 @@ struct DecodeParams {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Atomic add with acquire-release semantics at gpu scope: the release makes
+// the CTA's earlier writes (ordered before it by a CTA barrier) visible to
+// whoever acquires the counter later; the acquire does the converse.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
