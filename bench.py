@@ -220,6 +220,8 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     K.load()
     w = W.workload(args.workload)
+    if args.layers:  # profiling runs: the workload's first N layers
+        w = W.scaled(w, num_layers=args.layers, layers=tuple(w.layers[:args.layers]))
     L, B, Hq, Hkv, D = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
     steps, warm = args.steps, args.warmup
     cap = w.context + warm + steps
@@ -329,48 +331,51 @@ def run_gpu(args):
     clocks = sampler.stop()
 
     # ---- end to end through the public API, pinned host copies every step
-    h_k = torch.empty((nst, L, B, Hkv, 1, D), dtype=torch.float16).pin_memory()
-    h_v = torch.empty_like(h_k).pin_memory()
-    h_q = torch.empty((nst, L, B, Hq, D), dtype=torch.float16).pin_memory()
-    h_k.copy_(kin.cpu())
-    h_v.copy_(vin.cpu())
-    h_q.copy_(qin.cpu())
-    h_out = torch.empty((L, B, Hq, D), dtype=torch.float32).pin_memory()
-    e2e_cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, cap, device=dev)
-    with torch.cuda.stream(stream):
-        for l in range(L):
-            k, v = W.gen_kv(w, l, 0, w.context, device=dev)
-            e2e_cache.append(l, k, v, stream=stream)
-            del k, v
-        stream.synchronize()
-
-        def e2e_step(s):
-            k_cur.copy_(h_k[s], non_blocking=True)
-            v_cur.copy_(h_v[s], non_blocking=True)
-            q_cur.copy_(h_q[s], non_blocking=True)
-            e2e_cache.decode_step(Ks, Vs, Qs, Os, stream=stream)
-            h_out.copy_(outs, non_blocking=True)
+    e2e_tps = None
+    e2e_cache = None
+    if not args.no_e2e:
+        h_k = torch.empty((nst, L, B, Hkv, 1, D), dtype=torch.float16).pin_memory()
+        h_v = torch.empty_like(h_k).pin_memory()
+        h_q = torch.empty((nst, L, B, Hq, D), dtype=torch.float16).pin_memory()
+        h_k.copy_(kin.cpu())
+        h_v.copy_(vin.cpu())
+        h_q.copy_(qin.cpu())
+        h_out = torch.empty((L, B, Hq, D), dtype=torch.float32).pin_memory()
+        e2e_cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, cap, device=dev)
+        with torch.cuda.stream(stream):
+            for l in range(L):
+                k, v = W.gen_kv(w, l, 0, w.context, device=dev)
+                e2e_cache.append(l, k, v, stream=stream)
+                del k, v
             stream.synchronize()
 
-        for s in range(warm):
-            e2e_step(s)
-        _barrier(world)
-        t0 = time.perf_counter()
-        for s in range(warm, warm + steps):
-            e2e_step(s)
-        t1 = time.perf_counter()
-        _barrier(world)
-    e2e_s = _max_over_ranks(t1 - t0, world)
-    e2e_tps = world * B * steps / e2e_s
+            def e2e_step(s):
+                k_cur.copy_(h_k[s], non_blocking=True)
+                v_cur.copy_(h_v[s], non_blocking=True)
+                q_cur.copy_(h_q[s], non_blocking=True)
+                e2e_cache.decode_step(Ks, Vs, Qs, Os, stream=stream)
+                h_out.copy_(outs, non_blocking=True)
+                stream.synchronize()
+
+            for s in range(warm):
+                e2e_step(s)
+            _barrier(world)
+            t0 = time.perf_counter()
+            for s in range(warm, warm + steps):
+                e2e_step(s)
+            t1 = time.perf_counter()
+            _barrier(world)
+        e2e_s = _max_over_ranks(t1 - t0, world)
+        e2e_tps = world * B * steps / e2e_s
     h2d = L * (2 * B * Hkv * D * 2 + B * Hq * D * 2)
     d2h = L * B * Hq * D * 4
-    err = cache.device_error(stream) | e2e_cache.device_error(stream)
+    err = cache.device_error(stream) | (e2e_cache.device_error(stream) if e2e_cache is not None else 0)
     if err:
         raise RuntimeError(f"device error word {err}")
 
     peak, peak_kind = _peaks()
     achieved = dec_bytes_per_launch / (dec_ms_per_launch / 1e3) / 1e9
-    traffic = _ncu_traffic(args.workload)
+    traffic = _ncu_traffic(w.name)
     result = {
         "metric": METRIC,
         "value": round(tokens_per_s, 1),
@@ -396,8 +401,8 @@ def run_gpu(args):
                      "bytes_per_launch": int(dec_bytes_per_launch),
                      "us_per_launch": round(dec_ms_per_launch * 1e3, 3),
                      "peak_source": f"{peak_kind} HBM copy bandwidth"},
-        "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e_tps is None else {"value": round(e2e_tps, 1), "unit": "tokens/s",
+                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
@@ -412,23 +417,24 @@ def run_gpu(args):
         print(json.dumps(result))
 
 
-def _ncu_traffic(widx):
-    """DRAM bytes per decode launch from a committed ncu summary, if one
-    matches this workload and the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+def _ncu_traffic(workload_name):
+    """Mean DRAM bytes (read + write) per decode launch of one step, from the
+    committed ncu summary of this workload, if it was taken on the current
+    decode kernel source (its sha256 prefix is recorded in the summary)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_dram_{workload_name}.txt")
     try:
-        with open(path) as f:
-            d = json.load(f)
-        ent = d.get(str(widx))
-        if not ent:
-            return None
-        import hashlib
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith((" ", "#", "|")):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
         src = os.path.join(ROOT, "mixed_precision_quantized_quant_gb300", "csrc", "kvq_decode.cuh")
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if ent.get("kernel_sha") != h:
+        if kv.get("kernel_source_sha256_16") != h:
             return None
-        return ent.get("traffic_bytes_per_launch")
-    except Exception:
+        return int(float(kv["dram_bytes_per_launch_mean"]))
+    except (OSError, KeyError, ValueError):
         return None
 
 
@@ -471,6 +477,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2, help="1..5; 2 is the Llama-3.1-8B-shaped decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="profiling runs: skip the end-to-end leg")
+    ap.add_argument("--layers", type=int, default=0, help="profiling runs: only the workload's first N layers")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

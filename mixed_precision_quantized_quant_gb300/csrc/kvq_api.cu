@@ -121,6 +121,7 @@ struct kvq_handle {
   std::vector<int64_t> tokens;  // host mirror of each layer's appended tokens
   std::vector<kvq::DecodeKernel> dec;
   std::vector<int> grid;
+  std::vector<int> app_grid;  // persistent CTAs of a prefill flush launch
   StepGraph graph;
 };
 
@@ -162,20 +163,24 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   const size_t smem = kvq::append_smem_bytes(lp.kb, lp.vb, P.D, P.G, static_cast<int>(lp.rec_bytes));
   cudaError_t e = cudaSuccess;
   if (n == 1) {
+    // one CTA per unit: its flush job (if a group fills) and its new token
     ap.mode = kvq::kFlush | kvq::kResidual | kvq::kUpdateState;
     ap.ctas = P.units;
-    e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(1, P.units), smem, s);
+    e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(P.units, 1), kvq::append_block_threads(P.G), smem, s);
   } else {
     if (nflush > 0) {
+      const int64_t jobs = nflush * P.units;
+      const int ctas = static_cast<int>(jobs < h->app_grid[layer] ? jobs : h->app_grid[layer]);
       ap.mode = kvq::kFlush | (nres == 0 ? kvq::kUpdateState : 0);
-      ap.ctas = static_cast<int>(nflush * P.units);
-      e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(static_cast<unsigned>(nflush), P.units), smem, s);
+      ap.ctas = ctas;
+      e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(static_cast<unsigned>(ctas), 1),
+                               kvq::append_block_threads(P.G), smem, s);
     }
     if (e == cudaSuccess && nres > 0) {
       const int64_t chunks = (nres + 15) / 16;
       ap.mode = kvq::kResidual | kvq::kUpdateState;
       ap.ctas = static_cast<int>(chunks * P.units);
-      e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(static_cast<unsigned>(chunks), P.units), 0, s);
+      e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(static_cast<unsigned>(chunks), P.units), 128, 0, s);
     }
   }
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
@@ -251,6 +256,13 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
     int gsz = sms * k.ctas_per_sm;
     if (gsz > kMaxGrid) gsz = kMaxGrid;
     h->grid.push_back(gsz);
+    const size_t asmem = kvq::append_smem_bytes(lp.kb, lp.vb, P.D, P.G, static_cast<int>(lp.rec_bytes));
+    const int aocc = kvq::append_ctas_per_sm(lp.kb, lp.vb, P.D, kvq::append_block_threads(P.G), asmem);
+    if (aocc < 1) {
+      delete h;
+      return KVQ_ERR_UNSUPPORTED;
+    }
+    h->app_grid.push_back(sms * aocc);
   }
   if (cudaMemset(dev_buf, 0, static_cast<size_t>(P.total)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {

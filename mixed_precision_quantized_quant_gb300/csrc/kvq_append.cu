@@ -1,8 +1,11 @@
 // Fused quantize + pack + append for one layer of the mixed-precision KV cache.
 //
-// One CTA (4 warps) per (unit, job); a unit is one (batch, kv head).  A job is
-// either one key group to quantize ("flush") or a chunk of new tokens to copy
-// into the FP16 residual ring.  Keys are quantized per channel over the G
+// A unit is one (batch, kv head).  Key groups to quantize ("flush jobs") are
+// spread over persistent CTAs of 4 warps: each CTA stages the K and V rows of
+// its next group in shared memory with bulk (TMA) copies while it quantizes
+// the current one.  New tokens that stay in the FP16 residual window are
+// copied into the unit's ring by the same launch (one token per unit in a
+// decode step) or by a second launch in 16-token chunks (prefill).  Keys are quantized per channel over the G
 // tokens of a group, values per token, with
 //   scale = (max - min)/(2^b - 1) in fp32, stored fp16; zero = min;
 //   code  = clamp(rint((x - min) / scale), 0, 2^b - 1)
@@ -11,7 +14,8 @@
 // reciprocal estimate decides the code unless the quotient lies within 2^-14
 // of a rounding boundary, where the correctly rounded __fdiv_rn decides.
 //
-// Per-channel and per-token min/max use warp shuffles; packed codes are
+// Per-channel min/max runs over the staged rows, per-token min/max uses warp
+// shuffles; each scale is computed once, by one thread; packed codes are
 // assembled in shared memory and leave as one bulk (TMA) store per group.
 #include "kvq_device.cuh"
 #include "kvq_kernels.h"
@@ -25,19 +29,6 @@ struct BitsT {
 };
 
 __host__ __device__ constexpr int words_per_row(int d, int b) { return b == 3 ? (d + 10) / 11 : d * b / 32; }
-
-// code = clamp(rint(a / s), 0, qmax) with a = x - min already rounded to fp32;
-// s > 0 is the fp32 value of the stored scale, r = 1/s (rounded).
-__device__ __forceinline__ uint32_t code_of(float a, float s, float r, float qmax) {
-  const float y = __fmul_rn(a, r);
-  float q = rintf(y);
-  const float dist = fabsf(__fsub_rn(y, q));
-  if (fabsf(dist - 0.5f) <= 6.103515625e-05f) {  // 2^-14: decide with the exact quotient
-    q = rintf(__fdiv_rn(a, s));
-  }
-  q = fminf(fmaxf(q, 0.0f), qmax);
-  return static_cast<uint32_t>(q);
-}
 
 struct Scale {
   float mn;   // zero (fp16 value, exact in fp32)
@@ -66,11 +57,6 @@ __device__ __forceinline__ Scale make_scale(__half mn, __half mx, bool slot10) {
   return sc;
 }
 
-__device__ __forceinline__ uint32_t quant(float x, const Scale& sc) {
-  if (!(sc.s > 0.0f)) return 0u;
-  return code_of(__fsub_rn(x, sc.mn), sc.s, sc.r, sc.qmax);
-}
-
 __device__ __forceinline__ void h8(const uint4& v, __half (&h)[8]) {
   const __half2* p = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
@@ -97,261 +83,437 @@ __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint
   }
 }
 
-// Row chunk address of token i (absolute position) of unit u: the FP16 ring
-// if the token was appended before this call, else the caller's input.
-__device__ __forceinline__ const uint4* src_chunk(const AppendParams& p, const __half* ring, const __half* in,
-                                                  int u, int64_t i, int64_t T, int chunk, int D) {
-  if (i < T) {
-    const int slot = static_cast<int>(i % p.R);
-    const int phys = chunk ^ (slot & 7);
-    return reinterpret_cast<const uint4*>(ring + u * p.res_stride + static_cast<int64_t>(slot) * D) + phys;
-  }
-  const int64_t j = i - T;
-  return reinterpret_cast<const uint4*>(in + (static_cast<int64_t>(u) * p.n + j) * D) + chunk;
+// Shared-memory layout of the flush path.
+struct AppendSmem {
+  int tile;  // bytes of one staged [G][D] fp16 tile
+  int off_stage1, off_rec, off_ksc, off_vsc, off_vr2, off_kmn, off_kmx, off_vpart, off_bars, total;
+};
+
+// Flush CTAs run 4*G threads: each thread owns one 16-byte chunk of D/32 rows.
+__host__ __device__ constexpr int append_threads(int G) { return 4 * G; }
+
+__host__ __device__ inline AppendSmem append_smem_layout(int D, int G, int rec_bytes) {
+  AppendSmem a;
+  a.tile = G * D * 2;
+  const int warps = append_threads(G) / 32;
+  int off = 2 * a.tile;  // stage 0 at offset 0: K tile, then V tile
+  a.off_stage1 = off;
+  off += 2 * a.tile;
+  a.off_rec = off;
+  off += (rec_bytes + 127) / 128 * 128;
+  a.off_ksc = off;
+  off += D * 16;  // per channel {min, s, 1/s, qmax}, channel 8c + k at k*(D/8) + c
+  a.off_vsc = off;
+  off += G * 16;  // per token {min, s, 1/s, s2}
+  a.off_vr2 = off;
+  off += G * 4;   // per token 1/s2 (3-bit values)
+  a.off_kmn = off;
+  off += warps * D * 2;  // per warp, per channel: min over the warp's rows
+  a.off_kmx = off;
+  off += warps * D * 2;  // ... and max
+  a.off_vpart = off;
+  off += G * 4;   // per token {min, -max}
+  a.off_bars = off;
+  off += 16;
+  a.total = off;
+  return a;
 }
 
+constexpr float kNearHalf = 0.5f - 6.103515625e-05f;  // 2^-14 from a rounding boundary
+
+// code = min(rint((x - min) / s), qmax) with IEEE fp32 subtraction and
+// division: the product with 1/s decides unless it lies within 2^-14 of a
+// rounding boundary, where the correctly rounded quotient decides.  x >= min
+// always, so no lower clamp.  sc = {min, s, 1/s, qmax}; s == 0 carries
+// 1/s == 0 and gives code 0.
+__device__ __forceinline__ uint32_t quant_fast(float x, const float4& sc) {
+  const float a = __fsub_rn(x, sc.x);
+  const float y = __fmul_rn(a, sc.z);
+  float q = rintf(y);
+  if (fabsf(__fsub_rn(y, q)) >= kNearHalf && sc.z > 0.0f) q = rintf(__fdiv_rn(a, sc.y));
+  return static_cast<uint32_t>(fminf(q, sc.w));
+}
+
+// The rare exact path of quant8, kept out of line so the common path stays
+// compact.  Scales come from the shared-memory table (element k at
+// tab[k * stride]; qmax from the table when qm < 0); the eight codes return
+// as bytes, codes 0-3 in .x.
+__device__ __noinline__ uint2 quant8_exact(uint4 xv, const float4* tab, int stride, float qm) {
+  const __half2* h = reinterpret_cast<const __half2*>(&xv);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float x = (k & 1) ? __high2float(h[k >> 1]) : __low2float(h[k >> 1]);
+    float4 sc = tab[k * stride];
+    if (qm >= 0.0f) sc.w = qm;
+    const uint32_t q = quant_fast(x, sc);
+    if (k < 4) lo |= q << (8 * k);
+    else hi |= q << (8 * (k - 4));
+  }
+  return make_uint2(lo, hi);
+}
+
+// Eight codes of one 16-byte chunk, branch-free on the common path:
+// 0 <= y < 2^22, so y + 2^23 rounds y to the nearest integer (ties to even)
+// and that integer sits in the low mantissa bits.  A chunk with any quotient
+// near a rounding boundary is redone element by element by quant8_exact.
+// sc: the scales in registers, one per element (keys) or sc[0] for all
+// (values, PER = false); tab/stride/qm: the same scales in shared memory.
+template <bool PER>
+__device__ __forceinline__ void quant8(const uint4& xv, const float4* sc, const float4* tab, int stride, float qm,
+                                       uint32_t (&code)[8]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&xv);
+  bool near = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4& s = sc[PER ? k : 0];
+    const float x = (k & 1) ? __high2float(h[k >> 1]) : __low2float(h[k >> 1]);
+    const float y = __fmul_rn(__fsub_rn(x, s.x), s.z);
+    const float t = __fadd_rn(y, 8388608.0f);
+    near |= fabsf(__fsub_rn(y, __fsub_rn(t, 8388608.0f))) >= kNearHalf;
+    const uint32_t c = __float_as_uint(t) - 0x4B000000u;
+    const uint32_t q = static_cast<uint32_t>(s.w);
+    code[k] = c < q ? c : q;
+  }
+  if (near) {
+    const uint2 b = quant8_exact(xv, tab, stride, qm);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) code[k] = ((k < 4 ? b.x : b.y) >> (8 * (k & 3))) & 0xFFu;
+  }
+}
+
+// Quantizes one staged group (rows of the stage are the group's G tokens; a
+// row that came from the ring has its 16-byte chunks swizzled by t & 7) into
+// the record staging area.  Thread (chunk c, row group rg) owns chunk c of
+// rows rg + k*RG, k < D/32, and keeps them in registers from the min/max pass
+// to the code pass.
 template <int KB, int VB, int D>
-__device__ void quantize_group(const AppendParams& p, int u, int64_t grp, int64_t T, uint8_t* smem) {
+__device__ bool flush_group(const AppendParams& p, const __half* kt, const __half* vt, int nring, uint8_t* smem,
+                            const AppendSmem& L, bool staged) {
   constexpr int WK = words_per_row(D, KB);
   constexpr int WV = words_per_row(D, VB);
+  constexpr int CH = D / 8;     // 16-byte chunks per row
+  constexpr int RT = D / 32;    // rows per thread
+  constexpr int LPC = 32 / CH;  // lanes of a warp on the same chunk
   const int G = p.G;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint8_t* rec = smem;
+  const int RG = 4 * G / CH;    // row groups
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = tid % CH, rg = tid / CH;
+  uint8_t* rec = smem + L.off_rec;
   uint32_t* kc = reinterpret_cast<uint32_t*>(rec);
   uint32_t* vc = kc + G * WK;
-  __half* ks = reinterpret_cast<__half*>(vc + G * WV);
-  __half* kz = ks + D;
-  __half2* vsz = reinterpret_cast<__half2*>(kz + D);
-  uint8_t* bytes = rec + p.rec_bytes;  // 3-bit staging: [G][D] codes
-  const int64_t t0 = grp * G;
+  __half* ks16 = reinterpret_cast<__half*>(vc + G * WV);
+  __half* kz16 = ks16 + D;
+  __half2* vsz = reinterpret_cast<__half2*>(kz16 + D);
+  float4* ksc = reinterpret_cast<float4*>(smem + L.off_ksc);
+  float4* vsc = reinterpret_cast<float4*>(smem + L.off_vsc);
+  float* vr2 = reinterpret_cast<float*>(smem + L.off_vr2);
+  __half* kmn = reinterpret_cast<__half*>(smem + L.off_kmn);
+  __half* kmx = reinterpret_cast<__half*>(smem + L.off_kmx);
+  __half2* vpart = reinterpret_cast<__half2*>(smem + L.off_vpart);
+  auto key_of = [&](int t) { return t < nring ? (t & 7) : 0; };
+  // channel scales are stored element-major ([k][chunk]) so that the lanes of
+  // a row, one chunk each, read consecutive entries
+  auto ksc_at = [&](int ch) -> float4& { return ksc[(ch & 7) * CH + (ch >> 3)]; };
+  const uint4* kq = reinterpret_cast<const uint4*>(kt);
+  const uint4* vq = reinterpret_cast<const uint4*>(vt);
 
-  // ---------------- keys: per channel over the group's G tokens
+  // ---- phase 1: load the thread's chunks; key min/max per channel (over
+  // the thread's rows, then the warp's lanes on the chunk, then per warp in
+  // shared memory); value min/max per token (the row's CH lanes)
+  uint4 xk[RT], xv[RT];
+#pragma unroll
+  for (int k = 0; k < RT; ++k) {
+    const int t = rg + k * RG;
+    const int pc = c ^ key_of(t);
+    xk[k] = kq[t * CH + pc];
+    xv[k] = vq[t * CH + pc];
+  }
   {
-    constexpr int CW = D / 4;          // channels per warp
-    constexpr int LPR = CW / 8;        // lanes per token row
-    constexpr int RPL = 32 / LPR;      // token rows per warp-load
-    constexpr int NLMAX = 128 / RPL;   // loads for the largest group
-    const int r = lane / LPR, cs = lane % LPR;
-    const int cb = warp * CW + cs * 8;  // first of this lane's 8 channels
-    const int nl = G / RPL;
-    uint4 x[NLMAX];
     __half2 mn[4], mx[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      mn[k] = __float2half2_rn(65504.f);
-      mx[k] = __float2half2_rn(-65504.f);
+    for (int i = 0; i < 4; ++i) {
+      mn[i] = reinterpret_cast<const __half2*>(&xk[0])[i];
+      mx[i] = mn[i];
     }
 #pragma unroll
-    for (int it = 0; it < NLMAX; ++it) {
-      if (it < nl) {
-        const int64_t i = t0 + it * RPL + r;
-        x[it] = *src_chunk(p, p.res_k, p.K, u, i, T, cb / 8, D);
-        const __half2* h = reinterpret_cast<const __half2*>(&x[it]);
+    for (int k = 1; k < RT; ++k)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          mn[k] = __hmin2(mn[k], h[k]);
-          mx[k] = __hmax2(mx[k], h[k]);
-        }
+      for (int i = 0; i < 4; ++i) {
+        const __half2 x = reinterpret_cast<const __half2*>(&xk[k])[i];
+        mn[i] = __hmin2(mn[i], x);
+        mx[i] = __hmax2(mx[i], x);
       }
-    }
 #pragma unroll
-    for (int off = LPR; off < 32; off <<= 1) {
+    for (int off = CH; off < 32; off <<= 1)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t a = __shfl_xor_sync(0xffffffffu, h2_as_u32(mn[k]), off);
-        const uint32_t b = __shfl_xor_sync(0xffffffffu, h2_as_u32(mx[k]), off);
-        mn[k] = __hmin2(mn[k], u32_as_h2(a));
-        mx[k] = __hmax2(mx[k], u32_as_h2(b));
+      for (int i = 0; i < 4; ++i) {
+        mn[i] = __hmin2(mn[i], u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mn[i]), off)));
+        mx[i] = __hmax2(mx[i], u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(mx[i]), off)));
       }
-    }
-    Scale sc[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      sc[2 * k] = make_scale<KB>(__low2half(mn[k]), __low2half(mx[k]), (cb + 2 * k) % 11 == 10);
-      sc[2 * k + 1] = make_scale<KB>(__high2half(mn[k]), __high2half(mx[k]), (cb + 2 * k + 1) % 11 == 10);
-    }
-    if (r == 0) {
-      __half s8[8], z8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        s8[k] = sc[k].s16;
-        z8[k] = sc[k].z16;
-      }
-      *reinterpret_cast<uint4*>(ks + cb) = *reinterpret_cast<uint4*>(s8);
-      *reinterpret_cast<uint4*>(kz + cb) = *reinterpret_cast<uint4*>(z8);
-    }
-#pragma unroll
-    for (int it = 0; it < NLMAX; ++it) {
-      if (it < nl) {
-        const int t = it * RPL + r;
-        __half h[8];
-        h8(x[it], h);
-        uint32_t c[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) c[k] = quant(__half2float(h[k]), sc[k]);
-        if (KB == 3) {
-          uint32_t lo = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-          uint32_t hi = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-          *reinterpret_cast<uint2*>(bytes + t * D + cb) = make_uint2(lo, hi);
-        } else {
-          uint32_t w0, w1;
-          pack8<KB>(c, w0, w1);
-          if (KB == 8) {
-            *reinterpret_cast<uint2*>(kc + t * WK + cb / 4) = make_uint2(w0, w1);
-          } else if (KB == 4) {
-            kc[t * WK + cb / 8] = w0;
-          } else {  // KB == 2: two lanes form one word
-            const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
-            if ((cs & 1) == 0) kc[t * WK + cb / 16] = w0 | (other << 16);
-          }
-        }
-      }
+    if (lane < CH) {
+      *reinterpret_cast<uint4*>(kmn + warp * D + 8 * c) =
+          make_uint4(h2_as_u32(mn[0]), h2_as_u32(mn[1]), h2_as_u32(mn[2]), h2_as_u32(mn[3]));
+      *reinterpret_cast<uint4*>(kmx + warp * D + 8 * c) =
+          make_uint4(h2_as_u32(mx[0]), h2_as_u32(mx[1]), h2_as_u32(mx[2]), h2_as_u32(mx[3]));
     }
   }
-
-  // ---------------- values: per token over its D channels
-  {
-    constexpr int TPL = D / 8;         // lanes per token
-    constexpr int TPW = 32 / TPL;      // tokens per warp-load
-    const int sub = lane / TPL, cs = lane % TPL;
-    const int cb = cs * 8;
-    for (int t = (warp * TPW) + sub; t < G; t += kWarps * TPW) {
-      const int64_t i = t0 + t;
-      const uint4 x = *src_chunk(p, p.res_v, p.V, u, i, T, cs, D);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&x);
-      __half2 mn2 = __hmin2(__hmin2(h2[0], h2[1]), __hmin2(h2[2], h2[3]));
-      __half2 mx2 = __hmax2(__hmax2(h2[0], h2[1]), __hmax2(h2[2], h2[3]));
-      __half mn = __hmin(__low2half(mn2), __high2half(mn2));
-      __half mx = __hmax(__low2half(mx2), __high2half(mx2));
 #pragma unroll
-      for (int off = 1; off < TPL; off <<= 1) {
-        const __half a = __ushort_as_half(
-            static_cast<unsigned short>(__shfl_xor_sync(0xffffffffu, __half_as_ushort(mn), off)));
-        const __half b = __ushort_as_half(
-            static_cast<unsigned short>(__shfl_xor_sync(0xffffffffu, __half_as_ushort(mx), off)));
-        mn = __hmin(mn, a);
-        mx = __hmax(mx, b);
-      }
-      const Scale s3 = make_scale<VB>(mn, mx, false);
-      Scale s2 = s3;
-      if (VB == 3) s2 = make_scale<VB>(mn, mx, true);
-      __half h[8];
-      h8(x, h);
-      uint32_t c[8];
+  for (int k = 0; k < RT; ++k) {
+    const __half2* h = reinterpret_cast<const __half2*>(&xv[k]);
+    const __half2 m2 = __hmin2(__hmin2(h[0], h[1]), __hmin2(h[2], h[3]));
+    const __half2 M2 = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+    // (min, -max): one min-reduction serves both
+    __half2 r = __halves2half2(__hmin(__low2half(m2), __high2half(m2)),
+                               __hneg(__hmax(__low2half(M2), __high2half(M2))));
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const bool two = (VB == 3) && ((cb + k) % 11 == 10);
-        c[k] = quant(__half2float(h[k]), two ? s2 : s3);
-      }
-      if (cs == 0) vsz[t] = __halves2half2(s3.s16, s3.z16);
-      if (VB == 3) {
-        uint32_t lo = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-        uint32_t hi = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-        *reinterpret_cast<uint2*>(bytes + G * D + t * D + cb) = make_uint2(lo, hi);
-      } else {
-        uint32_t w0, w1;
-        pack8<VB>(c, w0, w1);
-        if (VB == 8) {
-          *reinterpret_cast<uint2*>(vc + t * WV + cb / 4) = make_uint2(w0, w1);
-        } else if (VB == 4) {
-          vc[t * WV + cb / 8] = w0;
-        } else {
-          const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
-          if ((cs & 1) == 0) vc[t * WV + cb / 16] = w0 | (other << 16);
-        }
-      }
-    }
+    for (int off = 1; off < CH; off <<= 1)
+      r = __hmin2(r, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(r), off)));
+    if (c == 0) vpart[rg + k * RG] = r;
   }
+  if (tid == 0) bulk_wait_read_all();  // the previous record has left the staging area
+  // every thread saw its stage arrive, or all of them stop here
+  if (__syncthreads_or(!staged)) return false;
 
-  // ---------------- 3-bit words: ten 3-bit fields and one 2-bit field
-  if (KB == 3 || VB == 3) {
-    __syncthreads();
-    if (KB == 3) {
-      for (int idx = tid; idx < G * WK; idx += kThreads) {
-        const int t = idx / WK, w = idx % WK;
-        uint32_t word = 0;
-        for (int j = 0; j < 11; ++j) {
-          const int c = 11 * w + j;
-          if (c < D) word |= static_cast<uint32_t>(bytes[t * D + c]) << (j == 10 ? 30 : 3 * j);
-        }
-        kc[idx] = word;
-      }
+  // ---- phase 2: one scale per thread (channel tid, token tid)
+  if (tid < D) {
+    // thread tid takes channel 8*(tid % CH) + tid / CH, whose table slot is tid
+    const int ch = 8 * (tid % CH) + tid / CH;
+    const int warps = 4 * G / 32;
+    __half mn = kmn[ch], mx = kmx[ch];
+    for (int w = 1; w < warps; ++w) {
+      mn = __hmin(mn, kmn[w * D + ch]);
+      mx = __hmax(mx, kmx[w * D + ch]);
     }
+    const Scale sc = make_scale<KB>(mn, mx, KB == 3 && ch % 11 == 10);
+    ksc[tid] = make_float4(sc.mn, sc.s, sc.r, sc.qmax);
+    ks16[ch] = sc.s16;
+    kz16[ch] = sc.z16;
+  }
+  if (tid < G) {
+    const __half2 r = vpart[tid];
+    const __half mn = __low2half(r), mx = __hneg(__high2half(r));
+    const Scale s3 = make_scale<VB>(mn, mx, false);
+    float s2 = s3.s, r2 = s3.r;
     if (VB == 3) {
-      for (int idx = tid; idx < G * WV; idx += kThreads) {
-        const int t = idx / WV, w = idx % WV;
-        uint32_t word = 0;
-        for (int j = 0; j < 11; ++j) {
-          const int c = 11 * w + j;
-          if (c < D) word |= static_cast<uint32_t>(bytes[G * D + t * D + c]) << (j == 10 ? 30 : 3 * j);
-        }
-        vc[idx] = word;
+      const Scale t2 = make_scale<VB>(mn, mx, true);
+      s2 = t2.s;
+      r2 = t2.r;
+    }
+    vsc[tid] = make_float4(s3.mn, s3.s, s3.r, s2);
+    vr2[tid] = r2;
+    vsz[tid] = __halves2half2(s3.s16, s3.z16);
+  }
+  __syncthreads();
+
+  // ---- phase 3: codes, packed LSB first into the record staging area
+  if constexpr (KB != 3) {
+    float4 sc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sc[k] = ksc[k * CH + c];
+#pragma unroll
+    for (int k = 0; k < RT; ++k) {
+      const int t = rg + k * RG;
+      uint32_t code[8];
+      quant8<true>(xk[k], sc, ksc + c, CH, -1.0f, code);
+      uint32_t w0, w1;
+      pack8<KB>(code, w0, w1);
+      if (KB == 8) {
+        *reinterpret_cast<uint2*>(kc + t * WK + 2 * c) = make_uint2(w0, w1);
+      } else if (KB == 4) {
+        kc[t * WK + c] = w0;
+      } else {  // KB == 2: two lanes form one word
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
+        if ((c & 1) == 0) kc[t * WK + c / 2] = w0 | (other << 16);
       }
     }
+  } else {
+    for (int idx = tid; idx < G * WK; idx += blockDim.x) {
+      const int t = idx / WK, w = idx - (idx / WK) * WK;
+      const int key = key_of(t);
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 11; ++j) {
+        const int ch = 11 * w + j;
+        if (ch < D) {
+          const __half x = kt[t * D + ((((ch >> 3) ^ key) << 3) | (ch & 7))];
+          word |= quant_fast(__half2float(x), ksc_at(ch)) << (j == 10 ? 30 : 3 * j);
+        }
+      }
+      kc[idx] = word;
+    }
   }
-
-  // ---------------- one bulk store of the finished record
-  __syncthreads();
-  if (tid == 0) {
-    fence_proxy_async_smem();
-    uint8_t* dst = p.records + static_cast<int64_t>(u) * p.unit_rec_stride + grp * p.rec_bytes;
-    bulk_s2g(dst, rec, static_cast<uint32_t>(p.rec_bytes));
-    bulk_commit();
-    bulk_wait_all();
+  if constexpr (VB != 3) {
+#pragma unroll
+    for (int k = 0; k < RT; ++k) {
+      const int t = rg + k * RG;
+      const float4 s = vsc[t];
+      const float4 sq = make_float4(s.x, s.y, s.z, static_cast<float>((1 << VB) - 1));
+      uint32_t code[8];
+      quant8<false>(xv[k], &sq, vsc + t, 0, static_cast<float>((1 << VB) - 1), code);
+      uint32_t w0, w1;
+      pack8<VB>(code, w0, w1);
+      if (VB == 8) {
+        *reinterpret_cast<uint2*>(vc + t * WV + 2 * c) = make_uint2(w0, w1);
+      } else if (VB == 4) {
+        vc[t * WV + c] = w0;
+      } else {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
+        if ((c & 1) == 0) vc[t * WV + c / 2] = w0 | (other << 16);
+      }
+    }
+  } else {
+    for (int idx = tid; idx < G * WV; idx += blockDim.x) {
+      const int t = idx / WV, w = idx - (idx / WV) * WV;
+      const int key = key_of(t);
+      const float4 s = vsc[t];
+      const float4 s3 = make_float4(s.x, s.y, s.z, 7.0f);
+      const float4 s2 = make_float4(s.x, s.w, vr2[t], 3.0f);
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 11; ++j) {
+        const int ch = 11 * w + j;
+        if (ch < D) {
+          const __half x = vt[t * D + ((((ch >> 3) ^ key) << 3) | (ch & 7))];
+          word |= quant_fast(__half2float(x), j == 10 ? s2 : s3) << (j == 10 ? 30 : 3 * j);
+        }
+      }
+      vc[idx] = word;
+    }
   }
-  __syncthreads();
+  return true;
 }
 
 // Copy new tokens [lo, hi) (absolute positions, all from this call's input)
-// into the unit's FP16 rings, 16-byte chunks swizzled by slot.
+// into the unit's FP16 rings, 16-byte chunks swizzled by slot.  A thread
+// issues up to four loads before its stores.
 template <int D>
 __device__ void write_residual(const AppendParams& p, int u, int64_t lo, int64_t hi, int64_t T) {
   constexpr int CH = D / 8;  // 16-byte chunks per row
-  const int64_t n = hi - lo;
-  for (int64_t idx = threadIdx.x; idx < n * 2 * CH; idx += kThreads) {
-    const int64_t tok = lo + idx / (2 * CH);
-    const int rem = static_cast<int>(idx % (2 * CH));
-    const int which = rem / CH, c = rem % CH;
-    const __half* in = which ? p.V : p.K;
-    __half* ring = which ? p.res_v : p.res_k;
-    const uint4 v = reinterpret_cast<const uint4*>(in + (static_cast<int64_t>(u) * p.n + (tok - T)) * D)[c];
-    const int slot = static_cast<int>(tok % p.R);
-    reinterpret_cast<uint4*>(ring + u * p.res_stride + static_cast<int64_t>(slot) * D)[c ^ (slot & 7)] = v;
+  const int n = static_cast<int>(hi - lo);
+  const int base = static_cast<int>(lo - T);
+  const int total = n * 2 * CH;
+  const int step = blockDim.x;
+  for (int idx0 = threadIdx.x; idx0 < total; idx0 += 4 * step) {
+    uint4 v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int idx = idx0 + r * step;
+      if (idx < total) {
+        const int tok = idx / (2 * CH);
+        const int rem = idx - tok * (2 * CH);
+        const __half* in = rem >= CH ? p.V : p.K;
+        v[r] = __ldg(reinterpret_cast<const uint4*>(in + (static_cast<int64_t>(u) * p.n + base + tok) * D) +
+                     (rem % CH));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int idx = idx0 + r * step;
+      if (idx < total) {
+        const int tok = idx / (2 * CH);
+        const int rem = idx - tok * (2 * CH);
+        __half* ring = rem >= CH ? p.res_v : p.res_k;
+        const int slot = static_cast<int>((lo + tok) % p.R);
+        reinterpret_cast<uint4*>(ring + u * p.res_stride + static_cast<int64_t>(slot) * D)[(rem % CH) ^ (slot & 7)] =
+            v[r];
+      }
+    }
   }
 }
 
 template <int KB, int VB, int D>
-__global__ void __launch_bounds__(kThreads) append_kernel(AppendParams p) {
+__global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int u = blockIdx.y;
-  const int64_t T = __ldcg(p.tokens);
-  const int64_t nq0 = quantized_after(T, p.R, p.G);
-  const int64_t nq1 = quantized_after(T + p.n, p.R, p.G);
+  const int tid = threadIdx.x;
+  const int T = __ldcg(p.tokens);
+  const int nq0 = static_cast<int>(quantized_after(T, p.R, p.G));
+  const int nq1 = static_cast<int>(quantized_after(T + p.n, p.R, p.G));
 
   if (p.mode & kFlush) {
-    const int64_t grp = nq0 / p.G + blockIdx.x;
-    if (grp < nq1 / p.G) quantize_group<KB, VB, D>(p, u, grp, T, smem);
+    // jobs j = (unit j / nflush, group nq0/G + j % nflush), CTA-strided
+    const AppendSmem L = append_smem_layout(D, p.G, p.rec_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
+    const int nflush = (nq1 - nq0) / p.G;
+    const int njobs = nflush * p.units;
+    const uint32_t tile = static_cast<uint32_t>(L.tile);
+    // stage the K and V rows of job j: ring rows first (slots of a group are
+    // contiguous: the group starts at a multiple of G and R is one too), then
+    // rows of this call's input
+    auto issue = [&](int j, int st) {
+      const int u = j / nflush, t0 = (nq0 / p.G + (j - u * nflush)) * p.G;
+      const int nring = T > t0 ? (T - t0 < p.G ? T - t0 : p.G) : 0;
+      uint8_t* ks = smem + st * L.off_stage1;
+      uint8_t* vs = ks + tile;
+      mbar_arrive_expect_tx(&bars[st], 2 * tile);
+      if (nring > 0) {
+        const int s0 = t0 % p.R;
+        const uint32_t b = static_cast<uint32_t>(nring) * D * 2;
+        bulk_g2s(ks, p.res_k + u * p.res_stride + static_cast<int64_t>(s0) * D, b, &bars[st]);
+        bulk_g2s(vs, p.res_v + u * p.res_stride + static_cast<int64_t>(s0) * D, b, &bars[st]);
+      }
+      if (nring < p.G) {
+        const int64_t row = static_cast<int64_t>(u) * p.n + (t0 + nring - T);
+        const uint32_t b = static_cast<uint32_t>(p.G - nring) * D * 2;
+        const uint32_t o = static_cast<uint32_t>(nring) * D * 2;
+        bulk_g2s(ks + o, p.K + row * D, b, &bars[st]);
+        bulk_g2s(vs + o, p.V + row * D, b, &bars[st]);
+      }
+    };
+    if (tid == 0) {
+      mbar_init(&bars[0], 1);
+      mbar_init(&bars[1], 1);
+      fence_mbar_init();
+      if (static_cast<int>(blockIdx.x) < njobs) issue(blockIdx.x, 0);
+      if (static_cast<int>(blockIdx.x + gridDim.x) < njobs) issue(blockIdx.x + gridDim.x, 1);
+    }
+    __syncthreads();
+    int k = 0;
+    for (int j = blockIdx.x; j < njobs; j += gridDim.x, ++k) {
+      const int st = k & 1;
+      const int u = j / nflush, grp = nq0 / p.G + (j - u * nflush);
+      const int t0 = grp * p.G;
+      const int nring = T > t0 ? (T - t0 < p.G ? T - t0 : p.G) : 0;
+      const bool ok = mbar_wait(&bars[st], static_cast<uint32_t>((k >> 1) & 1), p.err);
+      const __half* kt = reinterpret_cast<const __half*>(smem + st * L.off_stage1);
+      if (!flush_group<KB, VB, D>(p, kt, kt + p.G * D, nring, smem, L, ok)) {
+        // a copy never landed (all threads agree): give the other stage's copy
+        // its bounded wait, then stop
+        const int jn = j + static_cast<int>(gridDim.x);
+        if (jn < njobs) mbar_wait(&bars[st ^ 1], static_cast<uint32_t>(((k + 1) >> 1) & 1), p.err);
+        break;
+      }
+      __syncthreads();  // stage and record staging complete
+      if (tid == 0) {
+        fence_proxy_async_smem();
+        uint8_t* dst = p.records + static_cast<int64_t>(u) * p.unit_rec_stride + static_cast<int64_t>(grp) * p.rec_bytes;
+        bulk_s2g(dst, smem + L.off_rec, static_cast<uint32_t>(p.rec_bytes));
+        bulk_commit();
+        const int jn = j + 2 * static_cast<int>(gridDim.x);
+        if (jn < njobs) issue(jn, st);
+      }
+    }
+    if (tid == 0) bulk_wait_all();
   }
   if (p.mode & kResidual) {
     // tokens that stay in the window after this call
-    const int64_t first = (T > nq1) ? T : nq1;
-    const int64_t last = T + p.n;
-    if (p.mode & kFlush) {  // fused single-CTA-per-unit launch writes them all
-      if (first < last) write_residual<D>(p, u, first, last, T);
+    const int first = T > nq1 ? T : nq1;
+    const int last = T + p.n;
+    if (p.mode & kFlush) {  // decode step: CTA u writes unit u's tokens
+      if (first < last) write_residual<D>(p, blockIdx.x, first, last, T);
     } else {
-      const int64_t per = 16;
-      const int64_t lo = first + static_cast<int64_t>(blockIdx.x) * per;
-      const int64_t hi = (lo + per < last) ? lo + per : last;
-      if (lo < hi) write_residual<D>(p, u, lo, hi, T);
+      const int lo = first + static_cast<int>(blockIdx.x) * 16;
+      const int hi = (lo + 16 < last) ? lo + 16 : last;
+      if (lo < hi) write_residual<D>(p, blockIdx.y, lo, hi, T);
     }
   }
   if (p.mode & kUpdateState) {
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       __threadfence();
       const int prev = atomicAdd(p.done_ctr, 1);
       if (prev == p.ctas - 1) {
-        *p.tokens = static_cast<int32_t>(T + p.n);
+        *p.tokens = T + p.n;
         *p.done_ctr = 0;
         __threadfence();
       }
@@ -362,20 +524,32 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendParams p) {
 }  // namespace
 
 template <int KB, int VB, int D>
-static cudaError_t launch_append(const AppendParams& p, dim3 grid, size_t smem, cudaStream_t s) {
+static cudaError_t launch_append(const AppendParams& p, dim3 grid, int threads, size_t smem, cudaStream_t s) {
   auto k = append_kernel<KB, VB, D>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, s>>>(p);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  k<<<grid, threads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+template <int KB, int VB, int D>
+static int occupancy_append(int threads, size_t smem) {
+  auto k = append_kernel<KB, VB, D>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, threads, smem) != cudaSuccess) return 0;
+  return occ;
 }
 
 #define KVQ_APPEND_ENTRY(KB, VB)                                                     \
   case (KB * 16 + VB):                                                              \
-    return D == 128 ? launch_append<KB, VB, 128>(p, grid, smem, s)                  \
-                    : launch_append<KB, VB, 64>(p, grid, smem, s);
+    return D == 128 ? launch_append<KB, VB, 128>(p, grid, threads, smem, s)         \
+                    : launch_append<KB, VB, 64>(p, grid, threads, smem, s);
 
-cudaError_t append_dispatch(int kb, int vb, int D, const AppendParams& p, dim3 grid, size_t smem,
+cudaError_t append_dispatch(int kb, int vb, int D, const AppendParams& p, dim3 grid, int threads, size_t smem,
                             cudaStream_t s) {
   switch (kb * 16 + vb) {
     KVQ_APPEND_ENTRY(2, 2) KVQ_APPEND_ENTRY(2, 3) KVQ_APPEND_ENTRY(2, 4) KVQ_APPEND_ENTRY(2, 8)
@@ -386,11 +560,30 @@ cudaError_t append_dispatch(int kb, int vb, int D, const AppendParams& p, dim3 g
       return cudaErrorInvalidValue;
   }
 }
+#undef KVQ_APPEND_ENTRY
+
+#define KVQ_APPEND_OCC(KB, VB) \
+  case (KB * 16 + VB):        \
+    return D == 128 ? occupancy_append<KB, VB, 128>(threads, smem) : occupancy_append<KB, VB, 64>(threads, smem);
+
+int append_ctas_per_sm(int kb, int vb, int D, int threads, size_t smem) {
+  switch (kb * 16 + vb) {
+    KVQ_APPEND_OCC(2, 2) KVQ_APPEND_OCC(2, 3) KVQ_APPEND_OCC(2, 4) KVQ_APPEND_OCC(2, 8)
+    KVQ_APPEND_OCC(3, 2) KVQ_APPEND_OCC(3, 3) KVQ_APPEND_OCC(3, 4) KVQ_APPEND_OCC(3, 8)
+    KVQ_APPEND_OCC(4, 2) KVQ_APPEND_OCC(4, 3) KVQ_APPEND_OCC(4, 4) KVQ_APPEND_OCC(4, 8)
+    KVQ_APPEND_OCC(8, 2) KVQ_APPEND_OCC(8, 3) KVQ_APPEND_OCC(8, 4) KVQ_APPEND_OCC(8, 8)
+    default:
+      return 0;
+  }
+}
+#undef KVQ_APPEND_OCC
+
+int append_block_threads(int G) { return append_threads(G); }
 
 size_t append_smem_bytes(int kb, int vb, int D, int G, int rec_bytes) {
-  size_t b = static_cast<size_t>(rec_bytes);
-  if (kb == 3 || vb == 3) b += static_cast<size_t>(2) * G * D;
-  return (b + 127) / 128 * 128;
+  (void)kb;
+  (void)vb;
+  return static_cast<size_t>(append_smem_layout(D, G, rec_bytes).total);
 }
 
 }  // namespace kvq
