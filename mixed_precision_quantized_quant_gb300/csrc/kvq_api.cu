@@ -39,7 +39,7 @@ struct LayerPlan {
 struct Plan {
   int L, B, Hq, Hkv, D, G, max_tokens, gqa, units;
   std::vector<LayerPlan> layers;
-  int64_t off_ctrl, off_err, off_counters, off_partials, partial_floats;
+  int64_t off_ctrl, ctrl_stride, off_err, off_counters, off_partials, partial_floats;
   int64_t total;
 };
 
@@ -63,8 +63,10 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
   P->gqa = gqa;
   P->units = cfg->batch * cfg->num_kv_heads;
   int64_t off = 0;
+  // per layer: {append done-counter, padding to 64 B, appended-token counter per unit}
+  P->ctrl_stride = align_up(64 + static_cast<int64_t>(P->units) * 4, kAlign);
   P->off_ctrl = off;
-  off += align_up(static_cast<int64_t>(P->L) * 64, kAlign);
+  off += P->ctrl_stride * P->L;
   P->off_err = off;
   off += kAlign;
   P->off_counters = off;
@@ -128,8 +130,10 @@ struct kvq_handle {
 namespace {
 
 int32_t* ctrl(kvq_handle* h, int layer) {
-  return reinterpret_cast<int32_t*>(h->base + h->plan.off_ctrl + static_cast<int64_t>(layer) * 64);
+  return reinterpret_cast<int32_t*>(h->base + h->plan.off_ctrl + static_cast<int64_t>(layer) * h->plan.ctrl_stride);
 }
+// per-unit appended-token counters of a layer (16 ints past its done-counter)
+int32_t* unit_tokens(kvq_handle* h, int layer) { return ctrl(h, layer) + 16; }
 int32_t* errw(kvq_handle* h) { return reinterpret_cast<int32_t*>(h->base + h->plan.off_err); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -157,14 +161,14 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   ap.res_k = reinterpret_cast<__half*>(h->base + lp.off_res_k);
   ap.res_v = reinterpret_cast<__half*>(h->base + lp.off_res_v);
   ap.res_stride = lp.res_stride_elems;
-  ap.tokens = ctrl(h, layer);
-  ap.done_ctr = ctrl(h, layer) + 1;
+  ap.tokens = unit_tokens(h, layer);
+  ap.done_ctr = ctrl(h, layer);
   ap.err = errw(h);
   const size_t smem = kvq::append_smem_bytes(lp.kb, lp.vb, P.D, P.G, static_cast<int>(lp.rec_bytes));
   cudaError_t e = cudaSuccess;
   if (n == 1) {
     // one CTA per unit: its flush job (if a group fills) and its new token
-    ap.mode = kvq::kFlush | kvq::kResidual | kvq::kUpdateState;
+    ap.mode = kvq::kFlush | kvq::kResidual | kvq::kUpdateState | kvq::kPerUnit;
     ap.ctas = P.units;
     e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(P.units, 1), kvq::append_block_threads(P.G), smem, s);
   } else {
@@ -199,7 +203,7 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   dp.res_k = reinterpret_cast<const __half*>(h->base + lp.off_res_k);
   dp.res_v = reinterpret_cast<const __half*>(h->base + lp.off_res_v);
   dp.res_stride = lp.res_stride_elems;
-  dp.tokens = ctrl(h, layer);
+  dp.tokens = unit_tokens(h, layer);
   dp.partials = reinterpret_cast<float*>(h->base + P.off_partials);
   dp.counters = reinterpret_cast<int32_t*>(h->base + P.off_counters);
   dp.err = errw(h);
@@ -481,7 +485,7 @@ extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const vo
   dp.res_k = reinterpret_cast<const __half*>(h->base + lp.off_res_k);
   dp.res_v = reinterpret_cast<const __half*>(h->base + lp.off_res_v);
   dp.res_stride = lp.res_stride_elems;
-  dp.tokens = ctrl(h, layer);
+  dp.tokens = unit_tokens(h, layer);
   dp.partials = reinterpret_cast<float*>(scratch + counter_bytes);
   dp.counters = counters;
   dp.err = errw(h);

@@ -426,7 +426,15 @@ template <int KB, int VB, int D>
 __global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
-  const int T = __ldcg(p.tokens);
+  const bool per_unit = (p.mode & kPerUnit) != 0;
+  // single-token append: the token's K/V row is loaded while the counter is in flight
+  constexpr int CH = D / 8;
+  uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+  if (per_unit && tid < 2 * CH) {
+    const __half* in = tid >= CH ? p.V : p.K;
+    newrow = __ldg(reinterpret_cast<const uint4*>(in + static_cast<int64_t>(blockIdx.x) * D) + (tid % CH));
+  }
+  const int T = __ldcg(p.tokens + (per_unit ? blockIdx.x : 0));
   const int nq0 = static_cast<int>(quantized_after(T, p.R, p.G));
   const int nq1 = static_cast<int>(quantized_after(T + p.n, p.R, p.G));
 
@@ -499,8 +507,13 @@ __global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
     // tokens that stay in the window after this call
     const int first = T > nq1 ? T : nq1;
     const int last = T + p.n;
-    if (p.mode & kFlush) {  // decode step: CTA u writes unit u's tokens
-      if (first < last) write_residual<D>(p, blockIdx.x, first, last, T);
+    if (per_unit) {  // single token: CTA u writes unit u's token unless it was flushed
+      if (first < last && tid < 2 * CH) {
+        __half* ring = tid >= CH ? p.res_v : p.res_k;
+        const int slot = T % p.R;
+        reinterpret_cast<uint4*>(ring + blockIdx.x * p.res_stride + static_cast<int64_t>(slot) * D)[(tid % CH) ^ (slot & 7)] =
+            newrow;
+      }
     } else {
       const int lo = first + static_cast<int>(blockIdx.x) * 16;
       const int hi = (lo + 16 < last) ? lo + 16 : last;
@@ -508,14 +521,21 @@ __global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
     }
   }
   if (p.mode & kUpdateState) {
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const int prev = atomicAdd(p.done_ctr, 1);
-      if (prev == p.ctas - 1) {
-        *p.tokens = T + p.n;
-        *p.done_ctr = 0;
+    if (per_unit) {
+      // the next kernel on the stream sees it; no CTA of this launch reads it again
+      if (tid == 0) p.tokens[blockIdx.x] = T + p.n;
+    } else {
+      // the last CTA to finish advances every unit's counter
+      __shared__ int last;
+      __syncthreads();
+      if (tid == 0) {
         __threadfence();
+        last = atomicAdd(p.done_ctr, 1) == p.ctas - 1;
+      }
+      __syncthreads();
+      if (last) {
+        for (int u = tid; u < p.units; u += blockDim.x) p.tokens[u] = T + p.n;
+        if (tid == 0) *p.done_ctr = 0;
       }
     }
   }

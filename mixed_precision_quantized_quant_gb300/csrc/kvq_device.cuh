@@ -46,13 +46,16 @@ struct AppendParams {
   __half* res_k;          // [units][R][D] ring (chunk-swizzled)
   __half* res_v;
   int64_t res_stride;     // elements between units' rings
-  int32_t* tokens;        // device state: tokens appended so far
+  int32_t* tokens;        // device state: tokens appended so far, one counter per unit
   int32_t* done_ctr;      // last-CTA counter of this launch
   int32_t* err;
   int mode;               // kFlush | kResidual | kUpdateState
   int ctas;               // CTAs in this launch (for the last-CTA count)
 };
 constexpr int kFlush = 1, kResidual = 2, kUpdateState = 4;
+// one CTA per unit (a single-token append): each CTA reads and advances its
+// own unit's counter, no cross-CTA handshake
+constexpr int kPerUnit = 8;
 
 struct DecodeParams {
   const __half* q;        // [B][Hq][D]
@@ -62,7 +65,7 @@ struct DecodeParams {
   const __half* res_k;
   const __half* res_v;
   int64_t res_stride;     // elements
-  const int32_t* tokens;  // device state
+  const int32_t* tokens;  // device state: unit 0's appended-token counter (all units agree)
   float* partials;        // [slots][gqa][D + 2]
   int32_t* counters;      // [units]
   int32_t* err;
