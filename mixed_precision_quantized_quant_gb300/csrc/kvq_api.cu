@@ -92,7 +92,7 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
       // the decode kernel splits a layer's work in 32-bit byte-cost units
       const int64_t slice = 4LL * 32 * (lp.wk + lp.wv) + 4LL * P->D + 128;
       const int64_t tile = 16LL * 4 * P->D;
-      const int64_t setup = 4 * (slice > 2048 ? slice : 2048);
+      const int64_t setup = 8 * (slice > 2048 ? slice : 2048);  // up to 8 warps per CTA
       const int64_t per_unit = setup + lp.max_groups * (P->G / 32) * slice + ((lp.R + 15) / 16) * tile;
       if (per_unit * P->units >= (1LL << 32)) return KVQ_ERR_UNSUPPORTED;
     }
@@ -216,7 +216,7 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   dp.grid = h->grid[layer];
   dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
   const kvq::DecodeKernel& k = h->dec[layer];
-  k.fn<<<h->grid[layer], kvq::kDecThreads, k.smem, s>>>(dp);
+  k.fn<<<h->grid[layer], k.threads, k.smem, s>>>(dp);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
@@ -498,7 +498,7 @@ extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const vo
   dp.grid = grid;
   dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
   const kvq::DecodeKernel& k = h->dec[layer];
-  k.fn<<<grid, kvq::kDecThreads, k.smem, s>>>(dp);
+  k.fn<<<grid, k.threads, k.smem, s>>>(dp);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

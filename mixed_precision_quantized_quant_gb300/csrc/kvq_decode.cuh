@@ -56,13 +56,14 @@ struct DecodeSmem {
   int off_bars, off_qs, off_qp, off_qps, off_qr, off_wm, off_wl, off_dm, off_flags, off_wo, total;
 };
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, int rec_bytes) {
-  DecodeSmem s;
+// W warps per CTA, each with its own ring of `ring` bytes.
+__host__ __device__ constexpr DecodeSmem decode_smem_layout_ring(int D, int NT, int ring, int W) {
+  DecodeSmem s{};
   const int H = 4 * NT;
-  s.ring = ring_bytes(D, G, rec_bytes);
-  int off = kDecWarps * s.ring;
+  s.ring = ring;
+  int off = W * s.ring;
   s.off_bars = off;
-  off += (kDecWarps * kSlots + 2) * 8;  // ring slots, then the two query buffers
+  off += (W * kSlots + 2) * 8;       // ring slots, then the two query buffers
   s.off_qs = off;
   off += 2 * H * D * 2;              // double-buffered query rows of a unit
   // per-lane query tables, lane-interleaved in 8-byte pairs (conflict-free)
@@ -73,18 +74,38 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, i
   s.off_qr = off;
   off += 32 * NT * D / 16 * 2 * 4;   // residual (fp16 key) query table
   s.off_wm = off;
-  off += kDecWarps * H * 4;
+  off += W * H * 4;
   s.off_wl = off;
-  off += kDecWarps * H * 4;
+  off += W * H * 4;
   s.off_dm = off;
-  off += kDecWarps * H * 4;
+  off += W * H * 4;
   s.off_flags = off;
   off += 64;
   off = (off + 15) / 16 * 16;
   s.off_wo = off;
-  off += kDecWarps * H * D * 4;
+  off += W * H * D * 4;
   s.total = off;
   return s;
+}
+
+__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, int rec_bytes, int W) {
+  return decode_smem_layout_ring(D, NT, ring_bytes(D, G, rec_bytes), W);
+}
+
+// Warps per CTA of an instantiation: 8 where two such CTAs fit in an SM's
+// shared memory (fewer CTAs per unit: fewer query-table builds and split
+// merges at the same occupancy), else 4.  3-bit values keep 4: they need more
+// than the 128 registers a thread may use at 2 x 256 threads per SM.  The ring
+// size does not depend on G.
+template <int KB, int VB, int D, int NT>
+__host__ __device__ constexpr int decode_warps() {
+  constexpr int WK = (KB == 3) ? (D + 10) / 11 : D * KB / 32;
+  constexpr int WV = (VB == 3) ? (D + 10) / 11 : D * VB / 32;
+  constexpr int sl = kSlice * 4 * (WK + WV) + 4 * D + 4 * kSlice;
+  constexpr int rt = kResTile * 4 * D;
+  constexpr int ring = ((rt > 2 * sl ? rt : 2 * sl) + 127) / 128 * 128;
+  constexpr int smem8 = decode_smem_layout_ring(D, NT, ring, 8).total;
+  return (NT == 1 && VB != 3 && 2 * (smem8 + 1024) <= 228 * 1024) ? 8 : 4;
 }
 
 // ------------------------------------------------------------------ unpacking
@@ -378,7 +399,9 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
 // ------------------------------------------------------------------ kernel
 
 template <int KB, int VB, int D, int NT>
-__global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
+                                  decode_warps<KB, VB, D, NT>() == 8 ? 2 : (NT == 1 ? 3 : 2))
+    decode_kernel(DecodeParams p) {
   using KS_ = KeyShape<KB, D>;
   using VS_ = ValShape<VB, D>;
   constexpr int KS = D / 16;            // residual k-steps / channel m-tiles
@@ -390,9 +413,11 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
   constexpr int MTA = MTV > KS ? MTV : KS;
   constexpr int NP = D / 8;
   constexpr int H = 4 * NT;             // padded query heads
+  constexpr int W = decode_warps<KB, VB, D, NT>();  // warps per CTA
+  constexpr int TH = 32 * W;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  const DecodeSmem L = decode_smem_layout(D, NT, p.G, p.rec_bytes);
+  const DecodeSmem L = decode_smem_layout(D, NT, p.G, p.rec_bytes, W);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
   __half* qs = reinterpret_cast<__half*>(smem + L.off_qs);
   uint32_t* qp_tab = reinterpret_cast<uint32_t*>(smem + L.off_qp);
@@ -429,7 +454,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
   const int NI = NG + NRT;
   constexpr uint32_t cq = kSlice * 4 * (WK + WV) + 4 * D + 4 * kSlice;  // staged slice bytes
   constexpr uint32_t cr = kResTile * 4 * D;                             // residual tile bytes
-  constexpr uint32_t csu = 4u * (cq > 2048u ? cq : 2048u);              // per-unit setup cost
+  constexpr uint32_t csu = W * (cq > 2048u ? cq : 2048u);               // per-unit setup cost
   const uint32_t Cu = csu + static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(NRT) * cr;
   const uint32_t C = static_cast<uint32_t>(p.units) * Cu;
   // a CTA range must hold at least one item start: range >= largest item + setup
@@ -483,7 +508,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
   // ---------------- query rows of a unit, double-buffered bulk copies
   // (issued before the ring copies: the query tables gate every item;
   // rows past gqa are never read, the tables test h < gqa)
-  uint64_t* qbar = bars + kDecWarps * kSlots;
+  uint64_t* qbar = bars + W * kSlots;
   const uint32_t qbytes = static_cast<uint32_t>(p.gqa * D * 2);
   auto issue_q = [&](int u, int buf) {
     mbar_arrive_expect_tx(&qbar[buf], qbytes);
@@ -517,7 +542,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
   int ci = ii;
   auto try_issue = [&]() {
     while (nin < kSlots) {
-      const int f = f0 + warp + kDecWarps * kiss;
+      const int f = f0 + warp + W * kiss;
       if (f >= f1) break;
       const uint32_t sz = ii < NG ? cq : cr;
       int off;
@@ -569,7 +594,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
       }
       ++nin;
       ++kiss;
-      ii += kDecWarps;
+      ii += W;
       while (ii >= NI) {
         ii -= NI;
         ++iu;
@@ -600,7 +625,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + (g >> 1);
         const bool live = h < p.gqa;
-        for (int pi = warp; pi < NPK; pi += kDecWarps) {
+        for (int pi = warp; pi < NPK; pi += W) {
           int ca, cb;
           key_pair_channels<KB, D>(tig, pi, ca, cb);
           const __half z0 = __float2half(0.0f);
@@ -611,7 +636,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
           const float f = static_cast<float>(1 << (key_pos_max<KB>() - key_pos<KB, D>(pi)));
           qps_tab[kt_idx(j, pi, lane)] = h2_as_u32(__hmul2(q2, __float2half2_rn(f)));
         }
-        for (int kk = warp; kk < KS; kk += kDecWarps) {
+        for (int kk = warp; kk < KS; kk += W) {
           for (int rr = 0; rr < 2; ++rr) {
             const int c = 16 * kk + 8 * rr + 2 * tig;
             qr_tab[rt_idx(j, kk, lane) + rr] =
@@ -678,7 +703,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
     };
 
     while (true) {
-      const int f = f0 + warp + kDecWarps * kcon;
+      const int f = f0 + warp + W * kcon;
       if (f >= seg_hi) break;
       const int st = kcon & (kSlots - 1);
       const uint32_t ph = static_cast<uint32_t>((kcon >> 2) & 1);
@@ -1038,7 +1063,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
         }
       }
       ++kcon;
-      ci += kDecWarps;
+      ci += W;
       while (ci >= NI) ci -= NI;
       try_issue();
     }
@@ -1082,14 +1107,14 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
     const int64_t qrow = (static_cast<int64_t>(b) * p.kv_heads + kvh) * p.gqa;  // first query head row
     const int stride_slot = p.gqa * (D + 2);
     float* slot = p.partials + static_cast<int64_t>(pid + u) * stride_slot;
-    for (int idx = tid; idx < p.gqa * D; idx += kDecThreads) {
+    for (int idx = tid; idx < p.gqa * D; idx += TH) {
       const int h = idx / D, c = idx % D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, wm[w * H + h]);
+      for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w * H + h]);
       float O = 0.0f, Lsum = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
+      for (int w = 0; w < W; ++w) {
         const float mw = wm[w * H + h];
         if (mw == -INFINITY) continue;
         const float f = ex2(mw - M);
@@ -1118,7 +1143,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
         // one pass over the splits with a running (max, sum, output) per
         // element; a split's loads do not depend on the running values, so
         // the loads of several splits are in flight together
-        constexpr int PER = H * D / kDecThreads;
+        constexpr int PER = H * D / TH;
         const int nout = p.gqa * D;
         float Mr[PER], Lr[PER], Or[PER];
 #pragma unroll
@@ -1132,7 +1157,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
           const float* ps = p.partials + static_cast<int64_t>(sidx + u) * stride_slot;
 #pragma unroll
           for (int k = 0; k < PER; ++k) {
-            const int idx = tid + k * kDecThreads;
+            const int idx = tid + k * TH;
             if (idx < nout) {
               const int h = idx / D;
               const float ms = __ldcg(ps + nout + 2 * h), ls = __ldcg(ps + nout + 2 * h + 1);
@@ -1147,7 +1172,7 @@ __global__ void __launch_bounds__(kDecThreads, NT == 1 ? 3 : 2) decode_kernel(De
         }
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
-          const int idx = tid + k * kDecThreads;
+          const int idx = tid + k * TH;
           if (idx < nout) p.out[qrow * D + idx] = Or[k] / Lr[k];
         }
         if (tid == 0) p.counters[u] = 0;

@@ -11,11 +11,12 @@ static DecodeKernel make() {
   k.fn = decode_kernel<4, VB, D, NT>;
   k.smem = 0;
   k.ctas_per_sm = 0;
+  k.threads = 32 * decode_warps<4, VB, D, NT>();
   return k;
 }
 
 DecodeKernel decode_get_k4(int vb, int D, int nt) {
-  DecodeKernel none{nullptr, 0, 0};
+  DecodeKernel none{nullptr, 0, 0, 0};
 #define E(VB)                                                               \
   if (vb == VB) {                                                           \
     if (D == 128) return nt == 1 ? make<VB, 128, 1>() : make<VB, 128, 2>(); \

@@ -22,9 +22,10 @@ struct DecodeKernel {
   decode_kernel_t fn;
   size_t smem;      // dynamic shared memory per CTA
   int ctas_per_sm;  // occupancy at that smem
+  int threads;      // threads per CTA
 };
 // Returns fn == nullptr if the combination has no instantiation.
 DecodeKernel decode_select(int kb, int vb, int D, int gqa, int G, int rec_bytes);
-size_t decode_smem_bytes(int D, int nt, int G, int rec_bytes);
+size_t decode_smem_bytes(int D, int nt, int G, int rec_bytes, int warps);
 
 }  // namespace kvq
