@@ -86,7 +86,7 @@ __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint
 // Shared-memory layout of the flush path.
 struct AppendSmem {
   int tile;  // bytes of one staged [G][D] fp16 tile
-  int off_stage1, off_rec, off_ksc, off_vsc, off_vr2, off_kmn, off_kmx, off_vpart, off_bars, total;
+  int off_stage1, off_rec, off_ksc, off_kp, off_vsc, off_vr2, off_kmn, off_kmx, off_vpart, off_bars, total;
 };
 
 // Flush CTAs run 4*G threads: each thread owns one 16-byte chunk of D/32 rows.
@@ -103,6 +103,9 @@ __host__ __device__ inline AppendSmem append_smem_layout(int D, int G, int rec_b
   off += (rec_bytes + 127) / 128 * 128;
   a.off_ksc = off;
   off += D * 16;  // per channel {min, s, 1/s, qmax}, channel 8c + k at k*(D/8) + c
+  a.off_kp = off;
+  off += D * 8;   // per channel min and 1/s as pairs: {min[8c+2j], min[8c+2j+1]} at j*(D/8) + c,
+                  // then the same for 1/s at D/2 + j*(D/8) + c (8 bytes each)
   a.off_vsc = off;
   off += G * 16;  // per token {min, s, 1/s, s2}
   a.off_vr2 = off;
@@ -153,27 +156,57 @@ __device__ __noinline__ uint2 quant8_exact(uint4 xv, const float4* tab, int stri
   return make_uint2(lo, hi);
 }
 
-// Eight codes of one 16-byte chunk, branch-free on the common path:
-// 0 <= y < 2^22, so y + 2^23 rounds y to the nearest integer (ties to even)
-// and that integer sits in the low mantissa bits.  A chunk with any quotient
-// near a rounding boundary is redone element by element by quant8_exact.
-// sc: the scales in registers, one per element (keys) or sc[0] for all
-// (values, PER = false); tab/stride/qm: the same scales in shared memory.
-template <bool PER>
-__device__ __forceinline__ void quant8(const uint4& xv, const float4* sc, const float4* tab, int stride, float qm,
+// Two fp32 lanes in one 64-bit register: paired IEEE operations, each lane
+// rounded exactly like the scalar instruction.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2unpack(uint64_t d, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Eight codes of one 16-byte chunk, branch-free on the common path, two
+// elements per paired operation: 0 <= y < 2^22, so y + 2^23 rounds y to the
+// nearest integer (ties to even) and that integer sits in the low mantissa
+// bits.  A chunk with any quotient near a rounding boundary is redone element
+// by element by quant8_exact.  mn2[j], r2[j]: (min, 1/s) of elements 2j,
+// 2j+1; qmax is the same for all eight; tab/stride/qm: the scales in shared
+// memory for the exact path.
+__device__ __forceinline__ void quant8(const uint4& xv, const uint64_t (&mn2)[4], const uint64_t (&r2)[4],
+                                       uint32_t qmax, const float4* tab, int stride, float qm,
                                        uint32_t (&code)[8]) {
   const __half2* h = reinterpret_cast<const __half2*>(&xv);
+  const uint64_t magic = f2pack(8388608.0f, 8388608.0f);
   bool near = false;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4& s = sc[PER ? k : 0];
-    const float x = (k & 1) ? __high2float(h[k >> 1]) : __low2float(h[k >> 1]);
-    const float y = __fmul_rn(__fsub_rn(x, s.x), s.z);
-    const float t = __fadd_rn(y, 8388608.0f);
-    near |= fabsf(__fsub_rn(y, __fsub_rn(t, 8388608.0f))) >= kNearHalf;
-    const uint32_t c = __float_as_uint(t) - 0x4B000000u;
-    const uint32_t q = static_cast<uint32_t>(s.w);
-    code[k] = c < q ? c : q;
+  for (int j = 0; j < 4; ++j) {
+    const float2 xf = __half22float2(h[j]);
+    const uint64_t y = f2mul(f2sub(f2pack(xf.x, xf.y), mn2[j]), r2[j]);
+    const uint64_t t = f2add(y, magic);
+    float d0, d1, t0, t1;
+    f2unpack(f2sub(y, f2sub(t, magic)), d0, d1);
+    near |= (fabsf(d0) >= kNearHalf) | (fabsf(d1) >= kNearHalf);
+    f2unpack(t, t0, t1);
+    const uint32_t c0 = __float_as_uint(t0) - 0x4B000000u, c1 = __float_as_uint(t1) - 0x4B000000u;
+    code[2 * j] = c0 < qmax ? c0 : qmax;
+    code[2 * j + 1] = c1 < qmax ? c1 : qmax;
   }
   if (near) {
     const uint2 b = quant8_exact(xv, tab, stride, qm);
@@ -287,6 +320,12 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
     }
     const Scale sc = make_scale<KB>(mn, mx, KB == 3 && ch % 11 == 10);
     ksc[tid] = make_float4(sc.mn, sc.s, sc.r, sc.qmax);
+    {
+      float* kpf = reinterpret_cast<float*>(smem + L.off_kp);
+      const int pi = (((ch & 7) >> 1) * CH + (ch >> 3)) * 2 + (ch & 1);
+      kpf[pi] = sc.mn;
+      kpf[D + pi] = sc.r;
+    }
     ks16[ch] = sc.s16;
     kz16[ch] = sc.z16;
   }
@@ -308,14 +347,18 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
 
   // ---- phase 3: codes, packed LSB first into the record staging area
   if constexpr (KB != 3) {
-    float4 sc[8];
+    const uint64_t* kp = reinterpret_cast<const uint64_t*>(smem + L.off_kp);
+    uint64_t mn2[4], r2[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sc[k] = ksc[k * CH + c];
+    for (int j = 0; j < 4; ++j) {
+      mn2[j] = kp[j * CH + c];
+      r2[j] = kp[D / 2 + j * CH + c];
+    }
 #pragma unroll
     for (int k = 0; k < RT; ++k) {
       const int t = rg + k * RG;
       uint32_t code[8];
-      quant8<true>(xk[k], sc, ksc + c, CH, -1.0f, code);
+      quant8(xk[k], mn2, r2, (1u << KB) - 1, ksc + c, CH, -1.0f, code);
       uint32_t w0, w1;
       pack8<KB>(code, w0, w1);
       if (KB == 8) {
@@ -348,9 +391,10 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
     for (int k = 0; k < RT; ++k) {
       const int t = rg + k * RG;
       const float4 s = vsc[t];
-      const float4 sq = make_float4(s.x, s.y, s.z, static_cast<float>((1 << VB) - 1));
+      const uint64_t m = f2pack(s.x, s.x), r = f2pack(s.z, s.z);
+      const uint64_t mn2[4] = {m, m, m, m}, r2[4] = {r, r, r, r};
       uint32_t code[8];
-      quant8<false>(xv[k], &sq, vsc + t, 0, static_cast<float>((1 << VB) - 1), code);
+      quant8(xv[k], mn2, r2, (1u << VB) - 1, vsc + t, 0, static_cast<float>((1 << VB) - 1), code);
       uint32_t w0, w1;
       pack8<VB>(code, w0, w1);
       if (VB == 8) {
