@@ -92,7 +92,7 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
       // the decode kernel splits a layer's work in 32-bit byte-cost units
       const int64_t slice = 4LL * 32 * (lp.wk + lp.wv) + 4LL * P->D + 128;
       const int64_t tile = 16LL * 4 * P->D;
-      const int64_t setup = 8 * (slice > 2048 ? slice : 2048);  // up to 8 warps per CTA
+      const int64_t setup = 16 * (slice > 2048 ? slice : 2048);  // 2 x up to 8 warps per CTA
       const int64_t per_unit = setup + lp.max_groups * (P->G / 32) * slice + ((lp.R + 15) / 16) * tile;
       if (per_unit * P->units >= (1LL << 32)) return KVQ_ERR_UNSUPPORTED;
     }

@@ -454,7 +454,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
   const int NI = NG + NRT;
   constexpr uint32_t cq = kSlice * 4 * (WK + WV) + 4 * D + 4 * kSlice;  // staged slice bytes
   constexpr uint32_t cr = kResTile * 4 * D;                             // residual tile bytes
-  constexpr uint32_t csu = W * (cq > 2048u ? cq : 2048u);               // per-unit setup cost
+  // per-unit setup cost (query tables, warp merge, partial write): measured
+  // at about the time a CTA needs for 2*W slices
+  constexpr uint32_t csu = 2 * W * (cq > 2048u ? cq : 2048u);
   const uint32_t Cu = csu + static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(NRT) * cr;
   const uint32_t C = static_cast<uint32_t>(p.units) * Cu;
   // a CTA range must hold at least one item start: range >= largest item + setup
