@@ -478,7 +478,12 @@ __global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
     const __half* in = tid >= CH ? p.V : p.K;
     newrow = __ldg(reinterpret_cast<const uint4*>(in + static_cast<int64_t>(blockIdx.x) * D) + (tid % CH));
   }
-  const int T = __ldcg(p.tokens + (per_unit ? blockIdx.x : 0));
+  // the token count, read once per CTA so that every thread works from the
+  // same value even if a misordered launch changes it meanwhile
+  __shared__ int t_shared;
+  if (tid == 0) t_shared = __ldcg(p.tokens + (per_unit ? blockIdx.x : 0));
+  __syncthreads();
+  const int T = t_shared;
   const int nq0 = static_cast<int>(quantized_after(T, p.R, p.G));
   const int nq1 = static_cast<int>(quantized_after(T + p.n, p.R, p.G));
 

@@ -441,8 +441,13 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
   // each unit also carries a fixed cost for its setup and merge, so CTAs that
   // span two units get fewer bytes.  An item belongs to the CTA whose range
   // holds its start.  All of it is 32-bit arithmetic (the host keeps a
-  // layer's decode bytes below 2^32), computed by every thread, no barrier.
-  const int T = __ldcg(p.tokens);
+  // layer's decode bytes below 2^32), computed by every thread.  The token
+  // count is read once per CTA, so every thread works from the same value
+  // even if a misordered launch changes it meanwhile.
+  __shared__ int t_shared;
+  if (tid == 0) t_shared = __ldcg(p.tokens);
+  __syncthreads();
+  const int T = t_shared;
   if (T <= 0) return;
   const int lgG = 31 - __clz(p.G);        // G is 32, 64 or 128
   const int nq = T < p.R ? 0 : (((T - p.R) >> lgG) + 1) << lgG;  // tokens in key groups
