@@ -717,6 +717,21 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
       if (!failed && !mbar_wait(&wbar[st], ph, p.err)) failed = true;
       const uint8_t* stg = ring + rtail;
       const int i = ci;
+      // Frees the item's ring space and stages the next items.  Every value
+      // read from the slot must have been consumed by an instruction first.
+      bool released = false;
+      auto release_slot = [&]() {
+        __syncwarp();
+        const int sz = static_cast<int>(i < NG ? cq : cr);
+        --nin;
+        rtail += sz;
+        if (wrapped && rtail == rend) {
+          rtail = 0;
+          wrapped = false;
+        }
+        try_issue();
+        released = true;
+      };
 
       if (failed) {
         // a copy never landed: skip the work, keep the control flow
@@ -912,6 +927,16 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
           }
         }
 
+        // the last reads of the slot: each token's value (scale, zero); after
+        // them the slot is free for the next copy while the softmax and P.V run
+        float2 sz[2][2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          sz[t][0] = __half22float2(Vsz[16 * t + g]);
+          sz[t][1] = __half22float2(Vsz[16 * t + g + 8]);
+        }
+        release_slot();
+
         // raw scores: s[t][j][0] token 16t+g, [1] token 16t+g+8; m is kept in
         // units of alpha * raw (log2 domain), p = 2^(alpha*raw - m)
         float s[2][NT][2];
@@ -926,12 +951,6 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
           tmax[j] = alpha_q * fmaxf(fmaxf(s[0][j][0], s[0][j][1]), fmaxf(s[1][j][0], s[1][j][1]));
         }
         softmax_update(tmax);
-        float2 sz[2][2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          sz[t][0] = __half22float2(Vsz[16 * t + g]);
-          sz[t][1] = __half22float2(Vsz[16 * t + g + 8]);
-        }
         const int srcA = 4 * tig + (g >> 1);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -1058,21 +1077,11 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
         }
       }
 
-      // release the consumed item's ring space, then refill
-      __syncwarp();
-      {
-        const int sz = static_cast<int>(ci < NG ? cq : cr);
-        --nin;
-        rtail += sz;
-        if (wrapped && rtail == rend) {
-          rtail = 0;
-          wrapped = false;
-        }
-      }
+      // release the consumed item's ring space (if not done yet), then refill
+      if (!released) release_slot();
       ++kcon;
       ci += W;
       while (ci >= NI) ci -= NI;
-      try_issue();
     }
 
     // ---------------- warp -> shared memory
