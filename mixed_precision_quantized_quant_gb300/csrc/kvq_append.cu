@@ -53,7 +53,11 @@ __device__ __forceinline__ Scale make_scale(__half mn, __half mx, bool slot10) {
     sc.qmax = 3.0f;
   }
   sc.s = s;
-  sc.r = (s > 0.0f) ? __frcp_rn(s) : 0.0f;
+  // 1/s only steers the fast path of the code computation (see kNearHalf);
+  // an approximate reciprocal (relative error below 2^-22) is enough
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  sc.r = (s > 0.0f) ? r : 0.0f;
   return sc;
 }
 
@@ -122,7 +126,13 @@ __host__ __device__ inline AppendSmem append_smem_layout(int D, int G, int rec_b
   return a;
 }
 
-constexpr float kNearHalf = 0.5f - 6.103515625e-05f;  // 2^-14 from a rounding boundary
+// The fast path computes y = (x - min) * r with r within 2^-22 (relative) of
+// 1/s, so y is within 2^-22 * y of the correctly rounded quotient; y stays
+// below 1.5 * 255 < 512 (the fp16 scale is at least s32 / 1.5, and far closer
+// for normal scales).  A y within 2^-13 of a rounding boundary is redone
+// with the IEEE division, which covers every case where the two could round
+// to different integers.
+constexpr float kNearHalf = 0.5f - 1.220703125e-04f;  // 2^-13 from a rounding boundary
 
 // code = min(rint((x - min) / s), qmax) with IEEE fp32 subtraction and
 // division: the product with 1/s decides unless it lies within 2^-14 of a
