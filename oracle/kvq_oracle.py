@@ -288,43 +288,66 @@ def flush_state(total: int, residual: int, group: int) -> Tuple[int, int]:
     return n_q, r
 
 
-def record_layout(d: int, group: int, k_bits: int, v_bits: int) -> Dict[str, int]:
-    """Byte offsets inside one group record."""
+# Key quantization modes ([KVTuner] A3 and A4: the KIVI mode and the
+# per-token-asym mode, chosen per layer together with its precision pair)
+KEY_PER_CHANNEL = 0   # keys per channel over the G tokens of a group (KIVI)
+KEY_PER_TOKEN = 1     # keys per token over their d channels, like values
+
+
+def record_layout(d: int, group: int, k_bits: int, v_bits: int, key_mode: int = KEY_PER_CHANNEL) -> Dict[str, int]:
+    """Byte offsets inside one group record.
+
+    Per-channel keys: [K codes][V codes][K scale d][K zero d][V (scale, zero) G].
+    Per-token keys:   [K codes][V codes][K (scale, zero) G][V (scale, zero) G]."""
     wk = words_per_row(d, k_bits)
     wv = words_per_row(d, v_bits)
     off = {}
     off["k_codes"] = 0
     off["v_codes"] = off["k_codes"] + 4 * group * wk
     off["k_scale"] = off["v_codes"] + 4 * group * wv
-    off["k_zero"] = off["k_scale"] + 2 * d
-    off["v_scale"] = off["k_zero"] + 2 * d     # (scale, zero) pairs, one per token
+    if key_mode == KEY_PER_TOKEN:
+        off["k_zero"] = off["k_scale"]            # interleaved with the scales
+        off["v_scale"] = off["k_scale"] + 4 * group
+    else:
+        off["k_zero"] = off["k_scale"] + 2 * d
+        off["v_scale"] = off["k_zero"] + 2 * d    # (scale, zero) pairs, one per token
     off["bytes"] = off["v_scale"] + 4 * group
     off["wk"] = wk
     off["wv"] = wv
     return off
 
 
-def build_group_record(k_grp: np.ndarray, v_grp: np.ndarray, k_bits: int, v_bits: int) -> bytes:
+def build_group_record(k_grp: np.ndarray, v_grp: np.ndarray, k_bits: int, v_bits: int,
+                       key_mode: int = KEY_PER_CHANNEL) -> bytes:
     """Quantize one key group (k_grp, v_grp: [G, d] fp16) and lay out its record."""
-    kc, ks, kz = quantize_keys_group(k_grp, k_bits)
     vc, vs, vz = quantize_values_tokens(v_grp, v_bits)
     vsz = np.stack([vs.astype(F16), vz.astype(F16)], axis=1)  # [G, 2]
-    parts = [pack_rows(kc, k_bits).tobytes(), pack_rows(vc, v_bits).tobytes(),
-             ks.astype(F16).tobytes(), kz.astype(F16).tobytes(), vsz.tobytes()]
+    if key_mode == KEY_PER_TOKEN:
+        kc, ks, kz = quantize_values_tokens(k_grp, k_bits)
+        kparts = [np.stack([ks.astype(F16), kz.astype(F16)], axis=1).tobytes()]
+    else:
+        kc, ks, kz = quantize_keys_group(k_grp, k_bits)
+        kparts = [ks.astype(F16).tobytes(), kz.astype(F16).tobytes()]
+    parts = [pack_rows(kc, k_bits).tobytes(), pack_rows(vc, v_bits).tobytes(), *kparts, vsz.tobytes()]
     return b"".join(parts)
 
 
-def parse_group_record(rec: bytes, d: int, group: int, k_bits: int, v_bits: int):
+def parse_group_record(rec: bytes, d: int, group: int, k_bits: int, v_bits: int,
+                       key_mode: int = KEY_PER_CHANNEL):
     """Inverse of build_group_record's layout: returns dequantized K, V [G, d] fp64."""
-    lay = record_layout(d, group, k_bits, v_bits)
+    lay = record_layout(d, group, k_bits, v_bits, key_mode)
     buf = np.frombuffer(rec, dtype=np.uint8)
     kw = buf[lay["k_codes"]:lay["v_codes"]].view(np.uint32).reshape(group, lay["wk"])
     vw = buf[lay["v_codes"]:lay["k_scale"]].view(np.uint32).reshape(group, lay["wv"])
-    ks = buf[lay["k_scale"]:lay["k_zero"]].view(F16)
-    kz = buf[lay["k_zero"]:lay["v_scale"]].view(F16)
     vsz = buf[lay["v_scale"]:lay["bytes"]].view(F16).reshape(group, 2)
     vs, vz = vsz[:, 0], vsz[:, 1]
-    k_hat = dequant_keys(unpack_rows(kw, k_bits, d), ks, kz, k_bits)
+    if key_mode == KEY_PER_TOKEN:
+        ksz = buf[lay["k_scale"]:lay["v_scale"]].view(F16).reshape(group, 2)
+        k_hat = dequant_values(unpack_rows(kw, k_bits, d), ksz[:, 0], ksz[:, 1], k_bits)
+    else:
+        ks = buf[lay["k_scale"]:lay["k_zero"]].view(F16)
+        kz = buf[lay["k_zero"]:lay["v_scale"]].view(F16)
+        k_hat = dequant_keys(unpack_rows(kw, k_bits, d), ks, kz, k_bits)
     v_hat = dequant_values(unpack_rows(vw, v_bits, d), vs, vz, v_bits)
     return k_hat, v_hat
 
@@ -334,11 +357,12 @@ class OracleLayerCache:
     units, fed in token order."""
 
     def __init__(self, batch: int, n_kv_heads: int, head_dim: int, group: int,
-                 k_bits: int, v_bits: int, residual: int):
+                 k_bits: int, v_bits: int, residual: int, key_mode: int = KEY_PER_CHANNEL):
         if residual < group:
             raise ValueError("residual window must hold at least one key group")
         self.B, self.H, self.d, self.G = batch, n_kv_heads, head_dim, group
         self.kb, self.vb, self.R = k_bits, v_bits, residual
+        self.key_mode = key_mode
         self.total = 0
         self.n_q = 0
         # per unit: list of group records; pending fp16 tokens (oldest first)
@@ -357,7 +381,7 @@ class OracleLayerCache:
         while self.pend_k.shape[1] >= self.R:
             for u in range(self.B * self.H):
                 self.records[u].append(build_group_record(
-                    self.pend_k[u, : self.G], self.pend_v[u, : self.G], self.kb, self.vb))
+                    self.pend_k[u, : self.G], self.pend_v[u, : self.G], self.kb, self.vb, self.key_mode))
             self.pend_k = self.pend_k[:, self.G:]
             self.pend_v = self.pend_v[:, self.G:]
             self.n_q += self.G
@@ -367,7 +391,7 @@ class OracleLayerCache:
         return self.pend_k.shape[1]
 
     def record_bytes(self) -> int:
-        return record_layout(self.d, self.G, self.kb, self.vb)["bytes"]
+        return record_layout(self.d, self.G, self.kb, self.vb, self.key_mode)["bytes"]
 
     def unit_records(self, u: int) -> bytes:
         return b"".join(self.records[u])
@@ -391,7 +415,7 @@ class OracleLayerCache:
         dequantized, residual tokens exact)."""
         ks, vs = [], []
         for rec in self.records[u]:
-            kh, vh = parse_group_record(rec, self.d, self.G, self.kb, self.vb)
+            kh, vh = parse_group_record(rec, self.d, self.G, self.kb, self.vb, self.key_mode)
             ks.append(kh)
             vs.append(vh)
         ks.append(self.pend_k[u].astype(np.float64))

@@ -398,3 +398,74 @@ def test_record_layout_sizes():
             for kb in O.BITS_ALLOWED:
                 for vb in O.BITS_ALLOWED:
                     assert O.record_layout(d, G, kb, vb)["bytes"] % 16 == 0
+
+
+# ---------------------------------------------------------------------------
+# Per-token-asym key mode ([KVTuner] A3-A4: the second quantization mode,
+# keys quantized per token like values)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_per_token_key_record_quantizes_along_tokens(bits):
+    # keys with strong channel outliers: per token, each token's min and max
+    # must land on codes 0 and 2^b - 1 and every element stay within s_t/2
+    rng = np.random.default_rng(100 + bits)
+    G, d = 32, 128
+    k = rng.standard_normal((G, d)) * 1.5
+    k[:, 3] *= 12.0
+    k = k.astype(np.float16)
+    v = rng.standard_normal((G, d)).astype(np.float16)
+    rec = O.build_group_record(k, v, bits, 4, O.KEY_PER_TOKEN)
+    lay = O.record_layout(d, G, bits, 4, O.KEY_PER_TOKEN)
+    assert len(rec) == lay["bytes"]
+    buf = np.frombuffer(rec, dtype=np.uint8)
+    codes = O.unpack_rows(buf[lay["k_codes"]:lay["v_codes"]].view(np.uint32).reshape(G, lay["wk"]), bits, d)
+    ksz = buf[lay["k_scale"]:lay["v_scale"]].view(np.float16).reshape(G, 2)
+    kf = k.astype(np.float64)
+    rows = np.arange(G)
+    assert (codes[rows, kf.argmin(axis=1)] == 0).all()
+    assert (codes[rows, kf.argmax(axis=1)] == 2 ** bits - 1).all()
+    assert (ksz[:, 1] == k.min(axis=1)).all()                        # zero = per-token min
+    s = ksz[:, 0].astype(np.float64)[:, None]
+    kh, vh = O.parse_group_record(rec, d, G, bits, 4, O.KEY_PER_TOKEN)
+    bound = s / 2 + 4 * 2.0 ** -24 * (np.abs(ksz[:, 1].astype(np.float64))[:, None] + (2 ** bits - 1) * s)
+    assert (np.abs(kf - kh) <= bound).all()
+    # values are unaffected by the key mode
+    _, vh0 = O.parse_group_record(O.build_group_record(k, v, bits, 4), d, G, bits, 4)
+    assert (vh == vh0).all()
+    # with outlier channels, per-token keys lose far more than per-channel ones
+    kh0, _ = O.parse_group_record(O.build_group_record(k, v, bits, 4), d, G, bits, 4)
+    assert np.abs(kf - kh).mean() > np.abs(kf - kh0).mean()
+
+
+def test_per_token_key_record_layout_sizes():
+    for d in (64, 128):
+        for G in (32, 64, 128):
+            for kb in (2, 4, 8):
+                for vb in O.BITS_ALLOWED:
+                    lay = O.record_layout(d, G, kb, vb, O.KEY_PER_TOKEN)
+                    assert lay["bytes"] == 4 * G * (lay["wk"] + lay["wv"]) + 4 * G + 4 * G
+                    assert lay["bytes"] % 16 == 0
+
+
+def test_per_token_key_cache_streaming_matches_bulk():
+    rng = np.random.default_rng(13)
+    B, H, d, G, R = 1, 2, 64, 32, 64
+    k = rng.standard_normal((B, H, 200, d)).astype(np.float16)
+    v = rng.standard_normal((B, H, 200, d)).astype(np.float16)
+    a = O.OracleLayerCache(B, H, d, G, 8, 2, R, O.KEY_PER_TOKEN)
+    a.append(k, v)
+    b = O.OracleLayerCache(B, H, d, G, 8, 2, R, O.KEY_PER_TOKEN)
+    pos = 0
+    for n in (3, 61, 1, 1, 90, 44):
+        b.append(k[:, :, pos:pos + n], v[:, :, pos:pos + n])
+        pos += n
+    assert (a.n_q, a.r) == (b.n_q, b.r) == O.flush_state(200, R, G)
+    for u in range(B * H):
+        assert a.unit_records(u) == b.unit_records(u)
+    # attention over per-token-quantized 8-bit keys stays close to exact attention
+    q = rng.standard_normal((B, H, d)).astype(np.float16)
+    kh, vh = a.dequantized(0)
+    o = O.attention_fp64(q[0, 0].astype(np.float64), kh, vh)
+    oe = O.attention_fp64(q[0, 0].astype(np.float64), k[0, 0].astype(np.float64), vh)
+    assert np.abs(o - oe).max() < 0.05
