@@ -8,8 +8,8 @@
  *     ("KVTuner: Sensitivity-Aware Layer-Wise Mixed-Precision KV Cache
  *     Quantization ...", sections A1 and A2; "KVmix: Gradient-Based Layer
  *     Importance-Aware Mixed-Precision Quantization for KV Cache", 关键设计 2 and 4);
- *   - keys are quantized asymmetrically per channel over groups of G tokens,
- *     values per token, with scale = (max - min)/(2^b - 1), zero = min and
+ *   - keys are quantized asymmetrically per channel over groups of G tokens
+ *     (or, per layer, per token), values per token, with scale = (max - min)/(2^b - 1), zero = min and
  *     code = clamp(rint((x - min)/scale), 0, 2^b - 1); codes are packed into
  *     32-bit words, 3-bit words holding ten 3-bit fields and one 2-bit field
  *     (KVTuner section A3 "KV缓存量化基础"; KVmix 关键设计 2; "LLM 量化精读笔记 · 08
@@ -59,12 +59,21 @@ typedef enum {
   KVQ_ERR_UNSUPPORTED = 7 /* a shape this build has no kernel for          */
 } kvq_status;
 
-/* One layer's static precision pair and FP16 residual window (tokens).
- * k_bits, v_bits in {2, 3, 4, 8}; residual >= group_size and a multiple of it. */
+/* Key quantization mode of a layer (KVTuner sections A3-A4 evaluate both):
+ *   KVQ_KEY_PER_CHANNEL: keys per channel over each group of G tokens (KIVI);
+ *   KVQ_KEY_PER_TOKEN:   keys per token over their head_dim channels, like
+ *                        values ("per-token-asym"); k_bits in {2, 4, 8}. */
+#define KVQ_KEY_PER_CHANNEL 0
+#define KVQ_KEY_PER_TOKEN 1
+
+/* One layer's static precision pair, key mode and FP16 residual window (tokens).
+ * k_bits, v_bits in {2, 3, 4, 8}; residual >= group_size and a multiple of it.
+ * key_mode KVQ_KEY_PER_TOKEN with k_bits = 3 is KVQ_ERR_UNSUPPORTED. */
 typedef struct {
   uint8_t k_bits;
   uint8_t v_bits;
-  uint16_t reserved; /* must be 0 */
+  uint8_t key_mode;  /* KVQ_KEY_PER_CHANNEL or KVQ_KEY_PER_TOKEN */
+  uint8_t reserved;  /* must be 0 */
   int32_t residual;
 } kvq_layer_cfg;
 
@@ -95,7 +104,8 @@ typedef struct kvq_handle kvq_handle;
  *   quantized key group (group j covers tokens [j*G, (j+1)*G)), each
  *   record_bytes long:
  *     [K codes: G rows x k_words u32][V codes: G rows x v_words u32]
- *     [K scale: head_dim f16][K zero: head_dim f16]
+ *     [K scale: head_dim f16][K zero: head_dim f16]   (per-channel keys), or
+ *     [K (scale, zero): G pairs of f16]               (per-token keys)
  *     [V (scale, zero): G pairs of f16]
  *   A code row is one token's head_dim codes, least significant field first:
  *   for b in {2,4,8} field j of word w is channel w*32/b + j at bits [b*j, b*j+b);
@@ -107,6 +117,7 @@ typedef struct kvq_handle kvq_handle;
 typedef struct {
   int32_t k_bits, v_bits, residual, group_size, head_dim;
   int32_t k_words, v_words;          /* u32 words per code row                */
+  int32_t key_mode;                  /* KVQ_KEY_PER_CHANNEL or _PER_TOKEN     */
   int64_t record_bytes;
   int64_t unit_record_stride;        /* bytes between units' record arrays    */
   int64_t residual_stride;           /* bytes between units' rings            */

@@ -28,6 +28,7 @@ bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 8; }
 
 struct LayerPlan {
   int kb, vb, R;
+  int km;  // key mode: 0 per channel over key groups, 1 per token
   int wk, wv;
   int64_t rec_bytes;
   int64_t max_groups;
@@ -79,6 +80,8 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
     const kvq_layer_cfg& lc = cfg->layers[l];
     if (lc.reserved != 0) return KVQ_ERR_ARG;
     if (!bits_ok(lc.k_bits) || !bits_ok(lc.v_bits)) return KVQ_ERR_BITS;
+    if (lc.key_mode != KVQ_KEY_PER_CHANNEL && lc.key_mode != KVQ_KEY_PER_TOKEN) return KVQ_ERR_ARG;
+    if (lc.key_mode == KVQ_KEY_PER_TOKEN && lc.k_bits == 3) return KVQ_ERR_UNSUPPORTED;
     if (lc.residual < P->G || lc.residual % P->G != 0) return KVQ_ERR_ARG;
     LayerPlan lp;
     lp.kb = lc.k_bits;
@@ -86,11 +89,13 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
     lp.R = lc.residual;
     lp.wk = words_per_row(P->D, lp.kb);
     lp.wv = words_per_row(P->D, lp.vb);
-    lp.rec_bytes = 4LL * P->G * (lp.wk + lp.wv) + 4LL * P->D + 4LL * P->G;
+    lp.km = lc.key_mode;
+    // key scale/zero: d pairs of rows per group (per channel) or one pair per token
+    lp.rec_bytes = 4LL * P->G * (lp.wk + lp.wv) + (lp.km ? 4LL * P->G : 4LL * P->D) + 4LL * P->G;
     lp.max_groups = P->max_tokens / P->G;
     {
       // the decode kernel splits a layer's work in 32-bit byte-cost units
-      const int64_t slice = 4LL * 32 * (lp.wk + lp.wv) + 4LL * P->D + 128;
+      const int64_t slice = 4LL * 32 * (lp.wk + lp.wv) + (lp.km ? 128LL : 4LL * P->D) + 128;
       const int64_t tile = 16LL * 4 * P->D;
       const int64_t setup = 16 * (slice > 2048 ? slice : 2048);  // 2 x up to 8 warps per CTA
       const int64_t per_unit = setup + lp.max_groups * (P->G / 32) * slice + ((lp.R + 15) / 16) * tile;
@@ -156,6 +161,7 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   ap.G = P.G;
   ap.R = lp.R;
   ap.rec_bytes = static_cast<int>(lp.rec_bytes);
+  ap.key_mode = lp.km;
   ap.unit_rec_stride = lp.unit_rec_stride;
   ap.records = h->base + lp.off_records;
   ap.res_k = reinterpret_cast<__half*>(h->base + lp.off_res_k);
@@ -250,8 +256,7 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
   h->tokens.assign(P.L, 0);
   for (int l = 0; l < P.L; ++l) {
     const LayerPlan& lp = P.layers[l];
-    kvq::DecodeKernel k =
-        kvq::decode_select(lp.kb, lp.vb, P.D, P.gqa, P.G, static_cast<int>(lp.rec_bytes));
+    kvq::DecodeKernel k = kvq::decode_select(lp.kb, lp.vb, P.D, P.gqa, lp.km);
     if (!k.fn) {
       delete h;
       return KVQ_ERR_UNSUPPORTED;
@@ -365,6 +370,7 @@ kvq_status kvq_layer_view_get(const kvq_handle* h, int layer, kvq_layer_view* v)
   v->head_dim = P.D;
   v->k_words = lp.wk;
   v->v_words = lp.wv;
+  v->key_mode = lp.km;
   v->record_bytes = lp.rec_bytes;
   v->unit_record_stride = lp.unit_rec_stride;
   v->residual_stride = lp.res_stride_elems * 2;

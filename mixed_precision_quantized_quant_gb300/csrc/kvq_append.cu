@@ -90,7 +90,8 @@ __device__ __forceinline__ void pack8(const uint32_t (&c)[8], uint32_t& w0, uint
 // Shared-memory layout of the flush path.
 struct AppendSmem {
   int tile;  // bytes of one staged [G][D] fp16 tile
-  int off_stage1, off_rec, off_ksc, off_kp, off_vsc, off_vr2, off_kmn, off_kmx, off_vpart, off_bars, total;
+  int off_stage1, off_rec, off_ksc, off_kp, off_vsc, off_vr2, off_kmn, off_kmx, off_vpart, off_kpt, off_ksct,
+      off_bars, total;
 };
 
 // Flush CTAs run 4*G threads: each thread owns one 16-byte chunk of D/32 rows.
@@ -120,6 +121,10 @@ __host__ __device__ inline AppendSmem append_smem_layout(int D, int G, int rec_b
   off += warps * D * 2;  // ... and max
   a.off_vpart = off;
   off += G * 4;   // per token {min, -max}
+  a.off_kpt = off;
+  off += G * 4;   // per-token keys: per token {min, -max}
+  a.off_ksct = off;
+  off += G * 16;  // per-token keys: per token {min, s, 1/s, qmax}
   a.off_bars = off;
   off += 16;
   a.total = off;
@@ -245,9 +250,15 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
   uint8_t* rec = smem + L.off_rec;
   uint32_t* kc = reinterpret_cast<uint32_t*>(rec);
   uint32_t* vc = kc + G * WK;
+  // per-token keys (uniform for the launch): one (scale, zero) pair per token
+  // instead of the per-channel scale and zero rows
+  const bool ktok = p.key_mode == 1;
   __half* ks16 = reinterpret_cast<__half*>(vc + G * WV);
   __half* kz16 = ks16 + D;
-  __half2* vsz = reinterpret_cast<__half2*>(kz16 + D);
+  __half2* ksz = reinterpret_cast<__half2*>(vc + G * WV);
+  __half2* vsz = ktok ? ksz + G : reinterpret_cast<__half2*>(kz16 + D);
+  __half2* kpt = reinterpret_cast<__half2*>(smem + L.off_kpt);
+  float4* ksct = reinterpret_cast<float4*>(smem + L.off_ksct);
   float4* ksc = reinterpret_cast<float4*>(smem + L.off_ksc);
   float4* vsc = reinterpret_cast<float4*>(smem + L.off_vsc);
   float* vr2 = reinterpret_cast<float*>(smem + L.off_vr2);
@@ -272,7 +283,25 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
     xk[k] = kq[t * CH + pc];
     xv[k] = vq[t * CH + pc];
   }
-  {
+  // (min, -max) of a row's chunks over its CH lanes: one min-reduction serves both
+  auto row_minmax = [&](const uint4& x) -> __half2 {
+    const __half2* h = reinterpret_cast<const __half2*>(&x);
+    const __half2 m2 = __hmin2(__hmin2(h[0], h[1]), __hmin2(h[2], h[3]));
+    const __half2 M2 = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+    __half2 r = __halves2half2(__hmin(__low2half(m2), __high2half(m2)),
+                               __hneg(__hmax(__low2half(M2), __high2half(M2))));
+#pragma unroll
+    for (int off = 1; off < CH; off <<= 1)
+      r = __hmin2(r, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(r), off)));
+    return r;
+  };
+  if (ktok) {
+#pragma unroll
+    for (int k = 0; k < RT; ++k) {
+      const __half2 r = row_minmax(xk[k]);
+      if (c == 0) kpt[rg + k * RG] = r;
+    }
+  } else {
     __half2 mn[4], mx[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -303,23 +332,24 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
   }
 #pragma unroll
   for (int k = 0; k < RT; ++k) {
-    const __half2* h = reinterpret_cast<const __half2*>(&xv[k]);
-    const __half2 m2 = __hmin2(__hmin2(h[0], h[1]), __hmin2(h[2], h[3]));
-    const __half2 M2 = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
-    // (min, -max): one min-reduction serves both
-    __half2 r = __halves2half2(__hmin(__low2half(m2), __high2half(m2)),
-                               __hneg(__hmax(__low2half(M2), __high2half(M2))));
-#pragma unroll
-    for (int off = 1; off < CH; off <<= 1)
-      r = __hmin2(r, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(r), off)));
+    const __half2 r = row_minmax(xv[k]);
     if (c == 0) vpart[rg + k * RG] = r;
   }
   if (tid == 0) bulk_wait_read_all();  // the previous record has left the staging area
   // every thread saw its stage arrive, or all of them stop here
   if (__syncthreads_or(!staged)) return false;
 
-  // ---- phase 2: one scale per thread (channel tid, token tid)
-  if (tid < D) {
+  // ---- phase 2: one scale per thread (channel tid, token tid; per-token
+  // keys: token tid - G)
+  if (ktok) {
+    if (KB != 3 && tid >= G && tid < 2 * G) {
+      const int t = tid - G;
+      const __half2 r = kpt[t];
+      const Scale sc = make_scale<KB>(__low2half(r), __hneg(__high2half(r)), false);
+      ksct[t] = make_float4(sc.mn, sc.s, sc.r, sc.qmax);
+      ksz[t] = __halves2half2(sc.s16, sc.z16);
+    }
+  } else if (tid < D) {
     // thread tid takes channel 8*(tid % CH) + tid / CH, whose table slot is tid
     const int ch = 8 * (tid % CH) + tid / CH;
     const int warps = 4 * G / 32;
@@ -356,7 +386,33 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
   __syncthreads();
 
   // ---- phase 3: codes, packed LSB first into the record staging area
-  if constexpr (KB != 3) {
+  // (the packing of a row's codes is the same for both key modes)
+  auto put_k = [&](int t, const uint32_t (&code)[8]) {
+    uint32_t w0, w1;
+    pack8<KB>(code, w0, w1);
+    if (KB == 8) {
+      *reinterpret_cast<uint2*>(kc + t * WK + 2 * c) = make_uint2(w0, w1);
+    } else if (KB == 4) {
+      kc[t * WK + c] = w0;
+    } else {  // KB == 2: two lanes form one word
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
+      if ((c & 1) == 0) kc[t * WK + c / 2] = w0 | (other << 16);
+    }
+  };
+  if (ktok) {
+    if constexpr (KB != 3) {
+#pragma unroll
+      for (int k = 0; k < RT; ++k) {
+        const int t = rg + k * RG;
+        const float4 s = ksct[t];
+        const uint64_t m = f2pack(s.x, s.x), r = f2pack(s.z, s.z);
+        const uint64_t mn2[4] = {m, m, m, m}, r2[4] = {r, r, r, r};
+        uint32_t code[8];
+        quant8(xk[k], mn2, r2, (1u << KB) - 1, ksct + t, 0, -1.0f, code);
+        put_k(t, code);
+      }
+    }
+  } else if constexpr (KB != 3) {
     const uint64_t* kp = reinterpret_cast<const uint64_t*>(smem + L.off_kp);
     uint64_t mn2[4], r2[4];
 #pragma unroll
@@ -369,16 +425,7 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
       const int t = rg + k * RG;
       uint32_t code[8];
       quant8(xk[k], mn2, r2, (1u << KB) - 1, ksc + c, CH, -1.0f, code);
-      uint32_t w0, w1;
-      pack8<KB>(code, w0, w1);
-      if (KB == 8) {
-        *reinterpret_cast<uint2*>(kc + t * WK + 2 * c) = make_uint2(w0, w1);
-      } else if (KB == 4) {
-        kc[t * WK + c] = w0;
-      } else {  // KB == 2: two lanes form one word
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
-        if ((c & 1) == 0) kc[t * WK + c / 2] = w0 | (other << 16);
-      }
+      put_k(t, code);
     }
   } else {
     for (int idx = tid; idx < G * WK; idx += blockDim.x) {

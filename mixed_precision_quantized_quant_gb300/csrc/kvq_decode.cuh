@@ -35,25 +35,26 @@ namespace kvq {
 constexpr int kSlots = 4;   // copies in flight per warp (mbarrier slots)
 constexpr int kSlice = 32;  // tokens of a key group staged per work item
 
-// Bytes of one staged 32-token slice of a group record:
-// [K rows][V rows][K scale][K zero][V (scale, zero) pairs].
-__host__ __device__ constexpr int slice_bytes(int D, int G, int rec_bytes) {
-  return (rec_bytes - 4 * D - 4 * G) / G * kSlice + 4 * D + 4 * kSlice;
+// Bytes of one staged 32-token slice of a group record: [K rows][V rows]
+// then [K scale d][K zero d] (per-channel keys) or [K (scale, zero) 32 pairs]
+// (per-token keys), then [V (scale, zero) 32 pairs].
+__host__ __device__ constexpr int slice_bytes(int D, int wk, int wv, int km) {
+  return kSlice * 4 * (wk + wv) + (km ? 4 * kSlice : 4 * D) + 4 * kSlice;
 }
 
 // Per-warp ring of staged items: at least two slices, and at least one
 // residual tile (a tile waits for the ring to drain when it does not fit
 // beside the slices in flight; tiles are few, and a smaller ring fits more
 // CTAs on an SM).
-__host__ __device__ constexpr int ring_bytes(int D, int G, int rec_bytes) {
-  const int sl = slice_bytes(D, G, rec_bytes), rt = kResTile * 4 * D;
-  const int need = (rt > 2 * sl) ? rt : 2 * sl;
+__host__ __device__ constexpr int ring_bytes(int D, int cq) {
+  const int rt = kResTile * 4 * D;
+  const int need = (rt > 2 * cq) ? rt : 2 * cq;
   return (need + 127) / 128 * 128;
 }
 
 struct DecodeSmem {
   int ring;
-  int off_bars, off_qs, off_qp, off_qps, off_qr, off_wm, off_wl, off_dm, off_flags, off_wo, total;
+  int off_bars, off_qs, off_qp, off_qps, off_qr, off_qsum, off_wm, off_wl, off_dm, off_flags, off_wo, total;
 };
 
 // W warps per CTA, each with its own ring of `ring` bytes.
@@ -73,6 +74,8 @@ __host__ __device__ constexpr DecodeSmem decode_smem_layout_ring(int D, int NT, 
   off += 32 * NT * 18 * 4;           // same, scaled by 2^(Pmax - pos) per pair
   s.off_qr = off;
   off += 32 * NT * D / 16 * 2 * 4;   // residual (fp16 key) query table
+  s.off_qsum = off;
+  off += H * 4;                      // per head sum of the query (per-token keys)
   s.off_wm = off;
   off += W * H * 4;
   s.off_wl = off;
@@ -88,8 +91,8 @@ __host__ __device__ constexpr DecodeSmem decode_smem_layout_ring(int D, int NT, 
   return s;
 }
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, int rec_bytes, int W) {
-  return decode_smem_layout_ring(D, NT, ring_bytes(D, G, rec_bytes), W);
+__host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int cq, int W) {
+  return decode_smem_layout_ring(D, NT, ring_bytes(D, cq), W);
 }
 
 // Warps per CTA of an instantiation: 8 where two such CTAs fit in an SM's
@@ -97,13 +100,11 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int G, i
 // merges at the same occupancy), else 4.  3-bit values keep 4: they need more
 // than the 128 registers a thread may use at 2 x 256 threads per SM.  The ring
 // size does not depend on G.
-template <int KB, int VB, int D, int NT>
+template <int KB, int VB, int D, int NT, int KM>
 __host__ __device__ constexpr int decode_warps() {
   constexpr int WK = (KB == 3) ? (D + 10) / 11 : D * KB / 32;
   constexpr int WV = (VB == 3) ? (D + 10) / 11 : D * VB / 32;
-  constexpr int sl = kSlice * 4 * (WK + WV) + 4 * D + 4 * kSlice;
-  constexpr int rt = kResTile * 4 * D;
-  constexpr int ring = ((rt > 2 * sl ? rt : 2 * sl) + 127) / 128 * 128;
+  constexpr int ring = ring_bytes(D, slice_bytes(D, WK, WV, KM));
   constexpr int smem8 = decode_smem_layout_ring(D, NT, ring, 8).total;
   return (NT == 1 && VB != 3 && 2 * (smem8 + 1024) <= 228 * 1024) ? 8 : 4;
 }
@@ -398,10 +399,12 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
 
 // ------------------------------------------------------------------ kernel
 
-template <int KB, int VB, int D, int NT>
-__global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
-                                  decode_warps<KB, VB, D, NT>() == 8 ? 2 : (NT == 1 ? 3 : 2))
+// KM: key mode, 0 = per channel over key groups, 1 = per token.
+template <int KB, int VB, int D, int NT, int KM>
+__global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
+                                  decode_warps<KB, VB, D, NT, KM>() == 8 ? 2 : (NT == 1 ? 3 : 2))
     decode_kernel(DecodeParams p) {
+  static_assert(KM == 0 || KB != 3, "per-token keys are 2, 4 or 8 bits");
   using KS_ = KeyShape<KB, D>;
   using VS_ = ValShape<VB, D>;
   constexpr int KS = D / 16;            // residual k-steps / channel m-tiles
@@ -413,16 +416,18 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
   constexpr int MTA = MTV > KS ? MTV : KS;
   constexpr int NP = D / 8;
   constexpr int H = 4 * NT;             // padded query heads
-  constexpr int W = decode_warps<KB, VB, D, NT>();  // warps per CTA
+  constexpr int W = decode_warps<KB, VB, D, NT, KM>();  // warps per CTA
   constexpr int TH = 32 * W;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  const DecodeSmem L = decode_smem_layout(D, NT, p.G, p.rec_bytes, W);
+  constexpr int kCq = slice_bytes(D, WK, WV, KM);
+  const DecodeSmem L = decode_smem_layout(D, NT, kCq, W);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
   __half* qs = reinterpret_cast<__half*>(smem + L.off_qs);
   uint32_t* qp_tab = reinterpret_cast<uint32_t*>(smem + L.off_qp);
   uint32_t* qps_tab = reinterpret_cast<uint32_t*>(smem + L.off_qps);
   uint32_t* qr_tab = reinterpret_cast<uint32_t*>(smem + L.off_qr);
+  float* qsum_s = reinterpret_cast<float*>(smem + L.off_qsum);
   float* wm = reinterpret_cast<float*>(smem + L.off_wm);
   float* wl = reinterpret_cast<float*>(smem + L.off_wl);
   float* dm = reinterpret_cast<float*>(smem + L.off_dm);
@@ -457,7 +462,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
   const int NG = nq / kSlice;             // quantized work items (slices)
   const int NRT = (r + kResTile - 1) / kResTile;
   const int NI = NG + NRT;
-  constexpr uint32_t cq = kSlice * 4 * (WK + WV) + 4 * D + 4 * kSlice;  // staged slice bytes
+  constexpr uint32_t cq = kCq;                                          // staged slice bytes
   constexpr uint32_t cr = kResTile * 4 * D;                             // residual tile bytes
   // per-unit setup cost (query tables, warp merge, partial write): measured
   // at about the time a CTA needs for 2*W slices
@@ -587,9 +592,15 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
             mbar_arrive_expect_tx(&wbar[st], cq);
             bulk_g2s(dst, rec + t0 * WK * 4, kbytes, &wbar[st]);
             bulk_g2s(dst + kbytes, rec + p.G * WK * 4 + t0 * WV * 4, vbytes, &wbar[st]);
-            bulk_g2s(dst + kbytes + vbytes, rec + p.G * (WK + WV) * 4, 4 * D, &wbar[st]);
-            bulk_g2s(dst + kbytes + vbytes + 4 * D, rec + p.G * (WK + WV) * 4 + 4 * D + t0 * 4, 4 * kSlice,
-                     &wbar[st]);
+            if constexpr (KM == 0) {  // all key scales and zeros, the slice's value pairs
+              bulk_g2s(dst + kbytes + vbytes, rec + p.G * (WK + WV) * 4, 4 * D, &wbar[st]);
+              bulk_g2s(dst + kbytes + vbytes + 4 * D, rec + p.G * (WK + WV) * 4 + 4 * D + t0 * 4, 4 * kSlice,
+                       &wbar[st]);
+            } else {  // the slice's key pairs and value pairs
+              bulk_g2s(dst + kbytes + vbytes, rec + p.G * (WK + WV) * 4 + t0 * 4, 4 * kSlice, &wbar[st]);
+              bulk_g2s(dst + kbytes + vbytes + 4 * kSlice, rec + p.G * (WK + WV) * 4 + 4 * p.G + t0 * 4,
+                       4 * kSlice, &wbar[st]);
+            }
           }
         } else {
           const int slot0 = (nq + (i - NG) * kResTile) % p.R;
@@ -641,7 +652,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
           const __half2 q2 = __halves2half2(qa, qb);
           qp_tab[kt_idx(j, pi, lane)] = h2_as_u32(q2);
           const float f = static_cast<float>(1 << (key_pos_max<KB>() - key_pos<KB, D>(pi)));
-          qps_tab[kt_idx(j, pi, lane)] = h2_as_u32(__hmul2(q2, __float2half2_rn(f)));
+          const uint32_t scaled = h2_as_u32(__hmul2(q2, __float2half2_rn(f)));
+          // per-token keys: the scaled query is the whole B operand (hi column; lo = 0)
+          qps_tab[kt_idx(j, pi, lane)] = (KM == 1 && part) ? 0u : scaled;
         }
         for (int kk = warp; kk < KS; kk += W) {
           for (int rr = 0; rr < 2; ++rr) {
@@ -651,9 +664,36 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
           }
         }
       }
+      if constexpr (KM == 1) {
+        // per head: sum_c q_c (scaled like the scores), for the keys' zero term
+        constexpr float kSS = static_cast<float>(1 << key_pos_max<KB>()) / 16777216.0f;
+        for (int h = warp; h < H; h += W) {
+          float sum = 0.0f;
+#pragma unroll
+          for (int c = lane; c < D; c += 32) sum += __half2float(qu[h * D + c]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          if (lane == 0) qsum_s[h] = h < p.gqa ? sum * kSS : 0.0f;
+        }
+      }
     }
     __syncthreads();
     if (tid == 0 && u + 2 <= u_last) issue_q(u + 2, seg & 1);
+    // per-token keys: the B operand of the scores is fixed for the unit
+    uint32_t bqu[KM == 1 ? NT : 1][KM == 1 ? NPK : 1];
+    float qsj[NT];
+    if constexpr (KM == 1) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        qsj[j] = qsum_s[4 * j + tig];
+#pragma unroll
+        for (int pi = 0; pi < NPK; pi += 2) {
+          const uint2 v = *reinterpret_cast<const uint2*>(qps_tab + kt_idx(j, pi, lane));
+          bqu[j][pi] = v.x;
+          bqu[j][pi + 1] = v.y;
+        }
+      }
+    }
 
     // ---------------- warp state for this unit
     float m[NT], l[NT], vb[NT];
@@ -740,9 +780,20 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
         has_q = true;
         const uint32_t* Kc = reinterpret_cast<const uint32_t*>(stg);
         const uint32_t* Vc = Kc + kSlice * WK;
-        const __half* Ks = reinterpret_cast<const __half*>(Vc + kSlice * WV);
+        const __half* Ks = reinterpret_cast<const __half*>(Vc + kSlice * WV);  // per-channel keys
         const __half* Kz = Ks + D;
-        const __half2* Vsz = reinterpret_cast<const __half2*>(Kz + D);
+        const __half2* Ksz = reinterpret_cast<const __half2*>(Vc + kSlice * WV);  // per-token keys
+        const __half2* Vsz = KM == 0 ? reinterpret_cast<const __half2*>(Kz + D) : Ksz + kSlice;
+        float bias[NT];
+        uint32_t bq[NT][NPK];
+        if constexpr (KM == 1) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            bias[j] = 0.0f;
+#pragma unroll
+            for (int pi = 0; pi < NPK; ++pi) bq[j][pi] = bqu[j][pi];
+          }
+        } else {
 
         uint32_t qp[NT][NPK];
 #pragma unroll
@@ -805,7 +856,6 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
           }
         }
         // bias = sum_c q_c z_c: MMAs with the zeros broadcast over rows (two chains)
-        float bias[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -816,7 +866,6 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
           bias[j] = (c0[0] + c1[0]) * kScoreScale;  // in the scaled score domain
         }
         // folded query q~ = q * s (scaled): hi part in even columns, lo part in odd ones
-        uint32_t bq[NT][NPK];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -845,6 +894,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
               }
             }
           }
+        }  // per-channel keys
 
         // ---- scores of the slice's 32 tokens: tiles 0 (tokens 0..15) and 1 (16..31);
         // rows g and g+8 of each; two accumulator chains per tile (the bias is
@@ -929,11 +979,15 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
 
         // the last reads of the slot: each token's value (scale, zero); after
         // them the slot is free for the next copy while the softmax and P.V run
-        float2 sz[2][2];
+        float2 sz[2][2], kz2[2][2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           sz[t][0] = __half22float2(Vsz[16 * t + g]);
           sz[t][1] = __half22float2(Vsz[16 * t + g + 8]);
+          if constexpr (KM == 1) {
+            kz2[t][0] = __half22float2(Ksz[16 * t + g]);
+            kz2[t][1] = __half22float2(Ksz[16 * t + g + 8]);
+          }
         }
         release_slot();
 
@@ -945,8 +999,13 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT>(),
         for (int j = 0; j < NT; ++j) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            s[t][j][0] = (sc[t][j][0] + sc[t][j][1]) + bias[j];
-            s[t][j][1] = (sc[t][j][2] + sc[t][j][3]) + bias[j];
+            if constexpr (KM == 1) {  // s_t * (q . codes_t) + z_t * sum(q), per token
+              s[t][j][0] = fmaf(kz2[t][0].x, sc[t][j][0] + sc[t][j][1], kz2[t][0].y * qsj[j]);
+              s[t][j][1] = fmaf(kz2[t][1].x, sc[t][j][2] + sc[t][j][3], kz2[t][1].y * qsj[j]);
+            } else {
+              s[t][j][0] = (sc[t][j][0] + sc[t][j][1]) + bias[j];
+              s[t][j][1] = (sc[t][j][2] + sc[t][j][3]) + bias[j];
+            }
           }
           tmax[j] = alpha_q * fmaxf(fmaxf(s[0][j][0], s[0][j][1]), fmaxf(s[1][j][0], s[1][j][1]));
         }

@@ -5,22 +5,26 @@
 
 namespace kvq {
 
-template <int VB, int D, int NT>
+template <int VB, int D, int NT, int KM>
 static DecodeKernel make() {
   DecodeKernel k;
-  k.fn = decode_kernel<4, VB, D, NT>;
+  k.fn = decode_kernel<4, VB, D, NT, KM>;
   k.smem = 0;
   k.ctas_per_sm = 0;
-  k.threads = 32 * decode_warps<4, VB, D, NT>();
+  k.threads = 32 * decode_warps<4, VB, D, NT, KM>();
   return k;
 }
 
-DecodeKernel decode_get_k4(int vb, int D, int nt) {
+DecodeKernel decode_get_k4(int vb, int D, int nt, int km) {
   DecodeKernel none{nullptr, 0, 0, 0};
-#define E(VB)                                                               \
-  if (vb == VB) {                                                           \
-    if (D == 128) return nt == 1 ? make<VB, 128, 1>() : make<VB, 128, 2>(); \
-    return nt == 1 ? make<VB, 64, 1>() : make<VB, 64, 2>();                 \
+#define E(VB)                                                                         \
+  if (vb == VB) {                                                                     \
+    if (km == 0) {                                                                    \
+      if (D == 128) return nt == 1 ? make<VB, 128, 1, 0>() : make<VB, 128, 2, 0>();   \
+      return nt == 1 ? make<VB, 64, 1, 0>() : make<VB, 64, 2, 0>();                   \
+    }                                                                                 \
+    if (D == 128) return nt == 1 ? make<VB, 128, 1, 1>() : make<VB, 128, 2, 1>();     \
+    return nt == 1 ? make<VB, 64, 1, 1>() : make<VB, 64, 2, 1>();                     \
   }
   E(2) E(3) E(4) E(8)
 #undef E

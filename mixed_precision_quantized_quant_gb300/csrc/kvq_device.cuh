@@ -39,6 +39,7 @@ struct AppendParams {
   int units;              // batch * kv heads
   int G, R;
   int rec_bytes;
+  int key_mode;           // 0: keys per channel over each group; 1: keys per token
   int64_t unit_rec_stride;   // bytes
   uint8_t* records;
   __half* res_k;          // [units][R][D] ring (chunk-swizzled)

@@ -24,8 +24,9 @@ struct DecodeKernel {
   int ctas_per_sm;  // occupancy at that smem
   int threads;      // threads per CTA
 };
+// km: key mode (0 per channel over key groups, 1 per token).
 // Returns fn == nullptr if the combination has no instantiation.
-DecodeKernel decode_select(int kb, int vb, int D, int gqa, int G, int rec_bytes);
-size_t decode_smem_bytes(int D, int nt, int G, int rec_bytes, int warps);
+DecodeKernel decode_select(int kb, int vb, int D, int gqa, int km);
+size_t decode_smem_bytes(int kb, int vb, int D, int nt, int km, int warps);
 
 }  // namespace kvq

@@ -33,9 +33,12 @@ class KVQError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(status, status)}")
 
 
+KEY_PER_CHANNEL, KEY_PER_TOKEN = 0, 1
+
+
 class LayerCfg(ctypes.Structure):
-    _fields_ = [("k_bits", ctypes.c_uint8), ("v_bits", ctypes.c_uint8),
-                ("reserved", ctypes.c_uint16), ("residual", ctypes.c_int32)]
+    _fields_ = [("k_bits", ctypes.c_uint8), ("v_bits", ctypes.c_uint8), ("key_mode", ctypes.c_uint8),
+                ("reserved", ctypes.c_uint8), ("residual", ctypes.c_int32)]
 
 
 class Config(ctypes.Structure):
@@ -48,7 +51,7 @@ class Config(ctypes.Structure):
 class LayerView(ctypes.Structure):
     _fields_ = [("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32), ("residual", ctypes.c_int32),
                 ("group_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("k_words", ctypes.c_int32), ("v_words", ctypes.c_int32),
+                ("k_words", ctypes.c_int32), ("v_words", ctypes.c_int32), ("key_mode", ctypes.c_int32),
                 ("record_bytes", ctypes.c_int64), ("unit_record_stride", ctypes.c_int64),
                 ("residual_stride", ctypes.c_int64), ("tokens", ctypes.c_int64),
                 ("quantized_tokens", ctypes.c_int64), ("residual_tokens", ctypes.c_int64),
@@ -102,11 +105,14 @@ def _check(st: int, where: str) -> None:
         raise KVQError(st, where)
 
 
-def make_config(layers: Sequence[Tuple[int, int, int]], batch: int, num_q_heads: int, num_kv_heads: int,
+def make_config(layers: Sequence[Tuple[int, ...]], batch: int, num_q_heads: int, num_kv_heads: int,
                 head_dim: int, group_size: int, max_tokens: int):
+    """layers: (k_bits, v_bits, residual) or (k_bits, v_bits, residual, key_mode) per layer."""
     arr = (LayerCfg * len(layers))()
-    for i, (kb, vb, r) in enumerate(layers):
-        arr[i].k_bits, arr[i].v_bits, arr[i].reserved, arr[i].residual = kb, vb, 0, r
+    for i, spec in enumerate(layers):
+        kb, vb, r = spec[:3]
+        km = spec[3] if len(spec) > 3 else KEY_PER_CHANNEL
+        arr[i].k_bits, arr[i].v_bits, arr[i].key_mode, arr[i].reserved, arr[i].residual = kb, vb, km, 0, r
     cfg = Config(len(layers), batch, num_q_heads, num_kv_heads, head_dim, group_size, max_tokens,
                  ctypes.cast(arr, ctypes.POINTER(LayerCfg)))
     cfg._keep = arr  # keep the layer array alive with the struct

@@ -59,7 +59,7 @@ def compare_layer(cache, layer: int, ora: O.OracleLayerCache, units=None) -> Non
 
 
 def describe_record_mismatch(got: bytes, exp: bytes, ora, u: int) -> str:
-    lay = O.record_layout(ora.d, ora.G, ora.kb, ora.vb)
+    lay = O.record_layout(ora.d, ora.G, ora.kb, ora.vb, ora.key_mode)
     rb = lay["bytes"]
     if len(got) != len(exp):
         return f"unit {u}: record bytes {len(got)} != {len(exp)}"

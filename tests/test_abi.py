@@ -53,7 +53,8 @@ def test_cache_bytes_rejects_bad_configs(lib):
     assert K.kvq_cache_bytes(_cfg()) > 0
     bad = [dict(head_dim=96), dict(group_size=48), dict(num_q_heads=6, num_kv_heads=4),
            dict(num_q_heads=32, num_kv_heads=2), dict(layers=[(5, 2, 32)]), dict(layers=[(4, 2, 48)]),
-           dict(layers=[(4, 2, 16)]), dict(batch=0), dict(max_tokens=0)]
+           dict(layers=[(4, 2, 16)]), dict(batch=0), dict(max_tokens=0),
+           dict(layers=[(3, 2, 32, 1)]), dict(layers=[(4, 2, 32, 2)])]
     for b in bad:
         assert K.kvq_cache_bytes(_cfg(**b)) == 0, b
 
@@ -90,3 +91,14 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.kvq_destroy(None) == 1
     assert lib.kvq_equivalent_bits(None) == 0.0
     assert lib.kvq_decode_bytes(None, 0) == -1
+
+
+def test_per_token_key_layout(lib):
+    # per-token keys: the record keeps one (scale, zero) pair per token for the keys
+    for kb in (2, 4, 8):
+        for vb in (2, 3, 4, 8):
+            cfg = _cfg(layers=[(kb, vb, 32, 1)], max_tokens=64)
+            assert K.kvq_cache_bytes(cfg) > 0
+            lay = O.record_layout(128, 32, kb, vb, O.KEY_PER_TOKEN)
+            lay0 = O.record_layout(128, 32, kb, vb)
+            assert lay["bytes"] == lay0["bytes"] - 4 * 128 + 4 * 32

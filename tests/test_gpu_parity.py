@@ -34,12 +34,12 @@ def _rand_kv(gen, B, H, n, d, t0, total, outlier_ch=(3, 17), device="cuda"):
     return k.half().contiguous(), v.half().contiguous()
 
 
-def _run_stream(kb, vb, D, G, R, gqa, schedule, B=2, Hkv=2, attn_every=1, seed=0):
+def _run_stream(kb, vb, D, G, R, gqa, schedule, B=2, Hkv=2, attn_every=1, seed=0, key_mode=0):
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     total = sum(schedule)
-    cache = K.KVQCache([(kb, vb, R)], B, Hkv * gqa, Hkv, D, G, total)
-    ora = O.OracleLayerCache(B, Hkv, D, G, kb, vb, R)
+    cache = K.KVQCache([(kb, vb, R, key_mode)], B, Hkv * gqa, Hkv, D, G, total)
+    ora = O.OracleLayerCache(B, Hkv, D, G, kb, vb, R, key_mode)
     pos = 0
     for step, n in enumerate(schedule):
         k, v = _rand_kv(gen, B, Hkv, n, D, pos, total)
@@ -68,6 +68,22 @@ def test_stream_bitexact_and_attention(kb, vb, D):
     # chunk whose flush straddles the window and the input
     sched = [150] + [1] * 40 + [45, 1, 1, 77]
     _run_stream(kb, vb, D, 32, 64, 4, sched, attn_every=5)
+
+
+@pytest.mark.parametrize("kb", [2, 4, 8])
+@pytest.mark.parametrize("vb", [2, 3, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_per_token_keys_bitexact_and_attention(kb, vb, D):
+    # KVTuner's per-token-asym key mode: same stream schedule, keys quantized per token
+    sched = [150] + [1] * 40 + [45, 1, 1, 77]
+    _run_stream(kb, vb, D, 32, 64, 4, sched, attn_every=5, seed=kb * 16 + vb, key_mode=K.KEY_PER_TOKEN)
+
+
+@pytest.mark.parametrize("gqa", [1, 5, 8])
+@pytest.mark.parametrize("G", [64, 128])
+def test_per_token_keys_gqa_and_group_sizes(gqa, G):
+    _run_stream(4, 2, 128, G, G, gqa, [3 * G + 5] + [1] * (G + 2), attn_every=9, seed=gqa + G,
+                key_mode=K.KEY_PER_TOKEN)
 
 
 @pytest.mark.parametrize("gqa", [1, 2, 3, 4, 5, 7, 8])
@@ -120,9 +136,10 @@ def test_capacity_and_argument_errors():
     cache.close()
 
 
-def test_decode_step_graph_matches_layer_calls():
-    w = W.scaled(W.workload(2), batch=2, num_layers=3, context=200, decode_steps=40,
-                 layers=((8, 4, 32), (4, 2, 32), (2, 2, 64)))
+@pytest.mark.parametrize("layers", [((8, 4, 32), (4, 2, 32), (2, 2, 64)),
+                                    ((8, 4, 32, 1), (4, 2, 32, 0), (4, 4, 64, 1))])
+def test_decode_step_graph_matches_layer_calls(layers):
+    w = W.scaled(W.workload(2), batch=2, num_layers=3, context=200, decode_steps=40, layers=layers)
     stream = torch.cuda.Stream()
     caches = []
     for _ in range(2):
@@ -193,11 +210,15 @@ def _layers_to_check(w):
     return out
 
 
-@pytest.mark.parametrize("idx", [2, 3, 4, 5])
-def test_workload_full_size_sampled(idx):
+@pytest.mark.parametrize("idx,key_mode", [(2, 0), (3, 0), (4, 0), (5, 0), (3, 1)])
+def test_workload_full_size_sampled(idx, key_mode):
     """Full-size shapes in the benchmark's launch configuration, one layer per
-    distinct precision pair; codes and attention checked on sampled units."""
+    distinct precision pair; codes and attention checked on sampled units.
+    (3, 1): the Qwen2.5-7B-shaped workload with every layer in the
+    per-token-asym key mode, the mode KVTuner pairs with that model.)"""
     w = W.workload(idx)
+    if key_mode:
+        w = W.scaled(w, layers=tuple((kb, vb, r, key_mode) for kb, vb, r in w.layers))
     layers = _layers_to_check(w)
     steps = min(w.decode_steps, 40)
     sub = [w.layers[l] for l in layers]
@@ -207,12 +228,13 @@ def test_workload_full_size_sampled(idx):
     units = sorted({0, U - 1, U // 2, (U * 7) // 11})
     rep = w.num_q_heads // w.num_kv_heads
     for li, l in enumerate(layers):
-        kb, vb, R = w.layers[l]
+        kb, vb, R = w.layers[l][:3]
+        km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
         k, v = W.gen_kv(w, l, 0, w.context, device="cuda")
         cache.append(li, k, v)
         oras = {}
         for u in units:
-            o = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R)
+            o = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km)
             o.append(*_unit_stream(k, v, u, w.num_kv_heads))
             oras[u] = o
         del k, v
