@@ -161,8 +161,9 @@ class OracleSampler:
         self.unit_w = W.scaled(w, batch=1, num_kv_heads=1, num_q_heads=w.num_q_heads // w.num_kv_heads)
         self.caches = {}
         for l in self.layers:
-            kb, vb, R = w.layers[l]
-            ora = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R)
+            kb, vb, R = w.layers[l][:3]
+            km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
+            ora = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km)
             k, v = W.gen_kv(self.unit_w, l, 0, w.context)
             ora.append(k.numpy(), v.numpy())
             self.caches[l] = ora
@@ -205,6 +206,17 @@ def oracle_sample(w, budget_s: float = 12.0):
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def _with_key_mode(w, args):
+    """The workload with every layer's keys in the requested mode (per token:
+    KVTuner's per-token-asym mode; 2, 4 or 8-bit keys only)."""
+    if args.key_mode == "channel":
+        return w
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    if any(l[0] == 3 for l in w.layers):
+        raise SystemExit("per-token keys need 2, 4 or 8-bit keys; this workload has 3-bit keys")
+    return W.scaled(w, name=w.name + "-per-token-keys", layers=tuple((kb, vb, r, 1) for kb, vb, r in w.layers))
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -219,7 +231,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K.load()
-    w = W.workload(args.workload)
+    w = _with_key_mode(W.workload(args.workload), args)
     if args.layers:  # profiling runs: the workload's first N layers
         w = W.scaled(w, num_layers=args.layers, layers=tuple(w.layers[:args.layers]))
     L, B, Hq, Hkv, D = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -447,7 +459,7 @@ def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return
-    w = W.workload(args.workload)
+    w = _with_key_mode(W.workload(args.workload), args)
     smp = OracleSampler(w)
     vals = []
     for s in range(args.warmup + args.steps):
@@ -479,6 +491,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="profiling runs: skip the end-to-end leg")
     ap.add_argument("--layers", type=int, default=0, help="profiling runs: only the workload's first N layers")
+    ap.add_argument("--key-mode", choices=["channel", "token"], default="channel",
+                    help="keys per channel over groups (KIVI) or per token (per-token-asym) on every layer")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
