@@ -112,15 +112,15 @@ def qwen_like_table(seed: int, n_layers: int = 28, residual: int = 64) -> Tuple[
 
 
 def kvmix_table(seed: int, n_layers: int = 32, n_high: int = 6, context: int = 4096,
-                group_size: int = 32) -> Tuple[LayerSpec, ...]:
-    """KVmix-style table: a seeded pick of high-precision layers (K4V3) and the
-    rest K2V2, with a per-layer FP16 residual of 20% / 10% of the prefill
-    context rounded down to whole key groups."""
+                group_size: int = 32, high_pair: Tuple[int, int] = (4, 3)) -> Tuple[LayerSpec, ...]:
+    """KVmix-style table: a seeded pick of high-precision layers (high_pair,
+    K4V3 by default) and the rest K2V2, with a per-layer FP16 residual of
+    20% / 10% of the prefill context rounded down to whole key groups."""
     rng = np.random.Generator(np.random.PCG64(seed))
     hi = set(int(x) for x in rng.choice(n_layers, n_high, replace=False))
     r_hi = group_size * int((0.2 * context) // group_size)
     r_lo = group_size * int((0.1 * context) // group_size)
-    return tuple((4, 3, r_hi) if l in hi else (2, 2, r_lo) for l in range(n_layers))
+    return tuple((*high_pair, r_hi) if l in hi else (2, 2, r_lo) for l in range(n_layers))
 
 
 def _make_workloads() -> List[Workload]:
@@ -134,14 +134,18 @@ def _make_workloads() -> List[Workload]:
                   kvmix_table(1004))
     w5 = Workload("llama2-70b-shaped-32k", 80, 8, 64, 8, 128, 32768, 128, 64, 4, 10.0, 1005,
                   _uniform_pairs(80, {0, 1, 77, 78, 79}, (8, 4), (4, 2), 128))
-    return [w1, w2, w3, w4, w5]
+    # the KVmix page's own orientation: its averages (keys 2.19, values 2.38
+    # bits) mean K3V4 on the high-precision layers, the mirror of w4's K4V3
+    w6 = Workload("llama2-7b-shaped-kvmix-mha-k3v4", 32, 30, 32, 32, 128, 4096, 32, 256, 4, 10.0, 1006,
+                  kvmix_table(1006, high_pair=(3, 4)))
+    return [w1, w2, w3, w4, w5, w6]
 
 
 WORKLOADS: List[Workload] = _make_workloads()
 
 
 def workload(index: int) -> Workload:
-    """Workloads are numbered 1..5 in the order they are listed above."""
+    """Workloads are numbered 1..6 in the order they are listed above."""
     return WORKLOADS[index - 1]
 
 

@@ -61,7 +61,7 @@ def test_cache_bytes_rejects_bad_configs(lib):
 
 def test_cache_bytes_covers_layout(lib):
     # the buffer holds at least the records for max_tokens and the windows
-    for idx in range(1, 6):
+    for idx in range(1, 7):
         w = W.workload(idx)
         cfg = K.make_config(w.layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.group_size,
                             w.total_tokens)

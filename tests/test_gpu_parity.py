@@ -210,12 +210,13 @@ def _layers_to_check(w):
     return out
 
 
-@pytest.mark.parametrize("idx,key_mode", [(2, 0), (3, 0), (4, 0), (5, 0), (3, 1)])
+@pytest.mark.parametrize("idx,key_mode", [(2, 0), (3, 0), (4, 0), (5, 0), (3, 1), (6, 0)])
 def test_workload_full_size_sampled(idx, key_mode):
     """Full-size shapes in the benchmark's launch configuration, one layer per
     distinct precision pair; codes and attention checked on sampled units.
     (3, 1): the Qwen2.5-7B-shaped workload with every layer in the
-    per-token-asym key mode, the mode KVTuner pairs with that model.)"""
+    per-token-asym key mode, the mode KVTuner pairs with that model;
+    6: the KVmix page's own K3V4 orientation.)"""
     w = W.workload(idx)
     if key_mode:
         w = W.scaled(w, layers=tuple((kb, vb, r, key_mode) for kb, vb, r in w.layers))

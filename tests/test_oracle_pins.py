@@ -73,6 +73,12 @@ def test_equivalent_bits_workloads():
     assert len(hi) == 6
     assert all(p[2] == 800 for p in w4.layers if p[:2] == (4, 3))
     assert all(p[2] == 384 for p in w4.layers if p[:2] == (2, 2))
+    # KVmix's own orientation (page: key 2.19 and value 2.38 average bits): K3V4 on 6 of 32 layers
+    w6 = W.workload(6)
+    kavg = sum(p[0] for p in w6.layers) / len(w6.layers)
+    vavg = sum(p[1] for p in w6.layers) / len(w6.layers)
+    assert (kavg, vavg) == (2.1875, 2.375) and (round(kavg, 2), round(vavg, 2)) == (2.19, 2.38)
+    assert sorted(set(p[:2] for p in w6.layers)) == [(2, 2), (3, 4)]
 
 
 # ---------------------------------------------------------------- quantizer
