@@ -456,3 +456,53 @@ def quantize_keys_per_token(k: np.ndarray, bits: int) -> np.ndarray:
     used only to compare error orderings."""
     codes, s, z = quantize_values_tokens(k, bits)
     return dequant_values(codes, s, z, bits)
+
+
+# --------------------------------------------------------------------------
+# Intra-layer Pareto pruning of precision pairs ([KVTuner] two-stage
+# search-space pruning, step 1: a layer's candidate KxVy pairs are cut to
+# those not dominated in (equivalent bits, e_o))
+# --------------------------------------------------------------------------
+
+def pair_output_errors(k: np.ndarray, v: np.ndarray, queries: Sequence[np.ndarray],
+                       pairs: Sequence[Tuple[int, int]], group: int, residual: int,
+                       key_mode: int = KEY_PER_CHANNEL) -> Dict[Tuple[int, int], float]:
+    """e_o of each pair on one layer's KV ([KVTuner] A3, quantization basics:
+    e_o = mean(|o - o_hat| / |o|)).
+
+    k, v: [B, Hkv, T, d] fp16; queries: [B, Hq, d] fp16 arrays.  o is fp64
+    attention over the fp16 K and V; o_hat over the pair's quantized cache
+    after appending all T tokens (window `residual`)."""
+    k = np.asarray(k, dtype=F16)
+    v = np.asarray(v, dtype=F16)
+    B, H, T, d = k.shape
+    out = {}
+    for kb, vb in pairs:
+        cache = OracleLayerCache(B, H, d, group, kb, vb, residual, key_mode)
+        cache.append(k, v)
+        o_all, oh_all = [], []
+        for q in queries:
+            q = np.asarray(q, dtype=F16)
+            rep = q.shape[1] // H
+            oh = cache.attend(q)
+            for b in range(B):
+                for h in range(q.shape[1]):
+                    u = h // rep
+                    o_all.append(attention_fp64(q[b, h].astype(np.float64), k[b, u].astype(np.float64),
+                                                v[b, u].astype(np.float64)))
+                    oh_all.append(oh[b, h])
+        out[(kb, vb)] = rel_error(np.stack(o_all), np.stack(oh_all))
+    return out
+
+
+def pareto_front(errors: Dict[Tuple[int, int], float]) -> List[Tuple[int, int]]:
+    """Pairs not dominated: no other pair has equivalent bits <= and e_o <=
+    with at least one strictly smaller."""
+    bits = {p: (p[0] + p[1]) / 2 for p in errors}
+    keep = []
+    for p in errors:
+        dominated = any(bits[q] <= bits[p] and errors[q] <= errors[p] and (bits[q] < bits[p] or errors[q] < errors[p])
+                        for q in errors if q != p)
+        if not dominated:
+            keep.append(p)
+    return sorted(keep, key=lambda p: (bits[p], errors[p]))

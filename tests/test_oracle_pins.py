@@ -475,3 +475,39 @@ def test_per_token_key_cache_streaming_matches_bulk():
     o = O.attention_fp64(q[0, 0].astype(np.float64), kh, vh)
     oe = O.attention_fp64(q[0, 0].astype(np.float64), k[0, 0].astype(np.float64), vh)
     assert np.abs(o - oe).max() < 0.05
+
+
+# ---------------------------------------------------------------------------
+# Intra-layer pair pruning ([KVTuner] two-stage search-space pruning, and
+# Table 3 of its A3 observations)
+# ---------------------------------------------------------------------------
+
+def _pruning_case():
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    w = W.scaled(W.workload(2), batch=1, num_kv_heads=2, num_q_heads=8, context=512, decode_steps=4)
+    k, v = W.gen_kv(w, 5, 0, w.context)
+    qs = [W.gen_q(w, 5, s).numpy() for s in range(2)]
+    return k.numpy(), v.numpy(), qs
+
+
+def test_pareto_front_keeps_kvtuners_pairs():
+    # On keys with channel outliers and values with drifting means, the e_o
+    # front over {2, 4, 8}^2 is the five pairs KVTuner's pruning keeps:
+    # KV2, K4V2, KV4, K8V4, KV8 (K2V4, K8V2, K2V8 and K4V8 are dominated).
+    k, v, qs = _pruning_case()
+    pairs = [(kb, vb) for kb in (2, 4, 8) for vb in (2, 4, 8)]
+    err = O.pair_output_errors(k, v, qs, pairs, 32, 32)
+    assert O.pareto_front(err) == [(2, 2), (4, 2), (4, 4), (8, 4), (8, 8)]
+    # Table 3's reading: at the same memory, precise keys beat precise values
+    assert err[(4, 2)] < err[(2, 4)] and err[(8, 4)] < err[(4, 8)]
+    # more bits on both sides never hurts here
+    assert err[(8, 8)] < err[(4, 4)] < err[(2, 2)]
+
+
+def test_pareto_front_filter():
+    err = {(8, 8): 0.001, (8, 4): 0.01, (4, 8): 0.02, (4, 4): 0.015, (4, 2): 0.05, (2, 4): 0.2, (2, 2): 0.3}
+    # K4V8 (6 bits, 0.02) is dominated by K8V4 (6 bits, 0.01); K2V4 by K4V2
+    assert O.pareto_front(err) == [(2, 2), (4, 2), (4, 4), (8, 4), (8, 8)]
+    # fewer bits at an equal error dominates; a tie in both coordinates does not
+    assert O.pareto_front({(4, 4): 0.1, (2, 8): 0.1}) == [(4, 4)]
+    assert sorted(O.pareto_front({(8, 2): 0.1, (2, 8): 0.1})) == [(2, 8), (8, 2)]
