@@ -1,6 +1,7 @@
 """Intra-layer pruning of precision pairs by attention-output error.
 
-KVTuner, "两阶段搜索空间剪枝算法" (two-stage search-space pruning), step 1:
+KVTuner, section A2, "两阶段搜索空间剪枝算法" (two-stage search-space
+pruning), step 1:
 each layer's candidate KxVy pairs are scored by their equivalent bits and by
 the relative attention-output error e_o = mean(|o - o_hat| / |o|) (defined
 in its "A3 背景知识与关键观察" section, KV-cache quantization basics).  Pairs

@@ -439,6 +439,34 @@ class OracleLayerCache:
         return out
 
 
+    def attend_chunk(self, q: np.ndarray, units: Sequence[int] = None) -> np.ndarray:
+        """Causal attention of the n newest tokens' queries over the cache.
+
+        q: [B, Hq, n, d] fp16, query i belonging to the token at position
+        T - n + i (T = tokens appended so far).  It attends the tokens at
+        positions 0 .. T - n + i of the cache as it stands: quantized groups
+        dequantized, window tokens exact ([KVTuner] A2, calibration design: prefill
+        attention over the dequantized cache; [KVTuner] A3 attention).
+        Returns [B, Hq, n, d] fp64 (rows of units not listed stay NaN)."""
+        q = np.asarray(q, dtype=F16)
+        B, Hq, n, d = q.shape
+        if not 1 <= n <= self.total:
+            raise ValueError("chunk must hold between 1 and the appended tokens")
+        rep = Hq // self.H
+        out = np.full((B, Hq, n, d), np.nan)
+        if units is None:
+            units = range(self.B * self.H)
+        for u in units:
+            b, h = divmod(u, self.H)
+            kh, vh = self.dequantized(u)
+            for j in range(rep):
+                for i in range(n):
+                    last = self.total - n + i
+                    out[b, h * rep + j, i] = attention_fp64(q[b, h * rep + j, i].astype(np.float64),
+                                                            kh[: last + 1], vh[: last + 1])
+        return out
+
+
 # --------------------------------------------------------------------------
 # Relative error metrics ([KVTuner] A3)
 # --------------------------------------------------------------------------
@@ -459,7 +487,7 @@ def quantize_keys_per_token(k: np.ndarray, bits: int) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# Intra-layer Pareto pruning of precision pairs ([KVTuner] two-stage
+# Intra-layer Pareto pruning of precision pairs ([KVTuner] A2, two-stage
 # search-space pruning, step 1: a layer's candidate KxVy pairs are cut to
 # those not dominated in (equivalent bits, e_o))
 # --------------------------------------------------------------------------

@@ -1,4 +1,4 @@
-"""Intra-layer pair pruning on the GPU (KVTuner, two-stage search-space
+"""Intra-layer pair pruning on the GPU (KVTuner A2, two-stage search-space
 pruning, step 1): e_o per pair from the library's kernels against the
 oracle's fp64 e_o, and the resulting Pareto front."""
 

@@ -478,7 +478,7 @@ def test_per_token_key_cache_streaming_matches_bulk():
 
 
 # ---------------------------------------------------------------------------
-# Intra-layer pair pruning ([KVTuner] two-stage search-space pruning, and
+# Intra-layer pair pruning ([KVTuner] A2, two-stage search-space pruning, and
 # Table 3 of its A3 observations)
 # ---------------------------------------------------------------------------
 
@@ -511,3 +511,80 @@ def test_pareto_front_filter():
     # fewer bits at an equal error dominates; a tie in both coordinates does not
     assert O.pareto_front({(4, 4): 0.1, (2, 8): 0.1}) == [(4, 4)]
     assert sorted(O.pareto_front({(8, 2): 0.1, (2, 8): 0.1})) == [(2, 8), (8, 2)]
+
+
+# ---------------------------------------------------------------------------
+# Chunk attention: causal queries over the cache ([KVTuner] A2 calibration,
+# prefill over the dequantized cache; A3 attention)
+# ---------------------------------------------------------------------------
+
+def _sdpa_bottom_right(q, k, v):
+    """torch's attention routine (fp64, CPU) with an explicit mask: query i of
+    n sees keys 0 .. T - n + i.  q [Hq, n, d], k/v [Hq, T, d]."""
+    import torch
+    n, T = q.shape[1], k.shape[1]
+    mask = torch.ones(n, T, dtype=torch.bool).tril(diagonal=T - n)
+    return torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), attn_mask=mask).numpy()
+
+
+@pytest.mark.parametrize("kb,vb,km,T,n", [(4, 2, 0, 160, 160), (3, 3, 0, 150, 37), (8, 4, 1, 129, 64),
+                                          (2, 8, 0, 96, 1)])
+def test_chunk_attention_matches_library_routine(kb, vb, km, T, n):
+    rng = np.random.default_rng(11)
+    B, H, rep, d, G = 1, 2, 3, 64, 32
+    k = (rng.standard_normal((B, H, T, d)) * (1 + 4 * (np.arange(d) % 9 == 0))).astype(np.float16)
+    v = rng.standard_normal((B, H, T, d)).astype(np.float16)
+    q = rng.standard_normal((B, H * rep, n, d)).astype(np.float16)
+    c = O.OracleLayerCache(B, H, d, G, kb, vb, G, km)
+    c.append(k[:, :, : T // 2], v[:, :, : T // 2])
+    c.append(k[:, :, T // 2:], v[:, :, T // 2:])
+    assert c.n_q > 0
+    got = c.attend_chunk(q)
+    for h in range(H):
+        kh, vh = c.dequantized(h)
+        exp = _sdpa_bottom_right(q[0, h * rep:(h + 1) * rep].astype(np.float64),
+                                 np.broadcast_to(kh, (rep,) + kh.shape).copy(),
+                                 np.broadcast_to(vh, (rep,) + vh.shape).copy())
+        np.testing.assert_allclose(got[0, h * rep:(h + 1) * rep], exp, rtol=1e-12, atol=1e-12)
+
+
+def test_chunk_attention_full_causal_prefill_without_quantization():
+    # window longer than the prompt: nothing is quantized and n = T is the
+    # plain causal prefill attention over the fp16 K and V
+    import torch
+    rng = np.random.default_rng(12)
+    T, d = 70, 64
+    k = rng.standard_normal((1, 1, T, d)).astype(np.float16)
+    v = rng.standard_normal((1, 1, T, d)).astype(np.float16)
+    q = rng.standard_normal((1, 2, T, d)).astype(np.float16)
+    c = O.OracleLayerCache(1, 1, d, 32, 2, 2, 96)
+    c.append(k, v)
+    assert c.n_q == 0
+    got = c.attend_chunk(q)
+    exp = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q.astype(np.float64)), torch.from_numpy(np.repeat(k, 2, 1).astype(np.float64)),
+        torch.from_numpy(np.repeat(v, 2, 1).astype(np.float64)), is_causal=True).numpy()
+    np.testing.assert_allclose(got, exp, rtol=1e-12, atol=1e-12)
+
+
+def test_chunk_attention_equal_keys_give_running_means():
+    # all keys equal: every visible token has the same weight, so query i
+    # returns the mean of the values at positions 0 .. T - n + i
+    rng = np.random.default_rng(13)
+    T, n, d = 200, 50, 64
+    k = np.broadcast_to(rng.standard_normal(d).astype(np.float16), (1, 1, T, d)).copy()
+    v = rng.standard_normal((1, 1, T, d)).astype(np.float16)
+    q = rng.standard_normal((1, 1, n, d)).astype(np.float16)
+    c = O.OracleLayerCache(1, 1, d, 32, 8, 8, 256)
+    c.append(k, v)
+    got = c.attend_chunk(q)[0, 0]
+    run = np.cumsum(v[0, 0].astype(np.float64), axis=0) / np.arange(1, T + 1)[:, None]
+    np.testing.assert_allclose(got, run[T - n:], rtol=1e-9, atol=1e-12)
+
+
+def test_chunk_attention_rejects_bad_lengths():
+    c = O.OracleLayerCache(1, 1, 64, 32, 4, 4, 32)
+    c.append(np.zeros((1, 1, 5, 64), np.float16), np.zeros((1, 1, 5, 64), np.float16))
+    with pytest.raises(ValueError):
+        c.attend_chunk(np.zeros((1, 1, 6, 64), np.float16))
