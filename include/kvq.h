@@ -160,6 +160,22 @@ kvq_status kvq_append(kvq_handle* h, int layer, const void* K, const void* V, in
  * Scores are scaled by 1/sqrt(head_dim).  KVQ_ERR_STATE if the layer is empty. */
 kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, void* stream);
 
+/* Causal attention of the queries of the n_queries newest tokens over `layer`
+ * as it stands: prefill or chunked-prefill attention over the quantized cache
+ * (KVTuner, section A2, calibration design: prefill runs over the dequantized
+ * cache; the attention is its A3 equation).  Call after appending the chunk.
+ * With T tokens appended, query i (0 <= i < n_queries) belongs to the token at
+ * position T - n_queries + i and attends the tokens at positions
+ * 0 .. T - n_queries + i: quantized groups dequantized (code * s + z), window
+ * tokens as stored.  Scores are scaled by 1/sqrt(head_dim).
+ * q: device fp16 [batch][num_q_heads][n_queries][head_dim], 16-byte aligned;
+ *    query head j reads kv head j / (num_q_heads / num_kv_heads).
+ * out: device fp32 [batch][num_q_heads][n_queries][head_dim], written entirely.
+ * KVQ_ERR_ARG if n_queries < 1 or > tokens appended; KVQ_ERR_STATE if the layer
+ * is empty; KVQ_ERR_UNSUPPORTED if num_q_heads / num_kv_heads > 128 or
+ * batch * num_kv_heads > 65535.  Runs on the tensor cores (tcgen05). */
+kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries, float* out, void* stream);
+
 /* One decode step over every layer: for l = 0 .. num_layers-1,
  * kvq_append(l, K[l], V[l], 1) then kvq_decode_attn(l, q[l], out[l]).
  * K, V, q, out are host arrays of num_layers device pointers, with the shapes

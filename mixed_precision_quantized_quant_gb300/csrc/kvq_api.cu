@@ -227,6 +227,41 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   return KVQ_OK;
 }
 
+kvq_status launch_chunk(kvq_handle* h, int layer, const void* q, int n, float* out, cudaStream_t s) {
+  const Plan& P = h->plan;
+  const LayerPlan& lp = P.layers[layer];
+  kvq::ChunkParams cp;
+  cp.q = static_cast<const __half*>(q);
+  cp.out = out;
+  cp.records = h->base + lp.off_records;
+  cp.unit_rec_stride = lp.unit_rec_stride;
+  cp.res_k = reinterpret_cast<const __half*>(h->base + lp.off_res_k);
+  cp.res_v = reinterpret_cast<const __half*>(h->base + lp.off_res_v);
+  cp.res_stride = lp.res_stride_elems;
+  cp.err = errw(h);
+  cp.n = n;
+  cp.T = static_cast<int>(h->tokens[layer]);
+  cp.n_q = static_cast<int>(kvq::quantized_after(h->tokens[layer], lp.R, P.G));
+  cp.Hq = P.Hq;
+  cp.kv_heads = P.Hkv;
+  cp.gqa = P.gqa;
+  cp.qpb = kvq::chunk_queries_per_cta(P.gqa);
+  cp.G = P.G;
+  cp.R = lp.R;
+  cp.gshift = P.G == 32 ? 5 : P.G == 64 ? 6 : 7;
+  cp.kb = lp.kb;
+  cp.vb = lp.vb;
+  cp.km = lp.km;
+  cp.wk = lp.wk;
+  cp.wv = lp.wv;
+  cp.rec_bytes = static_cast<int>(lp.rec_bytes);
+  cp.off_kscale = static_cast<int>(4LL * P.G * (lp.wk + lp.wv));
+  cp.off_vsz = cp.off_kscale + static_cast<int>(lp.km ? 4LL * P.G : 4LL * P.D);
+  cp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
+  if (kvq::chunk_attn_launch(lp.kb, lp.vb, P.D, cp, P.units, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -297,6 +332,16 @@ kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, 
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
   if (h->tokens[layer] <= 0) return KVQ_ERR_STATE;
   return launch_decode(h, layer, q, out, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries, float* out, void* stream) {
+  if (!h || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
+  if (!q || !out) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
+  if (h->tokens[layer] <= 0) return KVQ_ERR_STATE;
+  if (n_queries < 1 || n_queries > h->tokens[layer]) return KVQ_ERR_ARG;
+  if (kvq::chunk_queries_per_cta(h->plan.gqa) < 1 || h->plan.units > 65535) return KVQ_ERR_UNSUPPORTED;
+  return launch_chunk(h, layer, q, n_queries, out, static_cast<cudaStream_t>(stream));
 }
 
 kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V, const void* const* q,

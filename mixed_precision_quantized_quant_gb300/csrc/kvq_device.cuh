@@ -77,6 +77,30 @@ struct DecodeParams {
   float alpha;            // log2(e) / sqrt(D)
 };
 
+struct ChunkParams {
+  const __half* q;        // [B][Hq][n][D]: queries of the n newest tokens
+  float* out;             // [B][Hq][n][D]
+  const uint8_t* records;
+  int64_t unit_rec_stride;
+  const __half* res_k;
+  const __half* res_v;
+  int64_t res_stride;     // elements
+  int32_t* err;
+  int n;                  // queries per (batch, head)
+  int T;                  // tokens appended so far
+  int n_q;                // tokens held as quantized groups
+  int Hq, kv_heads, gqa;
+  int qpb;                // queries per CTA: 128 / gqa
+  int G, R;
+  int gshift;             // log2(G)
+  int kb, vb, km;
+  int wk, wv;             // u32 words per key / value code row
+  int rec_bytes;
+  int off_kscale;         // record offset of the key (scale, zero) part
+  int off_vsz;            // record offset of the value (scale, zero) pairs
+  float alpha;            // log2(e) / sqrt(D)
+};
+
 // ---------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -23,7 +23,7 @@ STATUS = {
 EXPORTS = (
     "kvq_cache_bytes", "kvq_create", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
     "kvq_layer_view_get", "kvq_equivalent_bits", "kvq_decode_bytes", "kvq_device_error",
-    "kvq_destroy", "kvq_status_string", "kvq_decode_attn_noalloc",
+    "kvq_destroy", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_chunk_attn",
 )
 
 
@@ -81,6 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.kvq_decode_attn.restype = ctypes.c_int
     L.kvq_decode_attn_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, vp]
     L.kvq_decode_attn_noalloc.restype = ctypes.c_int
+    L.kvq_chunk_attn.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp]
+    L.kvq_chunk_attn.restype = ctypes.c_int
     L.kvq_decode_step.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                   ctypes.POINTER(vp), vp]
     L.kvq_decode_step.restype = ctypes.c_int
@@ -143,6 +145,10 @@ def kvq_decode_attn_noalloc(h: int, layer: int, q: int, out: int, stream: int) -
     """kvq_decode_attn with the library's static device scratch: for callers
     that may not allocate device memory (see include/kvq.h)."""
     _check(load().kvq_decode_attn_noalloc(h, layer, q, out, stream), "kvq_decode_attn_noalloc")
+
+
+def kvq_chunk_attn(h: int, layer: int, q: int, n_queries: int, out: int, stream: int) -> None:
+    _check(load().kvq_chunk_attn(h, layer, q, n_queries, out, stream), "kvq_chunk_attn")
 
 
 def kvq_decode_step(h: int, K: Sequence[int], V: Sequence[int], q: Sequence[int], out: Sequence[int],
@@ -232,6 +238,18 @@ class KVQCache:
             out = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=q.device)
         kvq_decode_attn(self.h, layer, _dev_ptr(q, "q", torch.float16, (self.B, self.Hq, self.D)),
                         _dev_ptr(out, "out", torch.float32, (self.B, self.Hq, self.D)), _stream_ptr(stream))
+        return out
+
+    def chunk_attn(self, layer: int, q, out=None, stream=None):
+        """Causal attention of the queries of the newest q.shape[2] tokens:
+        q fp16 [B, Hq, n, d] -> fp32 [B, Hq, n, d]."""
+        import torch
+        n = int(q.shape[2])
+        shp = (self.B, self.Hq, n, self.D)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.float32, device=q.device)
+        kvq_chunk_attn(self.h, layer, _dev_ptr(q, "q", torch.float16, shp), n,
+                       _dev_ptr(out, "out", torch.float32, shp), _stream_ptr(stream))
         return out
 
     def decode_step(self, K: List, V: List, q: List, out: List, stream=None) -> None:
