@@ -115,7 +115,7 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
 __device__ __forceinline__ float code_f32(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
 
 template <int KB, int VB, int D>
-__global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p) {
+__global__ void __launch_bounds__(kChunkThreads, 2) chunk_attn_kernel(ChunkParams p) {
   using L = ChunkSmem<D>;
   constexpr int KC = L::KC;
   constexpr int kTile = kChunkTile;
@@ -141,9 +141,10 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
   const __half* rv = p.res_v + static_cast<int64_t>(u) * p.res_stride;
 
   // ---- query rows -> shared memory (row r = query r / gqa, head r % gqa)
+  // (8 consecutive threads fill one 128-byte core matrix: conflict-free stores)
 #pragma unroll 1
   for (int idx = tid; idx < kChunkRows * KC; idx += kChunkThreads) {
-    const int r = idx / KC, kc = idx - r * KC;
+    const int r = (idx & 7) + 8 * (idx / (8 * KC)), kc = (idx >> 3) & (KC - 1);
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows) {
       const int i = i0 + r / p.gqa, hh = r % p.gqa;
@@ -197,6 +198,52 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
   const int ntiles = ntq + ntw;
   bool failed = false;
 
+  // ---- words of one quantized tile, loaded a tile ahead of their use
+  struct {
+    uint32_t kw0[kJ], kw1[kJ], vw0[kJ], vw1[kJ];
+    __half2 ksz[kJ];
+    uint4 sa, za, sb, zb;  // per-channel key scales and zeros of groups gA, gB
+    __half2 tsz;           // value (scale, zero) of token t0 + tid (tid < 64)
+    int gA;
+  } pf;
+  auto prefetch = [&](int t0) {
+    const int tq_end = min(t0 + kTile, p.n_q);  // whole groups: the rows exist
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int t = t0 + row0 + kStep * j;
+      pf.kw0[j] = pf.kw1[j] = pf.vw0[j] = pf.vw1[j] = 0u;
+      pf.ksz[j] = __floats2half2_rn(0.0f, 0.0f);
+      if (t < tq_end) {
+        const int gi = t >> gs, rr = t - (gi << gs);
+        const uint8_t* rec = urec + static_cast<int64_t>(gi) * p.rec_bytes;
+        const uint32_t* krow = reinterpret_cast<const uint32_t*>(rec) + rr * p.wk;
+        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec) + voff + rr * p.wv;
+        pf.kw0[j] = krow[ku.wa];
+        if (ku.second_word()) pf.kw1[j] = krow[ku.wa + 1];
+        pf.vw0[j] = vrow[vu.wa];
+        if (vu.second_word()) pf.vw1[j] = vrow[vu.wa + 1];
+        if (p.km) pf.ksz[j] = *reinterpret_cast<const __half2*>(rec + p.off_kscale + rr * 4);
+      }
+    }
+    // groups of the thread's first and last token, both below n_q / G
+    pf.gA = min(t0 + row0, tq_end - 1) >> gs;
+    const int gB = min(t0 + row0 + kStep * (kJ - 1), tq_end - 1) >> gs;
+    if (p.km == 0) {
+      const uint8_t* recA = urec + static_cast<int64_t>(pf.gA) * p.rec_bytes + p.off_kscale;
+      const uint8_t* recB = urec + static_cast<int64_t>(gB) * p.rec_bytes + p.off_kscale;
+      pf.sa = *reinterpret_cast<const uint4*>(recA + c0 * 2);
+      pf.za = *reinterpret_cast<const uint4*>(recA + D * 2 + c0 * 2);
+      pf.sb = *reinterpret_cast<const uint4*>(recB + c0 * 2);
+      pf.zb = *reinterpret_cast<const uint4*>(recB + D * 2 + c0 * 2);
+    }
+    pf.tsz = __floats2half2_rn(0.0f, 0.0f);
+    if (tid < kTile && t0 + tid < tq_end) {
+      const int t = t0 + tid, gi = t >> gs, rr = t - (gi << gs);
+      pf.tsz = *reinterpret_cast<const __half2*>(urec + static_cast<int64_t>(gi) * p.rec_bytes + p.off_vsz + rr * 4);
+    }
+  };
+  if (ntq > 0) prefetch(0);
+
 #pragma unroll 1
   for (int it = 0; it < ntiles; ++it) {
     const bool quant = it < ntq;
@@ -205,45 +252,16 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
     // the previous P.V product has read its operands (and written O)
     if (it > 0 && !failed) failed = !mbar_wait(barO, (it - 1) & 1, p.err);
 
-    // ---- keys (hi + lo halves) and values of the tile into shared memory;
-    // all global loads of the tile are issued before any is used
+    // ---- keys (hi + lo halves) and values of the tile into shared memory,
+    // from the words prefetched during the previous tile
     if (quant) {
-      const int tq_end = min(t0 + kTile, p.n_q);  // whole groups: the rows exist
-      uint32_t kw0[kJ], kw1[kJ], vw0[kJ], vw1[kJ];
-      __half2 ksz[kJ];
-#pragma unroll
-      for (int j = 0; j < kJ; ++j) {
-        const int t = t0 + row0 + kStep * j;
-        kw0[j] = kw1[j] = vw0[j] = vw1[j] = 0u;
-        ksz[j] = __floats2half2_rn(0.0f, 0.0f);
-        if (t < tq_end) {
-          const int gi = t >> gs, rr = t - (gi << gs);
-          const uint8_t* rec = urec + static_cast<int64_t>(gi) * p.rec_bytes;
-          const uint32_t* krow = reinterpret_cast<const uint32_t*>(rec) + rr * p.wk;
-          const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec) + voff + rr * p.wv;
-          kw0[j] = krow[ku.wa];
-          if (ku.second_word()) kw1[j] = krow[ku.wa + 1];
-          vw0[j] = vrow[vu.wa];
-          if (vu.second_word()) vw1[j] = vrow[vu.wa + 1];
-          if (p.km) ksz[j] = *reinterpret_cast<const __half2*>(rec + p.off_kscale + rr * 4);
-        }
-      }
-      // per-channel key (scale, zero) of the (at most two) groups of the
-      // thread's tokens, both below n_q / G
+      const int tq_end = min(t0 + kTile, p.n_q);
       float sA[8], zA[8], sB[8], zB[8];
-      const int gA = min(t0 + row0, tq_end - 1) >> gs;
-      const int gB = min(t0 + row0 + kStep * (kJ - 1), tq_end - 1) >> gs;
       if (p.km == 0) {
-        const uint8_t* recA = urec + static_cast<int64_t>(gA) * p.rec_bytes + p.off_kscale;
-        const uint8_t* recB = urec + static_cast<int64_t>(gB) * p.rec_bytes + p.off_kscale;
-        const uint4 sa = *reinterpret_cast<const uint4*>(recA + c0 * 2);
-        const uint4 za = *reinterpret_cast<const uint4*>(recA + D * 2 + c0 * 2);
-        const uint4 sb = *reinterpret_cast<const uint4*>(recB + c0 * 2);
-        const uint4 zb = *reinterpret_cast<const uint4*>(recB + D * 2 + c0 * 2);
-        const __half* psa = reinterpret_cast<const __half*>(&sa);
-        const __half* pza = reinterpret_cast<const __half*>(&za);
-        const __half* psb = reinterpret_cast<const __half*>(&sb);
-        const __half* pzb = reinterpret_cast<const __half*>(&zb);
+        const __half* psa = reinterpret_cast<const __half*>(&pf.sa);
+        const __half* pza = reinterpret_cast<const __half*>(&pf.za);
+        const __half* psb = reinterpret_cast<const __half*>(&pf.sb);
+        const __half* pzb = reinterpret_cast<const __half*>(&pf.zb);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           sA[e] = __half2float(psa[e]);
@@ -262,9 +280,9 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
       for (int j = 0; j < kJ; ++j) {
         const int nn = row0 + kStep * j;
         const int t = t0 + nn;
-        const bool inB = (t >> gs) != gA;
-        const uint32_t k0 = KB == 2 ? (kw0[j] >> ku.sh0) : kw0[j];
-        const uint32_t v0 = VB == 2 ? (vw0[j] >> vu.sh0) : vw0[j];
+        const bool inB = (t >> gs) != pf.gA;
+        const uint32_t k0 = KB == 2 ? (pf.kw0[j] >> ku.sh0) : pf.kw0[j];
+        const uint32_t v0 = VB == 2 ? (pf.vw0[j] >> vu.sh0) : pf.vw0[j];
         uint32_t hw[4], lw[4], vh[4];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
@@ -276,18 +294,18 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
               s = inB ? sB[e + q2] : sA[e + q2];
               z = inB ? zB[e + q2] : zA[e + q2];
             } else {
-              const float2 sz = __half22float2(ksz[j]);
+              const float2 sz = __half22float2(pf.ksz[j]);
               s = sz.x;
               z = sz.y;
               if constexpr (KB == 3) {
                 if ((ku.two >> (e + q2)) & 1u) s = __fdiv_rn(__fmul_rn(s, 7.0f), 3.0f);
               }
             }
-            kv[q2] = fmaf(code_f32(ku.get(k0, kw1[j], e + q2)), s, z);
+            kv[q2] = fmaf(code_f32(ku.get(k0, pf.kw1[j], e + q2)), s, z);
           }
           split_hi_lo(kv[0], kv[1], hw[e / 2], lw[e / 2]);
           // value codes (< 1024) as exact fp16 integers: (1024 + code) - 1024
-          uint32_t c_lo = vu.get(v0, vw1[j], e), c_hi = vu.get(v0, vw1[j], e + 1);
+          uint32_t c_lo = vu.get(v0, pf.vw1[j], e), c_hi = vu.get(v0, pf.vw1[j], e + 1);
           if constexpr (VB == 3) {
             if ((vu.two >> e) & 1u) c_lo *= 7u;
             if ((vu.two >> (e + 1)) & 1u) c_hi *= 7u;
@@ -301,6 +319,11 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
         *reinterpret_cast<uint4*>(sm + L::kh + off) = live ? make_uint4(hw[0], hw[1], hw[2], hw[3]) : zero;
         *reinterpret_cast<uint4*>(sm + L::kl + off) = live ? make_uint4(lw[0], lw[1], lw[2], lw[3]) : zero;
         *reinterpret_cast<uint4*>(sm + L::v + off) = live ? make_uint4(vh[0], vh[1], vh[2], vh[3]) : zero;
+      }
+      if (tid < kTile) {
+        const bool vis = t0 + tid < tend;
+        tok_s[tid] = vis ? __low2float(pf.tsz) : 0.0f;
+        tok_z[tid] = vis ? __high2float(pf.tsz) : 0.0f;
       }
     } else {
       const int tw_end = min(t0 + kTile, p.T);
@@ -324,23 +347,12 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
         *reinterpret_cast<uint4*>(sm + L::v + off) = vr[j];
       }
     }
-    if (tid < kTile) {
-      const int t = t0 + tid;
-      float s = 0.0f, z = 0.0f;
-      if (t < tend) {
-        if (quant) {
-          const int gi = t >> gs, rr = t - (gi << gs);
-          const __half2 sz =
-              *reinterpret_cast<const __half2*>(urec + static_cast<int64_t>(gi) * p.rec_bytes + p.off_vsz + rr * 4);
-          s = __low2float(sz);
-          z = __high2float(sz);
-        } else {
-          s = 1.0f;
-        }
-      }
-      tok_s[tid] = s;
-      tok_z[tid] = z;
+    if (!quant && tid < kTile) {
+      tok_s[tid] = t0 + tid < tend ? 1.0f : 0.0f;
+      tok_z[tid] = 0.0f;
     }
+    // prefetch the next quantized tile's words; they land during this tile's MMAs and softmax
+    if (it + 1 < ntq) prefetch((it + 1) * kTile);
     fence_proxy_async_smem();
     tc_fence_before_sync();
     failed = __syncthreads_or(failed);
@@ -367,7 +379,7 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
       tmem_ld16(tS + c, rr);
       tmem_ld_wait(rr);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) x[c + j] = __uint_as_float(rr[j]) * p.alpha;
+      for (int j = 0; j < 16; ++j) x[c + j] = __uint_as_float(rr[j]);
     }
     // tokens t0 .. t0 + nvis - 1 are visible to this row
     const int nvis = min(tend, lim + 1) - t0;
@@ -382,12 +394,15 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
         mx = fmaxf(mx, x[j]);
       }
     }
+    // scores are raw q.k; the log2-domain max is m, in units of alpha * q.k
+    mx *= p.alpha;
     const bool need = mx > m + 8.0f;
     float f = 1.0f;
     if (need) {
       f = ex2(m - mx);
       m = mx;
     }
+    const float nm = -m;
     l *= f;
     zs *= f;
     // O *= f where the max moved; 3-bit values: divide the 2-bit-field
@@ -413,7 +428,7 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_attn_kernel(ChunkParams p
     uint32_t hi[kTile / 2], lo[kTile / 2];
 #pragma unroll
     for (int j = 0; j < kTile; j += 2) {
-      const float p0 = ex2(x[j] - m), p1 = ex2(x[j + 1] - m);
+      const float p0 = ex2(fmaf(x[j], p.alpha, nm)), p1 = ex2(fmaf(x[j + 1], p.alpha, nm));
       const float2 s2 = *reinterpret_cast<const float2*>(tok_s + j);
       const float2 z2 = *reinterpret_cast<const float2*>(tok_z + j);
       ls += p0 + p1;
