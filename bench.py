@@ -451,6 +451,209 @@ def _ncu_traffic(workload_name):
 
 
 # ----------------------------------------------------------------------------
+# chunk attention (causal prefill over the quantized cache)
+# ----------------------------------------------------------------------------
+
+CHUNK_METRIC = "causal chunk attention over the quantized cache, TFLOP/s (4 d per visible (query, key) pair)"
+
+
+def _chunk_flops(B, Hq, D, T, n):
+    """Algorithmic FLOPs of one layer: 2 d for q.k and 2 d for p.v per visible pair."""
+    visible = n * (T - n) + n * (n + 1) // 2
+    return 4.0 * D * visible * Hq * B
+
+
+def _chunk_workload(args):
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    w = _with_key_mode(W.workload(args.workload), args)
+    w = W.scaled(w, batch=args.chunk_batch)
+    if args.layers:
+        w = W.scaled(w, num_layers=args.layers, layers=tuple(w.layers[:args.layers]))
+    n = args.chunk or w.context
+    return w, n
+
+
+class ChunkOracleSampler:
+    """Times the oracle's chunk attention (fp64 over the dequantized cache) for
+    the last `rows` queries of the chunk on one (batch, kv head) unit of each
+    distinct precision pair, and scales by visible pairs to the whole step."""
+
+    def __init__(self, w, n, rows=8):
+        import numpy as np
+        from mixed_precision_quantized_quant_gb300 import workloads as W
+        from oracle import kvq_oracle as O
+        self.w, self.n, self.rows = w, n, rows
+        T, D, rep = w.context, w.head_dim, w.num_q_heads // w.num_kv_heads
+        seen, self.layers = set(), []
+        for l, p in enumerate(w.layers):
+            if p not in seen:
+                seen.add(p)
+                self.layers.append(l)
+        uw = W.scaled(w, batch=1, num_kv_heads=1, num_q_heads=rep)
+        self.caches, self.q = {}, {}
+        rng = np.random.default_rng(7)
+        for l in self.layers:
+            kb, vb, R = w.layers[l][:3]
+            km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
+            ora = O.OracleLayerCache(1, 1, D, w.group_size, kb, vb, R, km)
+            k, v = W.gen_kv(uw, l, 0, T)
+            ora.append(k.numpy(), v.numpy())
+            self.caches[l] = ora
+            self.q[l] = rng.standard_normal((1, rep, rows, D)).astype(np.float16)
+        self.count = {l: sum(1 for p in w.layers if p == w.layers[l]) for l in self.layers}
+        # the sample's queries are the last `rows` positions: each sees about T keys
+        self.sample_flops = {l: 4.0 * D * rep * sum(T - rows + i + 1 for i in range(rows)) for l in self.layers}
+        self.step_flops = w.num_layers * _chunk_flops(w.batch, w.num_q_heads, D, T, n)
+        self.desc = (f"oracle chunk attention (fp64 over the dequantized cache) for the last {rows} queries x "
+                     f"{rep} heads of 1 (batch, kv head) unit on layers {self.layers} (one per distinct "
+                     f"precision pair) at context {T}; time per visible pair scaled to the step's "
+                     f"{self.step_flops / 4 / D:.3g} pairs")
+
+    def step(self) -> float:
+        """Seconds one full chunk step would take (all layers, all units)."""
+        secs, flops = 0.0, 0.0
+        for l in self.layers:
+            c = self.caches[l]
+            t0 = time.perf_counter()
+            c.attend_chunk(self.q[l])  # the queries of the newest `rows` tokens
+            secs += (time.perf_counter() - t0) * self.count[l]
+            flops += self.sample_flops[l] * self.count[l]
+        return secs * self.step_flops / flops
+
+
+def chunk_oracle_sample(w, n, budget_s):
+    smp = ChunkOracleSampler(w, n)
+    t_start = time.perf_counter()
+    steps = []
+    while len(steps) < 2 or (time.perf_counter() - t_start < budget_s and len(steps) < 16):
+        steps.append(smp.step())
+    step_s = statistics.median(steps)
+    return smp.step_flops / step_s / 1e12, step_s, smp.desc + f"; median over {len(steps)} samples"
+
+
+def _tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_chunk(args):
+    import torch
+
+    from mixed_precision_quantized_quant_gb300 import kvq as K
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K.load()
+    w, n = _chunk_workload(args)
+    L, B, Hq, Hkv, D, T = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.context
+    stream = torch.cuda.Stream(device=dev)
+    cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, T, device=dev)
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            k, v = W.gen_kv(w, l, 0, T, device=dev)
+            cache.append(l, k, v, stream=stream)
+            del k, v
+        stream.synchronize()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    q = torch.randn((B, Hq, n, D), generator=gen, device=dev).half()
+    out = torch.empty((B, Hq, n, D), dtype=torch.float32, device=dev)
+    flops_layer = _chunk_flops(B, Hq, D, T, n)
+
+    def run_step():
+        for l in range(L):
+            cache.chunk_attn(l, q, out, stream=stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run_step()
+        stream.synchronize()
+        _barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            run_step()
+        ev1.record(stream)
+        stream.synchronize()
+        sampler.mark(t0, time.time())
+        torch.cuda.synchronize()
+        _barrier(world)
+    ms_total = _max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = ms_total / args.steps
+    tflops = world * L * flops_layer * args.steps / (ms_total / 1e3) / 1e12
+    clocks = sampler.stop()
+
+    # end to end: each layer's queries copied from pinned host memory, outputs read back
+    e2e = None
+    if not args.no_e2e:
+        h_q = q.cpu().pin_memory()
+        h_out = torch.empty((B, Hq, n, D), dtype=torch.float32).pin_memory()
+        q_dev = torch.empty_like(q)
+        with torch.cuda.stream(stream):
+            def e2e_step():
+                for l in range(L):
+                    q_dev.copy_(h_q, non_blocking=True)
+                    cache.chunk_attn(l, q_dev, out, stream=stream)
+                    h_out.copy_(out, non_blocking=True)
+                stream.synchronize()
+            for _ in range(min(args.warmup, 3)):
+                e2e_step()
+            _barrier(world)
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                e2e_step()
+            t1 = time.perf_counter()
+            _barrier(world)
+        e2e_s = _max_over_ranks(t1 - t0, world)
+        e2e = {"value": round(world * L * flops_layer * args.steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": L * q.numel() * 2, "d2h_bytes_per_step": L * out.numel() * 4}
+    if cache.device_error(stream):
+        raise RuntimeError("device error word set")
+    peak, kind = _tensor_peak()
+    achieved = flops_layer / (ms_step / L / 1e3) / 1e12
+    result = {
+        "metric": CHUNK_METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 MMA operands (hi + lo halves)/fp32 accumulate",
+        "data": "synthetic (seeded: keys N(mu_c, sigma_c) with channel outliers, values with drifting mean)",
+        "config": {**w.describe(), "op": "chunk attention", "chunk_queries": n,
+                   "equivalent_bits": round(cache.equivalent_bits(), 5),
+                   "parallelism": f"replicas x{world}",
+                   "l2": "compute-bound; the quantized cache of a layer is L2-resident and read by every CTA of its unit"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "chunk_attn_kernel (all layers)", "flops_per_launch": flops_layer,
+                     "us_per_launch": round(ms_step / L * 1e3, 2),
+                     "peak_source": f"{kind} bf16 dense (fp16 has the same tensor rate); the kernel issues two "
+                                    f"MMAs (hi, lo) per algorithmic product"},
+        "e2e": e2e, "gpu_launches": L * args.steps, "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, step_s, desc = chunk_oracle_sample(w, n, args.cpu_budget)
+        result["cpu_baseline"] = {"value": round(tf, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                  "sample": desc, "seconds_per_step": round(step_s, 1)}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+# ----------------------------------------------------------------------------
 # reference arm: the oracle
 # ----------------------------------------------------------------------------
 
@@ -480,6 +683,30 @@ def run_reference(args):
     }))
 
 
+def run_chunk_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    w, n = _chunk_workload(args)
+    smp = ChunkOracleSampler(w, n)
+    vals = []
+    for s in range(args.warmup + args.steps):
+        step_s = smp.step()
+        if s >= args.warmup:
+            vals.append(step_s)
+    step_s = statistics.median(vals)
+    v = smp.step_flops / step_s / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": CHUNK_METRIC, "value": round(v, 8), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 quantizer / f64 attention", "data": "synthetic",
+        "config": {**w.describe(), "op": "chunk attention", "chunk_queries": n},
+        "cpu_baseline": {"value": round(v, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": smp.desc},
+        "e2e": {"value": round(v, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,11 +720,20 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="profiling runs: only the workload's first N layers")
     ap.add_argument("--key-mode", choices=["channel", "token"], default="channel",
                     help="keys per channel over groups (KIVI) or per token (per-token-asym) on every layer")
+    ap.add_argument("--op", choices=["decode", "chunk"], default="decode",
+                    help="decode: the per-token decode step; chunk: causal chunk attention of n queries "
+                         "over every layer's quantized cache (prefill over the dequantized cache)")
+    ap.add_argument("--chunk", type=int, default=0, help="--op chunk: queries per chunk (default: the context)")
+    ap.add_argument("--chunk-batch", type=int, default=2, help="--op chunk: sequences")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op == "chunk" and args.steps == 120:
+        args.steps = 5  # a chunk step is a whole-model prefill attention
     if args.impl == "reference":
-        run_reference(args)
+        run_chunk_reference(args) if args.op == "chunk" else run_reference(args)
+    elif args.op == "chunk":
+        run_chunk(args)
     else:
         run_gpu(args)
 
