@@ -1,13 +1,13 @@
 // Dispatch of the chunk-attention kernels (kvq_chunk.cuh): selects the
 // (k_bits, v_bits, head_dim) instantiation, sets its shared-memory attribute
-// once, and launches one CTA per 128 (query, head) rows of each unit.
+// once, and launches one CTA per 256 (query, head) rows of each unit.
 #include "kvq_kernels.h"
 
 namespace kvq {
 
 namespace {
-constexpr int kRowsPerCta = 128;
-constexpr int kThreadsPerCta = 128;
+constexpr int kRowsPerCta = 256;
+constexpr int kThreadsPerCta = 256;
 
 int bits_index(int b) { return b == 2 ? 0 : b == 3 ? 1 : b == 4 ? 2 : b == 8 ? 3 : -1; }
 }  // namespace

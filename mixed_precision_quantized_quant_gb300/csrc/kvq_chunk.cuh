@@ -4,22 +4,26 @@
 // (section A2, calibration design) runs prefill attention this way, over the
 // dequantized cache; the attention itself is its A3 equation.
 //
-// One CTA of 128 threads owns 128 (query, head) rows of one (batch, kv head)
-// unit and walks the unit's tokens in tiles of 64, first the quantized groups
-// and then the FP16 window.  Per tile:
-//   1. all threads unpack the tile into shared memory as MMA operands:
+// One CTA of 256 threads owns 256 (query, head) rows of one (batch, kv head)
+// unit, as two groups of 128 rows (one MMA tile each, one thread per row),
+// and walks the unit's tokens in tiles of 64, first the quantized groups and
+// then the FP16 window.  Per tile:
+//   1. all threads unpack the tile into shared memory as MMA operands, once
+//      for both groups:
 //      keys k^ = code*s + z in fp32, split into fp16 hi + lo halves (so the
 //      products keep about 22 bits); value codes as exact fp16 integers, the
 //      window's values as they are; the per-token value (scale, zero).
 //   2. one thread issues S = Q K^T as tcgen05 MMAs (hi and lo) into tensor
-//      memory (128 lanes x 64 fp32 columns).
+//      memory (128 lanes x 64 fp32 columns per group), group 0 first.
 //   3. each thread loads its row of S from tensor memory and runs the online
 //      softmax in the log2 domain (lazy rescale: only when the running max
 //      grows by more than 2^8).  It writes P' = p * s_value as fp16 hi + lo
 //      rows and keeps l = sum p and zs = sum p * z_value in registers, so the
 //      value zero never enters an MMA.
-//   4. one thread issues O += P' C (hi and lo) into tensor memory
-//      (128 lanes x d fp32 columns), C being the value codes.
+//   4. one thread per group issues O += P' C (hi and lo) into tensor memory
+//      (128 lanes x d fp32 columns per group), C being the value codes.
+// Group 0's softmax runs while group 1's score MMAs do, and group 1's while
+// group 0's P.V MMAs do.
 // The epilogue returns (O + zs) / l.  3-bit value rows store their 2-bit
 // field (channel 11w + 10) with scale s2 = (7 s)/3; those codes enter C as
 // 7 * code, and their O columns are divided by 3 once before the window
@@ -37,26 +41,29 @@
 
 namespace kvq {
 
-constexpr int kChunkRows = 128;     // (query, head) rows per CTA: the MMA's M
+constexpr int kChunkRows = 256;     // (query, head) rows per CTA: two groups
+constexpr int kChunkM = 128;        // rows per group: the MMA's M
 constexpr int kChunkTile = 64;      // tokens per tile: N of the score MMA, K of P.V
-constexpr int kChunkThreads = 128;  // one thread per row
+constexpr int kChunkThreads = 256;  // one thread per row
 
 template <int D>
 struct ChunkSmem {
   static constexpr int KC = D / 8;                                  // core matrices along d
-  static constexpr uint32_t q = 0;                                  // [128 rows][D] f16
+  static constexpr uint32_t q = 0;                                  // [256 rows][D] f16
   static constexpr uint32_t kh = q + kChunkRows * D * 2;            // [64 tokens][D] f16, hi
   static constexpr uint32_t kl = kh + kChunkTile * D * 2;           // lo
-  static constexpr uint32_t ph = kl + kChunkTile * D * 2;           // [128 rows][64 tokens] f16, hi
+  static constexpr uint32_t ph = kl + kChunkTile * D * 2;           // [256 rows][64 tokens] f16, hi
   static constexpr uint32_t pl = ph + kChunkRows * kChunkTile * 2;  // lo
+  static constexpr uint32_t pgroup = kChunkM * kChunkTile * 2;      // bytes of one group's P
   static constexpr uint32_t v = pl + kChunkRows * kChunkTile * 2;   // [64 tokens][D] f16
   static constexpr uint32_t ts = v + D * kChunkTile * 2;            // value scale per token, f32
   static constexpr uint32_t tz = ts + kChunkTile * 4;               // value zero per token, f32
-  static constexpr uint32_t bars = tz + kChunkTile * 4;             // two mbarriers
-  static constexpr uint32_t tslot = bars + 16;                      // tensor-memory address
+  static constexpr uint32_t bars = tz + kChunkTile * 4;             // mbarriers: S[2], O[2]
+  static constexpr uint32_t tslot = bars + 32;                      // tensor-memory address
   static constexpr uint32_t bytes = tslot + 16;
-  // tensor memory: S in columns [0, 64), O in [64, 64 + D)
-  static constexpr uint32_t tcols = D == 128 ? 256 : 128;
+  // tensor memory: S of group g in columns [64 g, 64 g + 64), O of group g
+  // in [128 + D g, 128 + D g + D)
+  static constexpr uint32_t tcols = D == 128 ? 512 : 256;
 };
 
 // Unpacking plan of one thread's 8 channels c0 .. c0+7 of a B-bit code row
@@ -111,21 +118,25 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
   lo = h2_as_u32(__floats2half2_rn(a - hf.x, b - hf.y));
 }
 
+// barrier of the 128 threads of one row group (ids 1 and 2; 0 is the CTA's)
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
 // exact small integer code (< 1024) as fp32: 2^23 + code, minus 2^23
 __device__ __forceinline__ float code_f32(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
 
 template <int KB, int VB, int D>
-__global__ void __launch_bounds__(kChunkThreads, 2) chunk_attn_kernel(ChunkParams p) {
+__global__ void __launch_bounds__(kChunkThreads, 1) chunk_attn_kernel(ChunkParams p) {
   using L = ChunkSmem<D>;
   constexpr int KC = L::KC;
   constexpr int kTile = kChunkTile;
   extern __shared__ __align__(1024) uint8_t sm[];
-  uint64_t* barS = reinterpret_cast<uint64_t*>(sm + L::bars);
-  uint64_t* barO = barS + 1;
+  uint64_t* barS = reinterpret_cast<uint64_t*>(sm + L::bars);  // [2]: S of group g ready
+  uint64_t* barO = barS + 2;                                   // [2]: P.V of group g done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::tslot);
   float* tok_s = reinterpret_cast<float*>(sm + L::ts);
   float* tok_z = reinterpret_cast<float*>(sm + L::tz);
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int grp = tid >> 7;  // row group: rows 128 grp .. 128 grp + 127
 
   const int u = blockIdx.y;
   const int blk = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest rows first
@@ -155,7 +166,9 @@ __global__ void __launch_bounds__(kChunkThreads, 2) chunk_attn_kernel(ChunkParam
   }
   if (tid == 0) {
     mbar_init(barS, 1);
+    mbar_init(barS + 1, 1);
     mbar_init(barO, 1);
+    mbar_init(barO + 1, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, L::tcols);
@@ -163,13 +176,14 @@ __global__ void __launch_bounds__(kChunkThreads, 2) chunk_attn_kernel(ChunkParam
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tb = *tslot;
-  const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-  const uint32_t tS = tb + lane_off, tO = tb + kTile + lane_off;  // this warp's lanes
+  const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  // this warp's lanes of its group's S and O
+  const uint32_t tS = tb + kTile * grp + lane_off, tO = tb + 2 * kTile + D * grp + lane_off;
   const uint32_t sq = smem_u32(sm + L::q);
   const uint32_t skh = smem_u32(sm + L::kh), skl = smem_u32(sm + L::kl);
   const uint32_t sph = smem_u32(sm + L::ph), spl = smem_u32(sm + L::pl), sv = smem_u32(sm + L::v);
-  constexpr uint32_t idS = idesc_f16_f32(kChunkRows, kTile);
-  constexpr uint32_t idO = idesc_f16_f32(kChunkRows, D) | (1u << 16);  // B (values) MN-major
+  constexpr uint32_t idS = idesc_f16_f32(kChunkM, kTile);
+  constexpr uint32_t idO = idesc_f16_f32(kChunkM, D) | (1u << 16);  // B (values) MN-major
 
   // ---- fill coordinates.  Thread (tid & 7) fills row tid & 7 of every core
   // matrix it touches, so 8 consecutive threads store one whole 128-byte
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__(kChunkThreads, 2) chunk_attn_kernel(ChunkParam
     const int t0 = quant ? it * kTile : p.n_q + (it - ntq) * kTile;
     const int tend = quant ? min(t0 + kTile, endQ) : min(t0 + kTile, endW);
     // the previous P.V product has read its operands (and written O)
-    if (it > 0 && !failed) failed = !mbar_wait(barO, (it - 1) & 1, p.err);
+    if (it > 0 && !failed) failed = !mbar_wait(barO, (it - 1) & 1, p.err) || !mbar_wait(barO + 1, (it - 1) & 1, p.err);
 
     // ---- keys (hi + lo halves) and values of the tile into shared memory,
     // from the words prefetched during the previous tile
@@ -357,18 +371,24 @@ __global__ void __launch_bounds__(kChunkThreads, 2) chunk_attn_kernel(ChunkParam
     tc_fence_before_sync();
     failed = __syncthreads_or(failed);
 
-    // ---- S = Q K^T (hi, then lo)
+    // ---- S = Q K^T (hi, then lo), group 0 then group 1
     if (tid == 0 && !failed) {
       tc_fence_after_sync();
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        umma_f16(tb, smem_desc(sq + ks * 256, 128, KC * 128), smem_desc(skh + ks * 256, 128, KC * 128), idS, ks > 0);
+      for (int g = 0; g < 2; ++g) {
+        const uint32_t qg = sq + g * (kChunkM * D * 2);
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        umma_f16(tb, smem_desc(sq + ks * 256, 128, KC * 128), smem_desc(skl + ks * 256, 128, KC * 128), idS, 1u);
-      umma_commit(barS);
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_f16(tb + kTile * g, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(skh + ks * 256, 128, KC * 128),
+                   idS, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_f16(tb + kTile * g, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(skl + ks * 256, 128, KC * 128),
+                   idS, 1u);
+        umma_commit(barS + g);
+      }
     }
-    if (!failed) failed = !mbar_wait(barS, it & 1, p.err);
+    if (!failed) failed = !mbar_wait(barS + grp, it & 1, p.err);
     tc_fence_after_sync();
 
     // ---- online softmax of this thread's row
@@ -439,32 +459,34 @@ __global__ void __launch_bounds__(kChunkThreads, 2) chunk_attn_kernel(ChunkParam
     zs += zsum;
 #pragma unroll
     for (int cc = 0; cc < kTile / 8; ++cc) {
-      *reinterpret_cast<uint4*>(sm + L::ph + core_off(r, 8 * cc, kTile / 8)) =
+      *reinterpret_cast<uint4*>(sm + L::ph + grp * L::pgroup + core_off(r & 127, 8 * cc, kTile / 8)) =
           make_uint4(hi[4 * cc], hi[4 * cc + 1], hi[4 * cc + 2], hi[4 * cc + 3]);
-      *reinterpret_cast<uint4*>(sm + L::pl + core_off(r, 8 * cc, kTile / 8)) =
+      *reinterpret_cast<uint4*>(sm + L::pl + grp * L::pgroup + core_off(r & 127, 8 * cc, kTile / 8)) =
           make_uint4(lo[4 * cc], lo[4 * cc + 1], lo[4 * cc + 2], lo[4 * cc + 3]);
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
-    __syncthreads();
+    group_sync(1 + grp);
 
-    // ---- O += P' C (hi, then lo); C token-major (MN-major B)
-    if (tid == 0 && !failed) {
+    // ---- O += P' C (hi, then lo) of this group; C token-major (MN-major B)
+    if ((tid & 127) == 0 && !failed) {
       tc_fence_after_sync();
+      const uint32_t dO = tb + 2 * kTile + D * grp;
+      const uint32_t pg = grp * L::pgroup;
 #pragma unroll
       for (int ks = 0; ks < kTile / 16; ++ks)
-        umma_f16(tb + kTile, smem_desc(sph + ks * 256, 128, (kTile / 8) * 128),
+        umma_f16(dO, smem_desc(sph + pg + ks * 256, 128, (kTile / 8) * 128),
                  smem_desc(sv + ks * 2 * KC * 128, KC * 128, 128), idO, (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < kTile / 16; ++ks)
-        umma_f16(tb + kTile, smem_desc(spl + ks * 256, 128, (kTile / 8) * 128),
+        umma_f16(dO, smem_desc(spl + pg + ks * 256, 128, (kTile / 8) * 128),
                  smem_desc(sv + ks * 2 * KC * 128, KC * 128, 128), idO, 1u);
-      umma_commit(barO);
+      umma_commit(barO + grp);
     }
   }
 
   // ---- epilogue: out = (O + zs) / l
-  if (!failed) failed = !mbar_wait(barO, (ntiles - 1) & 1, p.err);
+  if (!failed) failed = !mbar_wait(barO + grp, (ntiles - 1) & 1, p.err);
   tc_fence_after_sync();
   const bool third = VB == 3 && ntw == 0;
   const float inv = 1.0f / l;

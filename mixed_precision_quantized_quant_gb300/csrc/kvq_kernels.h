@@ -42,7 +42,7 @@ ChunkKernel chunk_get_k3(int vb, int D);
 ChunkKernel chunk_get_k4(int vb, int D);
 ChunkKernel chunk_get_k8(int vb, int D);
 cudaError_t chunk_attn_launch(int kb, int vb, int D, const ChunkParams& p, int units, cudaStream_t s);
-// Queries of the n newest tokens that one CTA serves (128 (query, head) rows).
+// Queries of the n newest tokens that one CTA serves (256 (query, head) rows).
 int chunk_queries_per_cta(int gqa);
 
 }  // namespace kvq
