@@ -232,6 +232,15 @@ int64_t kvq_decode_bytes(const kvq_handle* h, int layer);
  * consistency check), clearing it.  Synchronizes `stream`.  0 means none. */
 kvq_status kvq_device_error(kvq_handle* h, int32_t* code, void* stream);
 
+/* Failure-detection self-test of the device-side waits.  Launches one warp
+ * that waits on an mbarrier nothing ever completes, with a short bound (4096
+ * tries), as every wait in the library is bounded.  The wait must give up,
+ * record the timeout in the error word and return, with the CUDA context
+ * still usable.  KVQ_OK if exactly that happened (the word is read and
+ * cleared), KVQ_ERR_STATE if the timeout was not reported.  Synchronizes
+ * `stream`; changes nothing else. */
+kvq_status kvq_selftest_bounded_wait(kvq_handle* h, void* stream);
+
 /* Release the handle (host memory and any captured graph).  The device buffer
  * stays the caller's. */
 kvq_status kvq_destroy(kvq_handle* h);

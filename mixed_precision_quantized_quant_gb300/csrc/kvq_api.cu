@@ -262,6 +262,18 @@ kvq_status launch_chunk(kvq_handle* h, int layer, const void* q, int n, float* o
   return KVQ_OK;
 }
 
+// A wait that nothing completes: the bounded wait of every kernel must give
+// up, record kErrWaitTimeout in the error word and return (no trap, no hang).
+__global__ void bounded_wait_selftest_kernel(int32_t* err, uint32_t limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    kvq::mbar_init(&bar, 1);
+    kvq::fence_mbar_init();
+  }
+  __syncthreads();
+  kvq::mbar_wait(&bar, 0, err, limit);  // no arrival ever comes
+}
+
 }  // namespace
 
 extern "C" {
@@ -455,6 +467,20 @@ kvq_status kvq_device_error(kvq_handle* h, int32_t* code, void* stream) {
   *code = v;
   if (v != 0 && cudaMemset(errw(h), 0, 4) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
+}
+
+kvq_status kvq_selftest_bounded_wait(kvq_handle* h, void* stream) {
+  if (!h) return KVQ_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t before = 0;
+  kvq_status st = kvq_device_error(h, &before, stream);  // start from a clear error word
+  if (st != KVQ_OK) return st;
+  bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(errw(h), 4096u);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  int32_t code = 0;
+  st = kvq_device_error(h, &code, stream);  // synchronizes, reads and clears
+  if (st != KVQ_OK) return st;
+  return code == kvq::kErrWaitTimeout ? KVQ_OK : KVQ_ERR_STATE;
 }
 
 kvq_status kvq_destroy(kvq_handle* h) {

@@ -156,10 +156,10 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Bounded wait on an mbarrier phase.  Returns false (and records the error)
-// if the phase did not complete within the iteration limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t* err) {
+// if the phase did not complete within `limit` tries.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t* err, uint32_t limit = kWaitLimit) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"

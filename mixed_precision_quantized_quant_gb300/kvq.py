@@ -24,6 +24,7 @@ EXPORTS = (
     "kvq_cache_bytes", "kvq_create", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
     "kvq_layer_view_get", "kvq_equivalent_bits", "kvq_decode_bytes", "kvq_device_error",
     "kvq_destroy", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_chunk_attn",
+    "kvq_selftest_bounded_wait",
 )
 
 
@@ -94,6 +95,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.kvq_decode_bytes.restype = i64
     L.kvq_device_error.argtypes = [vp, ctypes.POINTER(i32), vp]
     L.kvq_device_error.restype = ctypes.c_int
+    L.kvq_selftest_bounded_wait.argtypes = [vp, vp]
+    L.kvq_selftest_bounded_wait.restype = ctypes.c_int
     L.kvq_destroy.argtypes = [vp]
     L.kvq_destroy.restype = ctypes.c_int
     L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -176,6 +179,10 @@ def kvq_device_error(h: int, stream: int) -> int:
     code = ctypes.c_int32(0)
     _check(load().kvq_device_error(h, ctypes.byref(code), stream), "kvq_device_error")
     return code.value
+
+
+def kvq_selftest_bounded_wait(h: int, stream: int) -> None:
+    _check(load().kvq_selftest_bounded_wait(h, stream), "kvq_selftest_bounded_wait")
 
 
 def kvq_destroy(h: int) -> None:
