@@ -160,3 +160,76 @@ def test_chunk_full_size_prefill_sampled(kb, vb):
                 got.append(on[b, h * rep + j, i])
         assert_attn_close(np.stack(got), np.stack(exp), f"unit {u} K{kb}V{vb}")
     cache.close()
+
+
+def test_chunk_after_single_token_appends():
+    """Chunks of several sizes after each of a run of one-token appends, so
+    the window fills, flushes and wraps between calls."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(21)
+    B, Hkv, gqa, D, G, R = 1, 2, 4, 128, 32, 64
+    T0, steps = 100, 45
+    cache = K.KVQCache([(4, 3, R)], B, Hkv * gqa, Hkv, D, G, T0 + steps)
+    ora = O.OracleLayerCache(B, Hkv, D, G, 4, 3, R)
+    k, v = _kv(gen, B, Hkv, T0, D, 0, T0 + steps)
+    cache.append(0, k, v)
+    ora.append(k.cpu().numpy(), v.cpu().numpy())
+    for s in range(steps):
+        k, v = _kv(gen, B, Hkv, 1, D, T0 + s, T0 + steps)
+        cache.append(0, k, v)
+        ora.append(k.cpu().numpy(), v.cpu().numpy())
+        if s % 7 == 0 or s == steps - 1:
+            n = 1 + (s * 13) % 70
+            q = torch.randn((B, Hkv * gqa, n, D), generator=gen, device="cuda").half()
+            out = cache.chunk_attn(0, q)
+            torch.cuda.synchronize()
+            assert_attn_close(out.cpu().numpy(), ora.attend_chunk(q.cpu().numpy()), f"step {s} n {n}")
+    assert cache.device_error() == 0
+    cache.close()
+
+
+@pytest.mark.parametrize("idx,key_mode,n", [(3, 1, 512), (4, 0, 256), (6, 0, 300)])
+def test_chunk_full_size_workloads_sampled(idx, key_mode, n):
+    """Chunk attention at the other workloads' full shapes (one layer of each
+    distinct precision pair, batch cut to 2): Qwen2.5-7B-shaped with 7 query
+    heads per kv head and per-token keys, KVmix's 800/384-token windows and
+    its K3V4 orientation.  Sampled (unit, query) rows against fp64."""
+    w = W.workload(idx)
+    if key_mode:
+        w = W.scaled(w, layers=tuple((kb, vb, r, key_mode) for kb, vb, r in w.layers))
+    w = W.scaled(w, batch=2)
+    seen, layers = set(), []
+    for l, lay in enumerate(w.layers):
+        if lay not in seen:
+            seen.add(lay)
+            layers.append(l)
+    T, D, Hkv, Hq = w.context, w.head_dim, w.num_kv_heads, w.num_q_heads
+    rep = Hq // Hkv
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(31)
+    for l in layers[:3]:
+        kb, vb, R = w.layers[l][:3]
+        km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
+        cache = K.KVQCache([w.layers[l]], w.batch, Hq, Hkv, D, w.group_size, T)
+        k, v = W.gen_kv(w, l, 0, T, device="cuda")
+        cache.append(0, k, v)
+        q = torch.randn((w.batch, Hq, n, D), generator=gen, device="cuda").half()
+        out = cache.chunk_attn(0, q)
+        torch.cuda.synchronize()
+        assert cache.device_error() == 0
+        on, qn = out.cpu().numpy(), q.cpu().numpy()
+        kn, vn = k.cpu().numpy(), v.cpu().numpy()
+        U = w.batch * Hkv
+        for u in sorted({0, U - 1}):
+            b, h = divmod(u, Hkv)
+            ora = O.OracleLayerCache(1, 1, D, w.group_size, kb, vb, R, km)
+            ora.append(kn[b:b + 1, h:h + 1], vn[b:b + 1, h:h + 1])
+            kh, vh = ora.dequantized(0)
+            got, exp = [], []
+            for j in (0, rep - 1):
+                for i in (0, n // 3, n - 1):
+                    pos = T - n + i
+                    exp.append(O.attention_fp64(qn[b, h * rep + j, i].astype(np.float64), kh[: pos + 1], vh[: pos + 1]))
+                    got.append(on[b, h * rep + j, i])
+            assert_attn_close(np.stack(got), np.stack(exp), f"workload {idx} layer {l} unit {u}")
+        cache.close()
