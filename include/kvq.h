@@ -171,10 +171,20 @@ kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, 
  * q: device fp16 [batch][num_q_heads][n_queries][head_dim], 16-byte aligned;
  *    query head j reads kv head j / (num_q_heads / num_kv_heads).
  * out: device fp32 [batch][num_q_heads][n_queries][head_dim], written entirely.
+ * workspace: caller-owned device scratch of at least
+ *    kvq_chunk_workspace_bytes(h) bytes, 16-byte aligned; the layer's tiles are
+ *    dequantized into it once, then read by the tensor-core kernel.  Its
+ *    contents are overwritten; a call must not share it with another in flight.
  * KVQ_ERR_ARG if n_queries < 1 or > tokens appended; KVQ_ERR_STATE if the layer
- * is empty; KVQ_ERR_UNSUPPORTED if num_q_heads / num_kv_heads > 128 or
- * batch * num_kv_heads > 65535.  Runs on the tensor cores (tcgen05). */
-kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries, float* out, void* stream);
+ * is empty; KVQ_ERR_CAPACITY if the workspace is too small;
+ * KVQ_ERR_UNSUPPORTED if batch * num_kv_heads > 65535.  Runs on the tensor
+ * cores (tcgen05). */
+kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries, float* out, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Bytes of the workspace kvq_chunk_attn needs for any layer of `h` (its
+ * dequantized tiles of every (batch, kv head) at max_tokens).  0 if h is null. */
+size_t kvq_chunk_workspace_bytes(const kvq_handle* h);
 
 /* One decode step over every layer: for l = 0 .. num_layers-1,
  * kvq_append(l, K[l], V[l], 1) then kvq_decode_attn(l, q[l], out[l]).

@@ -227,7 +227,11 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   return KVQ_OK;
 }
 
-kvq_status launch_chunk(kvq_handle* h, int layer, const void* q, int n, float* out, cudaStream_t s) {
+// Tiles of one unit in the chunk workspace: the quantized part and the
+// window part each start a new 64-token tile.
+int64_t chunk_ws_tiles(const Plan& P) { return (P.max_tokens + 63) / 64 + 1; }
+
+kvq_status launch_chunk(kvq_handle* h, int layer, const void* q, int n, float* out, void* ws, cudaStream_t s) {
   const Plan& P = h->plan;
   const LayerPlan& lp = P.layers[layer];
   kvq::ChunkParams cp;
@@ -258,7 +262,10 @@ kvq_status launch_chunk(kvq_handle* h, int layer, const void* q, int n, float* o
   cp.off_kscale = static_cast<int>(4LL * P.G * (lp.wk + lp.wv));
   cp.off_vsz = cp.off_kscale + static_cast<int>(lp.km ? 4LL * P.G : 4LL * P.D);
   cp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
-  if (kvq::chunk_attn_launch(lp.kb, lp.vb, P.D, cp, P.units, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  cp.ws = static_cast<uint8_t*>(ws);
+  cp.ws_tiles = static_cast<int>(chunk_ws_tiles(P));
+  const int tiles = (cp.n_q + 63) / 64 + (cp.T - cp.n_q + 63) / 64;
+  if (kvq::chunk_attn_launch(lp.kb, lp.vb, P.D, cp, P.units, tiles, s) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 
@@ -346,14 +353,22 @@ kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, 
   return launch_decode(h, layer, q, out, static_cast<cudaStream_t>(stream));
 }
 
-kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries, float* out, void* stream) {
+size_t kvq_chunk_workspace_bytes(const kvq_handle* h) {
+  if (!h) return 0;
+  return static_cast<size_t>(h->plan.units) * static_cast<size_t>(chunk_ws_tiles(h->plan)) *
+         kvq::chunk_tile_bytes(h->plan.D);
+}
+
+kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries, float* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
   if (!h || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
-  if (!q || !out) return KVQ_ERR_ARG;
-  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
+  if (!q || !out || !workspace) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVQ_ERR_ALIGN;
+  if (workspace_bytes < kvq_chunk_workspace_bytes(h)) return KVQ_ERR_CAPACITY;
   if (h->tokens[layer] <= 0) return KVQ_ERR_STATE;
   if (n_queries < 1 || n_queries > h->tokens[layer]) return KVQ_ERR_ARG;
   if (kvq::chunk_queries_per_cta(h->plan.gqa) < 1 || h->plan.units > 65535) return KVQ_ERR_UNSUPPORTED;
-  return launch_chunk(h, layer, q, n_queries, out, static_cast<cudaStream_t>(stream));
+  return launch_chunk(h, layer, q, n_queries, out, workspace, static_cast<cudaStream_t>(stream));
 }
 
 kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V, const void* const* q,

@@ -4,34 +4,34 @@
 // (section A2, calibration design) runs prefill attention this way, over the
 // dequantized cache; the attention itself is its A3 equation.
 //
-// One CTA of 256 threads owns 256 (query, head) rows of one (batch, kv head)
-// unit, as two groups of 128 rows (one MMA tile each, one thread per row),
-// and walks the unit's tokens in tiles of 64, first the quantized groups and
-// then the FP16 window.  Per tile:
-//   1. all threads unpack the tile into shared memory as MMA operands, once
-//      for both groups:
-//      keys k^ = code*s + z in fp32, split into fp16 hi + lo halves (so the
-//      products keep about 22 bits); value codes as exact fp16 integers, the
-//      window's values as they are; the per-token value (scale, zero).
-//   2. one thread issues S = Q K^T as tcgen05 MMAs (hi and lo) into tensor
-//      memory (128 lanes x 64 fp32 columns per group), group 0 first.
-//   3. each thread loads its row of S from tensor memory and runs the online
-//      softmax in the log2 domain (lazy rescale: only when the running max
-//      grows by more than 2^8).  It writes P' = p * s_value as fp16 hi + lo
-//      rows and keeps l = sum p and zs = sum p * z_value in registers, so the
-//      value zero never enters an MMA.
-//   4. one thread per group issues O += P' C (hi and lo) into tensor memory
-//      (128 lanes x d fp32 columns per group), C being the value codes.
-// Group 0's softmax runs while group 1's score MMAs do, and group 1's while
-// group 0's P.V MMAs do.
-// The epilogue returns (O + zs) / l.  3-bit value rows store their 2-bit
-// field (channel 11w + 10) with scale s2 = (7 s)/3; those codes enter C as
-// 7 * code, and their O columns are divided by 3 once before the window
-// tiles (or in the epilogue when there are none).
+// Two kernels.
 //
-// Operands in shared memory use the no-swizzle core-matrix layout: Q, K^ hi,
-// K^ lo and P' are K-major; the values are stored token-major, which is the
-// MN-major form of the P.V product's B operand.
+// chunk_dequant_kernel<KB, VB, D> unpacks each 64-token tile of a unit once
+// into a workspace, already in the shared-memory layout of the MMA operands:
+//   keys   k^ = code*s + z in fp32, split into fp16 hi + lo halves (so the
+//          products keep about 22 bits), K-major core matrices;
+//   values codes as exact fp16 integers (the window's values as they are),
+//          token-major, the MN-major form of the P.V product's B operand;
+//   the per-token value (scale, zero); window tokens (1, 0).
+// Tiles cover the quantized groups [0, n_q) in steps of 64, then the FP16
+// window [n_q, T) in steps of 64; tokens past a region's end are zero.
+//
+// chunk_attn_kernel<D>: one CTA owns 256 (query, head) rows of one (batch,
+// kv head) unit, as two groups of 128 rows (one MMA tile, M = 128, each; one
+// softmax thread per row), plus one warp whose first thread copies tiles in
+// (bulk copies, two stages, keys and values released separately) and issues
+// every tensor-core MMA:
+//   S = Q K^T  (hi, then lo) into tensor memory, 64 fp32 columns per group,
+//              double-buffered so that the scores of tile it+1 run while the
+//              softmax of tile it does;
+//   O += P' C  (hi, then lo) into tensor memory, d fp32 columns per group.
+// Each softmax thread loads its row of S, runs the online softmax in the log2
+// domain (lazy rescale of O when the max grows by more than 2^8), writes
+// P' = p * s_value as fp16 hi + lo rows and keeps l = sum p and zs = sum p z
+// in registers, so the value zero never enters an MMA.  The epilogue returns
+// (O + zs) / l.  3-bit value rows store their 2-bit field (channel 11w + 10)
+// with scale s2 = (7 s)/3; those codes enter C as 7 * code, and their O
+// columns are divided by 3 once before the window tiles (or at the end).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -41,29 +41,43 @@
 
 namespace kvq {
 
-constexpr int kChunkRows = 256;     // (query, head) rows per CTA: two groups
-constexpr int kChunkM = 128;        // rows per group: the MMA's M
-constexpr int kChunkTile = 64;      // tokens per tile: N of the score MMA, K of P.V
-constexpr int kChunkThreads = 256;  // one thread per row
+constexpr int kChunkRows = 256;                        // (query, head) rows per CTA: two groups
+constexpr int kChunkM = 128;                           // rows per group: the MMA's M
+constexpr int kChunkTile = 64;                         // tokens per tile
+constexpr int kChunkThreads = 256;                     // softmax threads, one per row
+constexpr int kChunkCtaThreads = kChunkThreads + 32;   // and the copy/MMA warp
+constexpr int kDequantThreads = 256;
+
+// One dequantized tile, in the workspace and (copied verbatim) in shared
+// memory: [K hi][K lo][V], each [64 tokens][D] f16 core-matrix tiles, then 64
+// (scale, zero) f16 pairs.  Keys and values are copied separately.
+template <int D>
+struct ChunkTile {
+  static constexpr int KC = D / 8;
+  static constexpr uint32_t kh = 0;
+  static constexpr uint32_t kl = kChunkTile * D * 2;
+  static constexpr uint32_t v = 2 * kChunkTile * D * 2;
+  static constexpr uint32_t sz = 3 * kChunkTile * D * 2;
+  static constexpr uint32_t kbytes = 2 * kChunkTile * D * 2;              // keys, one bulk copy
+  static constexpr uint32_t vbytes = kChunkTile * D * 2 + kChunkTile * 4;  // values + pairs, one bulk copy
+  static constexpr uint32_t bytes = kbytes + vbytes;
+};
 
 template <int D>
 struct ChunkSmem {
-  static constexpr int KC = D / 8;                                  // core matrices along d
+  using T = ChunkTile<D>;
+  static constexpr int KC = D / 8;
   static constexpr uint32_t q = 0;                                  // [256 rows][D] f16
-  static constexpr uint32_t kh = q + kChunkRows * D * 2;            // [64 tokens][D] f16, hi
-  static constexpr uint32_t kl = kh + kChunkTile * D * 2;           // lo
-  static constexpr uint32_t ph = kl + kChunkTile * D * 2;           // [256 rows][64 tokens] f16, hi
+  static constexpr uint32_t stage = q + kChunkRows * D * 2;         // two tile buffers
+  static constexpr uint32_t ph = stage + 2 * T::bytes;              // [256 rows][64 tokens] f16, hi
   static constexpr uint32_t pl = ph + kChunkRows * kChunkTile * 2;  // lo
   static constexpr uint32_t pgroup = kChunkM * kChunkTile * 2;      // bytes of one group's P
-  static constexpr uint32_t v = pl + kChunkRows * kChunkTile * 2;   // [64 tokens][D] f16
-  static constexpr uint32_t ts = v + D * kChunkTile * 2;            // value scale per token, f32
-  static constexpr uint32_t tz = ts + kChunkTile * 4;               // value zero per token, f32
-  static constexpr uint32_t bars = tz + kChunkTile * 4;             // mbarriers: S[2], O[2]
-  static constexpr uint32_t tslot = bars + 32;                      // tensor-memory address
+  static constexpr uint32_t bars = pl + kChunkRows * kChunkTile * 2;  // 16 mbarriers
+  static constexpr uint32_t tslot = bars + 128;                     // tensor-memory address
   static constexpr uint32_t bytes = tslot + 16;
-  // tensor memory: S of group g in columns [64 g, 64 g + 64), O of group g
-  // in [128 + D g, 128 + D g + D)
-  static constexpr uint32_t tcols = D == 128 ? 512 : 256;
+  // tensor memory: S of buffer b, group g in columns [64 (2b + g), +64); O of
+  // group g in [256 + D g, +D)
+  static constexpr uint32_t tcols = 512;
 };
 
 // Unpacking plan of one thread's 8 channels c0 .. c0+7 of a B-bit code row
@@ -118,25 +132,195 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
   lo = h2_as_u32(__floats2half2_rn(a - hf.x, b - hf.y));
 }
 
-// barrier of the 128 threads of one row group (ids 1 and 2; 0 is the CTA's)
-__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
-
 // exact small integer code (< 1024) as fp32: 2^23 + code, minus 2^23
 __device__ __forceinline__ float code_f32(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
 
+// one arrival on an mbarrier (release: earlier writes are visible to its waiters)
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Unpack tile `blockIdx.x` of unit `blockIdx.y` into the workspace.
 template <int KB, int VB, int D>
-__global__ void __launch_bounds__(kChunkThreads, 1) chunk_attn_kernel(ChunkParams p) {
+__global__ void __launch_bounds__(kDequantThreads) chunk_dequant_kernel(ChunkParams p) {
+  using T = ChunkTile<D>;
+  constexpr int KC = T::KC;
+  constexpr int kTile = kChunkTile;
+  const int tid = threadIdx.x;
+  const int u = blockIdx.y, tile = blockIdx.x;
+  const int gs = p.gshift;  // G = 1 << gs
+  const int ntq = (p.n_q + kTile - 1) / kTile;
+  const bool quant = tile < ntq;
+  const int t0 = quant ? tile * kTile : p.n_q + (tile - ntq) * kTile;
+  const int tq_end = quant ? min(t0 + kTile, p.n_q) : min(t0 + kTile, p.T);  // tokens that exist
+  const uint8_t* urec = p.records + static_cast<int64_t>(u) * p.unit_rec_stride;
+  uint8_t* dst = p.ws + (static_cast<int64_t>(u) * p.ws_tiles + tile) * T::bytes;
+
+  // Thread (tid & 7) fills row tid & 7 of every core matrix it touches (8
+  // consecutive threads write one whole 128-byte core matrix); its channel
+  // octet kc is fixed and its tokens are row0 + kStep * j.
+  constexpr int kJ = kTile * KC / kDequantThreads;
+  constexpr int kStep = kDequantThreads / KC;
+  const int kc = (tid >> 3) & (KC - 1);
+  const int c0 = kc * 8;
+  const int row0 = (tid & 7) + 8 * (tid / (8 * KC));
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+
+  if (quant) {
+    Unpack8<KB> ku;
+    Unpack8<VB> vu;
+    ku.init(c0);
+    vu.init(c0);
+    const int voff = p.G * p.wk;  // value code rows follow the key code rows
+    // all loads of the tile first
+    uint32_t kw0[kJ], kw1[kJ], vw0[kJ], vw1[kJ];
+    __half2 ksz[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int t = t0 + row0 + kStep * j;
+      kw0[j] = kw1[j] = vw0[j] = vw1[j] = 0u;
+      ksz[j] = __floats2half2_rn(0.0f, 0.0f);
+      if (t < tq_end) {
+        const int gi = t >> gs, rr = t - (gi << gs);
+        const uint8_t* rec = urec + static_cast<int64_t>(gi) * p.rec_bytes;
+        const uint32_t* krow = reinterpret_cast<const uint32_t*>(rec) + rr * p.wk;
+        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec) + voff + rr * p.wv;
+        kw0[j] = krow[ku.wa];
+        if (ku.second_word()) kw1[j] = krow[ku.wa + 1];
+        vw0[j] = vrow[vu.wa];
+        if (vu.second_word()) vw1[j] = vrow[vu.wa + 1];
+        if (p.km) ksz[j] = *reinterpret_cast<const __half2*>(rec + p.off_kscale + rr * 4);
+      }
+    }
+    // per-channel key (scale, zero) of the (at most two) groups of the
+    // thread's tokens, both below n_q / G
+    float sA[8], zA[8], sB[8], zB[8];
+    const int gA = min(t0 + row0, tq_end - 1) >> gs;
+    const int gB = min(t0 + row0 + kStep * (kJ - 1), tq_end - 1) >> gs;
+    if (p.km == 0) {
+      const uint8_t* recA = urec + static_cast<int64_t>(gA) * p.rec_bytes + p.off_kscale;
+      const uint8_t* recB = urec + static_cast<int64_t>(gB) * p.rec_bytes + p.off_kscale;
+      const uint4 sa = *reinterpret_cast<const uint4*>(recA + c0 * 2);
+      const uint4 za = *reinterpret_cast<const uint4*>(recA + D * 2 + c0 * 2);
+      const uint4 sb = *reinterpret_cast<const uint4*>(recB + c0 * 2);
+      const uint4 zb = *reinterpret_cast<const uint4*>(recB + D * 2 + c0 * 2);
+      const __half* psa = reinterpret_cast<const __half*>(&sa);
+      const __half* pza = reinterpret_cast<const __half*>(&za);
+      const __half* psb = reinterpret_cast<const __half*>(&sb);
+      const __half* pzb = reinterpret_cast<const __half*>(&zb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sA[e] = __half2float(psa[e]);
+        zA[e] = __half2float(pza[e]);
+        sB[e] = __half2float(psb[e]);
+        zB[e] = __half2float(pzb[e]);
+        if constexpr (KB == 3) {
+          if ((ku.two >> e) & 1u) {
+            sA[e] = __fdiv_rn(__fmul_rn(sA[e], 7.0f), 3.0f);
+            sB[e] = __fdiv_rn(__fmul_rn(sB[e], 7.0f), 3.0f);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int nn = row0 + kStep * j;
+      const int t = t0 + nn;
+      const bool inB = (t >> gs) != gA;
+      const uint32_t k0 = KB == 2 ? (kw0[j] >> ku.sh0) : kw0[j];
+      const uint32_t v0 = VB == 2 ? (vw0[j] >> vu.sh0) : vw0[j];
+      uint32_t hw[4], lw[4], vh[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        float kv[2];
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          float sc, zc;
+          if (p.km == 0) {
+            sc = inB ? sB[e + q2] : sA[e + q2];
+            zc = inB ? zB[e + q2] : zA[e + q2];
+          } else {
+            const float2 sz = __half22float2(ksz[j]);
+            sc = sz.x;
+            zc = sz.y;
+            if constexpr (KB == 3) {
+              if ((ku.two >> (e + q2)) & 1u) sc = __fdiv_rn(__fmul_rn(sc, 7.0f), 3.0f);
+            }
+          }
+          kv[q2] = fmaf(code_f32(ku.get(k0, kw1[j], e + q2)), sc, zc);
+        }
+        split_hi_lo(kv[0], kv[1], hw[e / 2], lw[e / 2]);
+        // value codes (< 1024) as exact fp16 integers: (1024 + code) - 1024
+        uint32_t c_lo = vu.get(v0, vw1[j], e), c_hi = vu.get(v0, vw1[j], e + 1);
+        if constexpr (VB == 3) {
+          if ((vu.two >> e) & 1u) c_lo *= 7u;
+          if ((vu.two >> (e + 1)) & 1u) c_hi *= 7u;
+        }
+        const uint32_t mag = 0x64006400u | c_lo | (c_hi << 16);
+        vh[e / 2] = h2_as_u32(__hsub2(u32_as_h2(mag), __float2half2_rn(1024.0f)));
+      }
+      const bool live = t < tq_end;
+      const uint32_t off = core_off(nn, c0, KC);
+      *reinterpret_cast<uint4*>(dst + T::kh + off) = live ? make_uint4(hw[0], hw[1], hw[2], hw[3]) : zero;
+      *reinterpret_cast<uint4*>(dst + T::kl + off) = live ? make_uint4(lw[0], lw[1], lw[2], lw[3]) : zero;
+      *reinterpret_cast<uint4*>(dst + T::v + off) = live ? make_uint4(vh[0], vh[1], vh[2], vh[3]) : zero;
+    }
+    if (tid < kTile) {
+      const int t = t0 + tid;
+      __half2 sz = __floats2half2_rn(0.0f, 0.0f);
+      if (t < tq_end) {
+        const int gi = t >> gs, rr = t - (gi << gs);
+        sz = *reinterpret_cast<const __half2*>(urec + static_cast<int64_t>(gi) * p.rec_bytes + p.off_vsz + rr * 4);
+      }
+      *reinterpret_cast<__half2*>(dst + T::sz + tid * 4) = sz;
+    }
+  } else {
+    const __half* rk = p.res_k + static_cast<int64_t>(u) * p.res_stride;
+    const __half* rv = p.res_v + static_cast<int64_t>(u) * p.res_stride;
+    uint4 kr[kJ], vr[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int t = t0 + row0 + kStep * j;
+      kr[j] = vr[j] = zero;
+      if (t < tq_end) {
+        const int slot = t % p.R;
+        const int64_t off = static_cast<int64_t>(slot) * D + ((kc ^ (slot & 7)) * 8);
+        kr[j] = *reinterpret_cast<const uint4*>(rk + off);
+        vr[j] = *reinterpret_cast<const uint4*>(rv + off);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const uint32_t off = core_off(row0 + kStep * j, c0, KC);
+      *reinterpret_cast<uint4*>(dst + T::kh + off) = kr[j];
+      *reinterpret_cast<uint4*>(dst + T::kl + off) = zero;
+      *reinterpret_cast<uint4*>(dst + T::v + off) = vr[j];
+    }
+    if (tid < kTile)
+      *reinterpret_cast<__half2*>(dst + T::sz + tid * 4) =
+          __floats2half2_rn(t0 + tid < tq_end ? 1.0f : 0.0f, 0.0f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkParams p) {
   using L = ChunkSmem<D>;
+  using T = ChunkTile<D>;
   constexpr int KC = L::KC;
   constexpr int kTile = kChunkTile;
   extern __shared__ __align__(1024) uint8_t sm[];
-  uint64_t* barS = reinterpret_cast<uint64_t*>(sm + L::bars);  // [2]: S of group g ready
-  uint64_t* barO = barS + 2;                                   // [2]: P.V of group g done
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(sm + L::bars);  // [stage]: keys landed (tx)
+  uint64_t* vfull = kfull + 2;   // [stage]: values and pairs landed (tx)
+  uint64_t* kfree = kfull + 4;   // [stage]: the scores that read the keys are done (commit)
+  uint64_t* vfree = kfull + 6;   // [stage]: the P.V products that read the values are done (commit)
+  uint64_t* s_done = kfull + 8;  // [stage][group]: scores ready (commit)
+  uint64_t* p_full = kfull + 12; // [group]: P' written, O rescaled (128 arrivals)
+  uint64_t* o_done = kfull + 14; // [group]: P.V done (commit)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::tslot);
-  float* tok_s = reinterpret_cast<float*>(sm + L::ts);
-  float* tok_z = reinterpret_cast<float*>(sm + L::tz);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int grp = tid >> 7;  // row group: rows 128 grp .. 128 grp + 127
+  const int grp = (tid >> 7) & 1;  // row group of a softmax thread
 
   const int u = blockIdx.y;
   const int blk = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest rows first
@@ -146,371 +330,269 @@ __global__ void __launch_bounds__(kChunkThreads, 1) chunk_attn_kernel(ChunkParam
   const int rows = nqb * p.gqa;
   const int pos0 = p.T - p.n;  // position of query 0
   const int last_pos = pos0 + i0 + nqb - 1;
-  const int gs = p.gshift;     // G = 1 << gs
-  const uint8_t* urec = p.records + static_cast<int64_t>(u) * p.unit_rec_stride;
-  const __half* rk = p.res_k + static_cast<int64_t>(u) * p.res_stride;
-  const __half* rv = p.res_v + static_cast<int64_t>(u) * p.res_stride;
+  const uint8_t* wsu = p.ws + static_cast<int64_t>(u) * p.ws_tiles * T::bytes;
 
   // ---- query rows -> shared memory (row r = query r / gqa, head r % gqa)
-  // (8 consecutive threads fill one 128-byte core matrix: conflict-free stores)
+  if (tid < kChunkThreads) {
 #pragma unroll 1
-  for (int idx = tid; idx < kChunkRows * KC; idx += kChunkThreads) {
-    const int r = (idx & 7) + 8 * (idx / (8 * KC)), kc = (idx >> 3) & (KC - 1);
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (r < rows) {
-      const int i = i0 + r / p.gqa, hh = r % p.gqa;
-      const int64_t row = (static_cast<int64_t>(b) * p.Hq + hk * p.gqa + hh) * p.n + i;
-      val = *reinterpret_cast<const uint4*>(p.q + row * D + kc * 8);
+    for (int idx = tid; idx < kChunkRows * KC; idx += kChunkThreads) {
+      const int r = (idx & 7) + 8 * (idx / (8 * KC)), kc = (idx >> 3) & (KC - 1);
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) {
+        const int i = i0 + r / p.gqa, hh = r % p.gqa;
+        const int64_t row = (static_cast<int64_t>(b) * p.Hq + hk * p.gqa + hh) * p.n + i;
+        val = *reinterpret_cast<const uint4*>(p.q + row * D + kc * 8);
+      }
+      *reinterpret_cast<uint4*>(sm + L::q + core_off(r, kc * 8, KC)) = val;
     }
-    *reinterpret_cast<uint4*>(sm + L::q + core_off(r, kc * 8, KC)) = val;
   }
   if (tid == 0) {
-    mbar_init(barS, 1);
-    mbar_init(barS + 1, 1);
-    mbar_init(barO, 1);
-    mbar_init(barO + 1, 1);
+    for (int i = 0; i < 12; ++i) mbar_init(kfull + i, 1);
+    mbar_init(p_full, kChunkM);
+    mbar_init(p_full + 1, kChunkM);
+    mbar_init(o_done, 1);
+    mbar_init(o_done + 1, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, L::tcols);
+  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tb = *tslot;
-  const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-  // this warp's lanes of its group's S and O
-  const uint32_t tS = tb + kTile * grp + lane_off, tO = tb + 2 * kTile + D * grp + lane_off;
-  const uint32_t sq = smem_u32(sm + L::q);
-  const uint32_t skh = smem_u32(sm + L::kh), skl = smem_u32(sm + L::kl);
-  const uint32_t sph = smem_u32(sm + L::ph), spl = smem_u32(sm + L::pl), sv = smem_u32(sm + L::v);
-  constexpr uint32_t idS = idesc_f16_f32(kChunkM, kTile);
-  constexpr uint32_t idO = idesc_f16_f32(kChunkM, D) | (1u << 16);  // B (values) MN-major
-
-  // ---- fill coordinates.  Thread (tid & 7) fills row tid & 7 of every core
-  // matrix it touches, so 8 consecutive threads store one whole 128-byte
-  // core matrix; its channel octet kc is fixed and its tokens are
-  // row0 + kStep * j.
-  constexpr int kJ = kTile * KC / kChunkThreads;  // 16-byte chunks per thread per operand
-  constexpr int kStep = kChunkThreads / KC;       // token stride between them
-  const int kc = (tid >> 3) & (KC - 1);
-  const int c0 = kc * 8;
-  const int row0 = (tid & 7) + 8 * (tid / (8 * KC));
-  Unpack8<KB> ku;
-  Unpack8<VB> vu;
-  ku.init(c0);
-  vu.init(c0);
-  const int voff = p.G * p.wk;  // value code rows follow the key code rows
-
-  // ---- row state: this thread's row and the last position it may see
-  const int r = tid;
-  const int lim = (r < rows) ? pos0 + i0 + r / p.gqa : last_pos;
-  float m = -INFINITY, l = 0.0f, zs = 0.0f;
 
   const int endQ = min(p.n_q, last_pos + 1);
   const int ntq = (endQ + kTile - 1) / kTile;
   const int endW = last_pos + 1;
   const int ntw = endW > p.n_q ? (endW - p.n_q + kTile - 1) / kTile : 0;
-  const int ntiles = ntq + ntw;
-  bool failed = false;
+  const int ntiles = ntq + ntw;  // the unit's tiles 0 .. ntiles-1 (same numbering as the workspace)
 
-  // ---- words of one quantized tile, loaded a tile ahead of their use
-  struct {
-    uint32_t kw0[kJ], kw1[kJ], vw0[kJ], vw1[kJ];
-    __half2 ksz[kJ];
-    uint4 sa, za, sb, zb;  // per-channel key scales and zeros of groups gA, gB
-    __half2 tsz;           // value (scale, zero) of token t0 + tid (tid < 64)
-    int gA;
-  } pf;
-  auto prefetch = [&](int t0) {
-    const int tq_end = min(t0 + kTile, p.n_q);  // whole groups: the rows exist
+  if (warp == kChunkThreads / 32) {
+    // ================= copy/MMA warp: its first thread issues every bulk
+    // copy and every MMA, in the order
+    //   S(it), then P.V(it-1), then the copies of tile it+1 into the stage
+    //   tile it-1 used (keys once S(it-1) is done, values once P.V(it-1) is)
+    if ((tid & 31) == 0) {
+      const uint32_t sq = smem_u32(sm + L::q);
+      const uint32_t sst = smem_u32(sm + L::stage);
+      const uint32_t sph = smem_u32(sm + L::ph), spl = smem_u32(sm + L::pl);
+      constexpr uint32_t idS = idesc_f16_f32(kChunkM, kTile);
+      constexpr uint32_t idO = idesc_f16_f32(kChunkM, D) | (1u << 16);  // B (values) MN-major
+      auto copy_k = [&](int it) {
+        uint64_t* bar = kfull + (it & 1);
+        mbar_arrive_expect_tx(bar, T::kbytes);
+        bulk_g2s(sm + L::stage + (it & 1) * T::bytes, wsu + static_cast<int64_t>(it) * T::bytes, T::kbytes, bar);
+      };
+      auto copy_v = [&](int it) {
+        uint64_t* bar = vfull + (it & 1);
+        mbar_arrive_expect_tx(bar, T::vbytes);
+        bulk_g2s(sm + L::stage + (it & 1) * T::bytes + T::v, wsu + static_cast<int64_t>(it) * T::bytes + T::v,
+                 T::vbytes, bar);
+      };
+      auto issue_pv = [&](int it, bool& bad) {
+        const int bs = it & 1;
+        bad = bad || !mbar_wait(vfull + bs, (it >> 1) & 1, p.err);
+        const uint32_t vb_ = sst + bs * T::bytes + T::v;
 #pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      const int t = t0 + row0 + kStep * j;
-      pf.kw0[j] = pf.kw1[j] = pf.vw0[j] = pf.vw1[j] = 0u;
-      pf.ksz[j] = __floats2half2_rn(0.0f, 0.0f);
-      if (t < tq_end) {
-        const int gi = t >> gs, rr = t - (gi << gs);
-        const uint8_t* rec = urec + static_cast<int64_t>(gi) * p.rec_bytes;
-        const uint32_t* krow = reinterpret_cast<const uint32_t*>(rec) + rr * p.wk;
-        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec) + voff + rr * p.wv;
-        pf.kw0[j] = krow[ku.wa];
-        if (ku.second_word()) pf.kw1[j] = krow[ku.wa + 1];
-        pf.vw0[j] = vrow[vu.wa];
-        if (vu.second_word()) pf.vw1[j] = vrow[vu.wa + 1];
-        if (p.km) pf.ksz[j] = *reinterpret_cast<const __half2*>(rec + p.off_kscale + rr * 4);
+        for (int g = 0; g < 2; ++g) {
+          bad = bad || !mbar_wait(p_full + g, it & 1, p.err);
+          if (bad) return;
+          tc_fence_after_sync();
+          const uint32_t dO = tb + 4 * kTile + D * g;
+          const uint32_t pg = g * L::pgroup;
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            umma_f16(dO, smem_desc(sph + pg + ks * 256, 128, (kTile / 8) * 128),
+                     smem_desc(vb_ + ks * 2 * KC * 128, KC * 128, 128), idO, (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            umma_f16(dO, smem_desc(spl + pg + ks * 256, 128, (kTile / 8) * 128),
+                     smem_desc(vb_ + ks * 2 * KC * 128, KC * 128, 128), idO, 1u);
+          umma_commit(o_done + g);
+        }
+        umma_commit(vfree + bs);
+      };
+      bool bad = false;
+      copy_k(0);
+      copy_v(0);
+      if (ntiles > 1) {
+        copy_k(1);
+        copy_v(1);
+      }
+#pragma unroll 1
+      for (int it = 0; it < ntiles && !bad; ++it) {
+        const int bs = it & 1;
+        bad = !mbar_wait(kfull + bs, (it >> 1) & 1, p.err);
+        if (bad) break;
+        tc_fence_after_sync();
+        const uint32_t kb_h = sst + bs * T::bytes, kb_l = kb_h + T::kl;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t qg = sq + g * (kChunkM * D * 2);
+          const uint32_t dS = tb + kTile * (2 * bs + g);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_f16(dS, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(kb_h + ks * 256, 128, KC * 128), idS,
+                     ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_f16(dS, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(kb_l + ks * 256, 128, KC * 128), idS, 1u);
+          umma_commit(s_done + 2 * bs + g);
+        }
+        umma_commit(kfree + bs);
+        if (it >= 1) {
+          issue_pv(it - 1, bad);
+          if (bad) break;
+          if (it + 1 < ntiles) {  // tile it+1 goes into the stage of tile it-1
+            const int b1 = (it - 1) & 1, ph = ((it - 1) >> 1) & 1;
+            bad = !mbar_wait(kfree + b1, ph, p.err);
+            if (!bad) copy_k(it + 1);
+            bad = bad || !mbar_wait(vfree + b1, ph, p.err);
+            if (!bad) copy_v(it + 1);
+          }
+        }
+      }
+      if (!bad && ntiles > 0) issue_pv(ntiles - 1, bad);
+      // copies still in flight (only after a failed wait) must land before exit
+      if (bad) {
+        mbar_wait(kfull, 0, p.err, 1u << 16);
+        mbar_wait(vfull, 0, p.err, 1u << 16);
       }
     }
-    // groups of the thread's first and last token, both below n_q / G
-    pf.gA = min(t0 + row0, tq_end - 1) >> gs;
-    const int gB = min(t0 + row0 + kStep * (kJ - 1), tq_end - 1) >> gs;
-    if (p.km == 0) {
-      const uint8_t* recA = urec + static_cast<int64_t>(pf.gA) * p.rec_bytes + p.off_kscale;
-      const uint8_t* recB = urec + static_cast<int64_t>(gB) * p.rec_bytes + p.off_kscale;
-      pf.sa = *reinterpret_cast<const uint4*>(recA + c0 * 2);
-      pf.za = *reinterpret_cast<const uint4*>(recA + D * 2 + c0 * 2);
-      pf.sb = *reinterpret_cast<const uint4*>(recB + c0 * 2);
-      pf.zb = *reinterpret_cast<const uint4*>(recB + D * 2 + c0 * 2);
-    }
-    pf.tsz = __floats2half2_rn(0.0f, 0.0f);
-    if (tid < kTile && t0 + tid < tq_end) {
-      const int t = t0 + tid, gi = t >> gs, rr = t - (gi << gs);
-      pf.tsz = *reinterpret_cast<const __half2*>(urec + static_cast<int64_t>(gi) * p.rec_bytes + p.off_vsz + rr * 4);
-    }
-  };
-  if (ntq > 0) prefetch(0);
+    __syncwarp();
+  } else {
+    // ================= softmax threads (one row each)
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tS = tb + kTile * grp + lane_off;          // + 2 kTile for S buffer 1
+    const uint32_t tO = tb + 4 * kTile + D * grp + lane_off;  // this warp's lanes of O
+    const int r = tid;
+    const int lim = (r < rows) ? pos0 + i0 + r / p.gqa : last_pos;
+    float m = -INFINITY, l = 0.0f, zs = 0.0f;
+    bool failed = false;
+    uint8_t* prow_h = sm + L::ph + grp * L::pgroup;
+    uint8_t* prow_l = sm + L::pl + grp * L::pgroup;
 
 #pragma unroll 1
-  for (int it = 0; it < ntiles; ++it) {
-    const bool quant = it < ntq;
-    const int t0 = quant ? it * kTile : p.n_q + (it - ntq) * kTile;
-    const int tend = quant ? min(t0 + kTile, endQ) : min(t0 + kTile, endW);
-    // the previous P.V product has read its operands (and written O)
-    if (it > 0 && !failed) failed = !mbar_wait(barO, (it - 1) & 1, p.err) || !mbar_wait(barO + 1, (it - 1) & 1, p.err);
-
-    // ---- keys (hi + lo halves) and values of the tile into shared memory,
-    // from the words prefetched during the previous tile
-    if (quant) {
-      const int tq_end = min(t0 + kTile, p.n_q);
-      float sA[8], zA[8], sB[8], zB[8];
-      if (p.km == 0) {
-        const __half* psa = reinterpret_cast<const __half*>(&pf.sa);
-        const __half* pza = reinterpret_cast<const __half*>(&pf.za);
-        const __half* psb = reinterpret_cast<const __half*>(&pf.sb);
-        const __half* pzb = reinterpret_cast<const __half*>(&pf.zb);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          sA[e] = __half2float(psa[e]);
-          zA[e] = __half2float(pza[e]);
-          sB[e] = __half2float(psb[e]);
-          zB[e] = __half2float(pzb[e]);
-          if constexpr (KB == 3) {
-            if ((ku.two >> e) & 1u) {
-              sA[e] = __fdiv_rn(__fmul_rn(sA[e], 7.0f), 3.0f);
-              sB[e] = __fdiv_rn(__fmul_rn(sB[e], 7.0f), 3.0f);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kJ; ++j) {
-        const int nn = row0 + kStep * j;
-        const int t = t0 + nn;
-        const bool inB = (t >> gs) != pf.gA;
-        const uint32_t k0 = KB == 2 ? (pf.kw0[j] >> ku.sh0) : pf.kw0[j];
-        const uint32_t v0 = VB == 2 ? (pf.vw0[j] >> vu.sh0) : pf.vw0[j];
-        uint32_t hw[4], lw[4], vh[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          float kv[2];
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            float s, z;
-            if (p.km == 0) {
-              s = inB ? sB[e + q2] : sA[e + q2];
-              z = inB ? zB[e + q2] : zA[e + q2];
-            } else {
-              const float2 sz = __half22float2(pf.ksz[j]);
-              s = sz.x;
-              z = sz.y;
-              if constexpr (KB == 3) {
-                if ((ku.two >> (e + q2)) & 1u) s = __fdiv_rn(__fmul_rn(s, 7.0f), 3.0f);
-              }
-            }
-            kv[q2] = fmaf(code_f32(ku.get(k0, pf.kw1[j], e + q2)), s, z);
-          }
-          split_hi_lo(kv[0], kv[1], hw[e / 2], lw[e / 2]);
-          // value codes (< 1024) as exact fp16 integers: (1024 + code) - 1024
-          uint32_t c_lo = vu.get(v0, pf.vw1[j], e), c_hi = vu.get(v0, pf.vw1[j], e + 1);
-          if constexpr (VB == 3) {
-            if ((vu.two >> e) & 1u) c_lo *= 7u;
-            if ((vu.two >> (e + 1)) & 1u) c_hi *= 7u;
-          }
-          const uint32_t mag = 0x64006400u | c_lo | (c_hi << 16);
-          vh[e / 2] = h2_as_u32(__hsub2(u32_as_h2(mag), __float2half2_rn(1024.0f)));
-        }
-        const bool live = t < tq_end;
-        const uint32_t off = core_off(nn, c0, KC);
-        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sm + L::kh + off) = live ? make_uint4(hw[0], hw[1], hw[2], hw[3]) : zero;
-        *reinterpret_cast<uint4*>(sm + L::kl + off) = live ? make_uint4(lw[0], lw[1], lw[2], lw[3]) : zero;
-        *reinterpret_cast<uint4*>(sm + L::v + off) = live ? make_uint4(vh[0], vh[1], vh[2], vh[3]) : zero;
-      }
-      if (tid < kTile) {
-        const bool vis = t0 + tid < tend;
-        tok_s[tid] = vis ? __low2float(pf.tsz) : 0.0f;
-        tok_z[tid] = vis ? __high2float(pf.tsz) : 0.0f;
-      }
-    } else {
-      const int tw_end = min(t0 + kTile, p.T);
-      uint4 kr[kJ], vr[kJ];
-#pragma unroll
-      for (int j = 0; j < kJ; ++j) {
-        const int t = t0 + row0 + kStep * j;
-        kr[j] = vr[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (t < tw_end) {
-          const int slot = t % p.R;
-          const int64_t off = static_cast<int64_t>(slot) * D + ((kc ^ (slot & 7)) * 8);
-          kr[j] = *reinterpret_cast<const uint4*>(rk + off);
-          vr[j] = *reinterpret_cast<const uint4*>(rv + off);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kJ; ++j) {
-        const uint32_t off = core_off(row0 + kStep * j, c0, KC);
-        *reinterpret_cast<uint4*>(sm + L::kh + off) = kr[j];
-        *reinterpret_cast<uint4*>(sm + L::kl + off) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sm + L::v + off) = vr[j];
-      }
-    }
-    if (!quant && tid < kTile) {
-      tok_s[tid] = t0 + tid < tend ? 1.0f : 0.0f;
-      tok_z[tid] = 0.0f;
-    }
-    // prefetch the next quantized tile's words; they land during this tile's MMAs and softmax
-    if (it + 1 < ntq) prefetch((it + 1) * kTile);
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    failed = __syncthreads_or(failed);
-
-    // ---- S = Q K^T (hi, then lo), group 0 then group 1
-    if (tid == 0 && !failed) {
+    for (int it = 0; it < ntiles; ++it) {
+      const bool quant = it < ntq;
+      const int t0 = quant ? it * kTile : p.n_q + (it - ntq) * kTile;
+      const int tend = quant ? min(t0 + kTile, endQ) : min(t0 + kTile, endW);
+      const int bs = it & 1;
+      // scores of tile it, its values' pairs, and this group's P.V of tile it-1 (P and O reuse)
+      if (!failed) failed = !mbar_wait(s_done + 2 * bs + grp, (it >> 1) & 1, p.err);
+      if (!failed) failed = !mbar_wait(vfull + bs, (it >> 1) & 1, p.err);
+      if (it >= 1 && !failed) failed = !mbar_wait(o_done + grp, (it - 1) & 1, p.err);
       tc_fence_after_sync();
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const uint32_t qg = sq + g * (kChunkM * D * 2);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma_f16(tb + kTile * g, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(skh + ks * 256, 128, KC * 128),
-                   idS, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma_f16(tb + kTile * g, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(skl + ks * 256, 128, KC * 128),
-                   idS, 1u);
-        umma_commit(barS + g);
-      }
-    }
-    if (!failed) failed = !mbar_wait(barS + grp, it & 1, p.err);
-    tc_fence_after_sync();
+      const uint32_t tSb = tS + 2 * kTile * bs;
+      const __half2* szr = reinterpret_cast<const __half2*>(sm + L::stage + bs * T::bytes + T::sz);
 
-    // ---- online softmax of this thread's row
-    float x[kTile];
+      // ---- online softmax of this thread's row: two passes over its scores
+      // in tensor memory (the max, then the probabilities 32 at a time)
+      // tokens t0 .. t0 + nvis - 1 are visible to this row
+      const int nvis = min(tend, lim + 1) - t0;
+      const bool full = __all_sync(0xffffffffu, nvis >= kTile);
+      float mx = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < kTile; c += 16) {
-      uint32_t rr[16];
-      tmem_ld16(tS + c, rr);
-      tmem_ld_wait(rr);
+      for (int c = 0; c < kTile; c += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tSb + c, rr);
+        tmem_ld_wait(rr);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) x[c + j] = __uint_as_float(rr[j]);
-    }
-    // tokens t0 .. t0 + nvis - 1 are visible to this row
-    const int nvis = min(tend, lim + 1) - t0;
-    float mx = -INFINITY;
-    if (__all_sync(0xffffffffu, nvis >= kTile)) {
-#pragma unroll
-      for (int j = 0; j < kTile; ++j) mx = fmaxf(mx, x[j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < kTile; ++j) {
-        x[j] = j < nvis ? x[j] : -INFINITY;
-        mx = fmaxf(mx, x[j]);
+        for (int j = 0; j < 16; ++j) mx = fmaxf(mx, (full || c + j < nvis) ? __uint_as_float(rr[j]) : -INFINITY);
       }
-    }
-    // scores are raw q.k; the log2-domain max is m, in units of alpha * q.k
-    mx *= p.alpha;
-    const bool need = mx > m + 8.0f;
-    float f = 1.0f;
-    if (need) {
-      f = ex2(m - mx);
-      m = mx;
-    }
-    const float nm = -m;
-    l *= f;
-    zs *= f;
-    // O *= f where the max moved; 3-bit values: divide the 2-bit-field
-    // columns by 3 when the quantized tiles end
-    const bool third = VB == 3 && it == ntq && ntq > 0;
-    if (it > 0 && (__any_sync(0xffffffffu, need) || third)) {
+      // scores are raw q.k; the log2-domain max is m, in units of alpha * q.k
+      mx *= p.alpha;
+      const bool need = mx > m + 8.0f;
+      float f = 1.0f;
+      if (need) {
+        f = ex2(m - mx);
+        m = mx;
+      }
+      const float nm = -m;
+      l *= f;
+      zs *= f;
+      // O *= f where the max moved; 3-bit values: divide the 2-bit-field
+      // columns by 3 when the quantized tiles end
+      const bool third = p.vb == 3 && it == ntq && ntq > 0;
+      if (it > 0 && (__any_sync(0xffffffffu, need) || third)) {
 #pragma unroll 1
-      for (int c = 0; c < D; c += 16) {
-        uint32_t o[16];
-        tmem_ld16(tO + c, o);
-        tmem_ld_wait(o);
+        for (int c = 0; c < D; c += 16) {
+          uint32_t o[16];
+          tmem_ld16(tO + c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float g = f;
+            if (third && (c + j) % 11 == 10) g = __fdiv_rn(g, 3.0f);
+            o[j] = __float_as_uint(__uint_as_float(o[j]) * g);
+          }
+          tmem_st16(tO + c, o);
+        }
+        tmem_st_wait();
+      }
+      float ls = 0.0f, zsum = 0.0f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t ra[16], rb[16];
+        tmem_ld16(tSb + 32 * half, ra);
+        tmem_ld16(tSb + 32 * half + 16, rb);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int jj = 32 * half + j;
+          const float2 sz0 = __half22float2(szr[jj]), sz1 = __half22float2(szr[jj + 1]);
+          const float x0 = j < 16 ? __uint_as_float(ra[j]) : __uint_as_float(rb[j - 16]);
+          const float x1 = j < 16 ? __uint_as_float(ra[j + 1]) : __uint_as_float(rb[j - 15]);
+          const float p0 = ex2(fmaf((full || jj < nvis) ? x0 : -INFINITY, p.alpha, nm));
+          const float p1 = ex2(fmaf((full || jj + 1 < nvis) ? x1 : -INFINITY, p.alpha, nm));
+          ls += p0 + p1;
+          zsum = fmaf(p0, sz0.y, fmaf(p1, sz1.y, zsum));
+          split_hi_lo(p0 * sz0.x, p1 * sz1.x, hi[j / 2], lo[j / 2]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t off = core_off(r & 127, 32 * half + 8 * cc, kTile / 8);
+          *reinterpret_cast<uint4*>(prow_h + off) = make_uint4(hi[4 * cc], hi[4 * cc + 1], hi[4 * cc + 2], hi[4 * cc + 3]);
+          *reinterpret_cast<uint4*>(prow_l + off) = make_uint4(lo[4 * cc], lo[4 * cc + 1], lo[4 * cc + 2], lo[4 * cc + 3]);
+        }
+      }
+      l += ls;
+      zs += zsum;
+      // P' visible to the tensor core, TMEM reads and the O rescale ordered
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(p_full + grp);
+    }
+
+    // ---- epilogue: out = (O + zs) / l
+    if (!failed && ntiles > 0) failed = !mbar_wait(o_done + grp, (ntiles - 1) & 1, p.err);
+    tc_fence_after_sync();
+    const bool third = p.vb == 3 && ntw == 0;
+    const float inv = 1.0f / l;
+    float* orow = nullptr;
+    if (r < rows) {
+      const int i = i0 + r / p.gqa, hh = r % p.gqa;
+      orow = p.out + ((static_cast<int64_t>(b) * p.Hq + hk * p.gqa + hh) * p.n + i) * D;
+    }
+#pragma unroll 1
+    for (int c = 0; c < D; c += 16) {
+      uint32_t o[16];
+      tmem_ld16(tO + c, o);
+      tmem_ld_wait(o);
+      if (orow) {
+        float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float g = f;
-          if (third && (c + j) % 11 == 10) g = __fdiv_rn(g, 3.0f);
-          o[j] = __float_as_uint(__uint_as_float(o[j]) * g);
+          float a = __uint_as_float(o[j]);
+          if (third && (c + j) % 11 == 10) a = __fdiv_rn(a, 3.0f);
+          v[j] = (a + zs) * inv;
         }
-        tmem_st16(tO + c, o);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<float4*>(orow + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
       }
-      tmem_st_wait();
-    }
-    float ls = 0.0f, zsum = 0.0f;
-    uint32_t hi[kTile / 2], lo[kTile / 2];
-#pragma unroll
-    for (int j = 0; j < kTile; j += 2) {
-      const float p0 = ex2(fmaf(x[j], p.alpha, nm)), p1 = ex2(fmaf(x[j + 1], p.alpha, nm));
-      const float2 s2 = *reinterpret_cast<const float2*>(tok_s + j);
-      const float2 z2 = *reinterpret_cast<const float2*>(tok_z + j);
-      ls += p0 + p1;
-      zsum = fmaf(p0, z2.x, fmaf(p1, z2.y, zsum));
-      split_hi_lo(p0 * s2.x, p1 * s2.y, hi[j / 2], lo[j / 2]);
-    }
-    l += ls;
-    zs += zsum;
-#pragma unroll
-    for (int cc = 0; cc < kTile / 8; ++cc) {
-      *reinterpret_cast<uint4*>(sm + L::ph + grp * L::pgroup + core_off(r & 127, 8 * cc, kTile / 8)) =
-          make_uint4(hi[4 * cc], hi[4 * cc + 1], hi[4 * cc + 2], hi[4 * cc + 3]);
-      *reinterpret_cast<uint4*>(sm + L::pl + grp * L::pgroup + core_off(r & 127, 8 * cc, kTile / 8)) =
-          make_uint4(lo[4 * cc], lo[4 * cc + 1], lo[4 * cc + 2], lo[4 * cc + 3]);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    group_sync(1 + grp);
-
-    // ---- O += P' C (hi, then lo) of this group; C token-major (MN-major B)
-    if ((tid & 127) == 0 && !failed) {
-      tc_fence_after_sync();
-      const uint32_t dO = tb + 2 * kTile + D * grp;
-      const uint32_t pg = grp * L::pgroup;
-#pragma unroll
-      for (int ks = 0; ks < kTile / 16; ++ks)
-        umma_f16(dO, smem_desc(sph + pg + ks * 256, 128, (kTile / 8) * 128),
-                 smem_desc(sv + ks * 2 * KC * 128, KC * 128, 128), idO, (it > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-      for (int ks = 0; ks < kTile / 16; ++ks)
-        umma_f16(dO, smem_desc(spl + pg + ks * 256, 128, (kTile / 8) * 128),
-                 smem_desc(sv + ks * 2 * KC * 128, KC * 128, 128), idO, 1u);
-      umma_commit(barO + grp);
-    }
-  }
-
-  // ---- epilogue: out = (O + zs) / l
-  if (!failed) failed = !mbar_wait(barO + grp, (ntiles - 1) & 1, p.err);
-  tc_fence_after_sync();
-  const bool third = VB == 3 && ntw == 0;
-  const float inv = 1.0f / l;
-  float* orow = nullptr;
-  if (r < rows) {
-    const int i = i0 + r / p.gqa, hh = r % p.gqa;
-    orow = p.out + ((static_cast<int64_t>(b) * p.Hq + hk * p.gqa + hh) * p.n + i) * D;
-  }
-#pragma unroll 1
-  for (int c = 0; c < D; c += 16) {
-    uint32_t o[16];
-    tmem_ld16(tO + c, o);
-    tmem_ld_wait(o);
-    if (orow) {
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float a = __uint_as_float(o[j]);
-        if (third && (c + j) % 11 == 10) a = __fdiv_rn(a, 3.0f);
-        v[j] = (a + zs) * inv;
-      }
-#pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        *reinterpret_cast<float4*>(orow + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
     }
   }
   tc_fence_before_sync();
@@ -522,8 +604,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1) chunk_attn_kernel(ChunkParam
 }
 
 template <int KB, int VB, int D>
-ChunkKernel chunk_make() {
-  return ChunkKernel{chunk_attn_kernel<KB, VB, D>, ChunkSmem<D>::bytes};
+ChunkDequant chunk_dequant_make() {
+  return ChunkDequant{chunk_dequant_kernel<KB, VB, D>};
 }
 
 }  // namespace kvq

@@ -1,14 +1,15 @@
-// Chunk-attention instantiations for 2-bit keys (all value widths, head_dim 64/128).
+// Dequantize-pass instantiations of the chunk attention for 2-bit keys
+// (all value widths, head_dim 64/128).
 #include "kvq_chunk.cuh"
 
 namespace kvq {
 
-ChunkKernel chunk_get_k2(int vb, int D) {
+ChunkDequant chunk_dequant_get_k2(int vb, int D) {
 #define E(VB) \
-  if (vb == VB) return D == 128 ? chunk_make<2, VB, 128>() : chunk_make<2, VB, 64>();
+  if (vb == VB) return D == 128 ? chunk_dequant_make<2, VB, 128>() : chunk_dequant_make<2, VB, 64>();
   E(2) E(3) E(4) E(8)
 #undef E
-  return ChunkKernel{nullptr, 0};
+  return ChunkDequant{nullptr};
 }
 
 }  // namespace kvq

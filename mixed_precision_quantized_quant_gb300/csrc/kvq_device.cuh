@@ -99,6 +99,8 @@ struct ChunkParams {
   int off_kscale;         // record offset of the key (scale, zero) part
   int off_vsz;            // record offset of the value (scale, zero) pairs
   float alpha;            // log2(e) / sqrt(D)
+  uint8_t* ws;            // workspace: dequantized tiles, ws_tiles per unit
+  int ws_tiles;
 };
 
 // ---------------------------------------------------------------- PTX helpers

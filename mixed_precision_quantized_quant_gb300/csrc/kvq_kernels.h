@@ -29,19 +29,21 @@ struct DecodeKernel {
 DecodeKernel decode_select(int kb, int vb, int D, int gqa, int km);
 size_t decode_smem_bytes(int kb, int vb, int D, int nt, int km, int warps);
 
-// Causal multi-query attention over the quantized cache (tensor-core MMAs
-// with accumulators in tensor memory), specialised on (k_bits, v_bits,
-// head_dim).  Prepares the kernel attributes on first use; launches grid
-// (ceil(n / qpb), units).
-struct ChunkKernel {
+// Causal multi-query attention over the quantized cache: a dequantize pass
+// (specialised on (k_bits, v_bits, head_dim)) writes every 64-token tile of
+// every unit into the workspace, then the attention kernel (specialised on
+// head_dim; tensor-core MMAs with accumulators in tensor memory) reads them.
+struct ChunkDequant {
   void (*fn)(ChunkParams);
-  uint32_t smem;  // dynamic shared memory per CTA
 };
-ChunkKernel chunk_get_k2(int vb, int D);
-ChunkKernel chunk_get_k3(int vb, int D);
-ChunkKernel chunk_get_k4(int vb, int D);
-ChunkKernel chunk_get_k8(int vb, int D);
-cudaError_t chunk_attn_launch(int kb, int vb, int D, const ChunkParams& p, int units, cudaStream_t s);
+ChunkDequant chunk_dequant_get_k2(int vb, int D);
+ChunkDequant chunk_dequant_get_k3(int vb, int D);
+ChunkDequant chunk_dequant_get_k4(int vb, int D);
+ChunkDequant chunk_dequant_get_k8(int vb, int D);
+// Bytes of one dequantized tile in the workspace.
+size_t chunk_tile_bytes(int D);
+// Both launches; `tiles` = the unit's tiles at the current length.
+cudaError_t chunk_attn_launch(int kb, int vb, int D, const ChunkParams& p, int units, int tiles, cudaStream_t s);
 // Queries of the n newest tokens that one CTA serves (256 (query, head) rows).
 int chunk_queries_per_cta(int gqa);
 

@@ -24,7 +24,7 @@ EXPORTS = (
     "kvq_cache_bytes", "kvq_create", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
     "kvq_layer_view_get", "kvq_equivalent_bits", "kvq_decode_bytes", "kvq_device_error",
     "kvq_destroy", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_chunk_attn",
-    "kvq_selftest_bounded_wait",
+    "kvq_selftest_bounded_wait", "kvq_chunk_workspace_bytes",
 )
 
 
@@ -82,8 +82,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.kvq_decode_attn.restype = ctypes.c_int
     L.kvq_decode_attn_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, vp]
     L.kvq_decode_attn_noalloc.restype = ctypes.c_int
-    L.kvq_chunk_attn.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp]
+    L.kvq_chunk_attn.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
     L.kvq_chunk_attn.restype = ctypes.c_int
+    L.kvq_chunk_workspace_bytes.argtypes = [vp]
+    L.kvq_chunk_workspace_bytes.restype = ctypes.c_size_t
     L.kvq_decode_step.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                   ctypes.POINTER(vp), vp]
     L.kvq_decode_step.restype = ctypes.c_int
@@ -150,8 +152,13 @@ def kvq_decode_attn_noalloc(h: int, layer: int, q: int, out: int, stream: int) -
     _check(load().kvq_decode_attn_noalloc(h, layer, q, out, stream), "kvq_decode_attn_noalloc")
 
 
-def kvq_chunk_attn(h: int, layer: int, q: int, n_queries: int, out: int, stream: int) -> None:
-    _check(load().kvq_chunk_attn(h, layer, q, n_queries, out, stream), "kvq_chunk_attn")
+def kvq_chunk_attn(h: int, layer: int, q: int, n_queries: int, out: int, workspace: int, workspace_bytes: int,
+                   stream: int) -> None:
+    _check(load().kvq_chunk_attn(h, layer, q, n_queries, out, workspace, workspace_bytes, stream), "kvq_chunk_attn")
+
+
+def kvq_chunk_workspace_bytes(h: int) -> int:
+    return int(load().kvq_chunk_workspace_bytes(h))
 
 
 def kvq_decode_step(h: int, K: Sequence[int], V: Sequence[int], q: Sequence[int], out: Sequence[int],
@@ -255,8 +262,11 @@ class KVQCache:
         shp = (self.B, self.Hq, n, self.D)
         if out is None:
             out = torch.empty(shp, dtype=torch.float32, device=q.device)
+        if getattr(self, "_chunk_ws", None) is None:  # allocated on first use, kept with the cache
+            self._chunk_ws = torch.empty(kvq_chunk_workspace_bytes(self.h), dtype=torch.uint8, device=self.buf.device)
         kvq_chunk_attn(self.h, layer, _dev_ptr(q, "q", torch.float16, shp), n,
-                       _dev_ptr(out, "out", torch.float32, shp), _stream_ptr(stream))
+                       _dev_ptr(out, "out", torch.float32, shp), int(self._chunk_ws.data_ptr()),
+                       self._chunk_ws.numel(), _stream_ptr(stream))
         return out
 
     def decode_step(self, K: List, V: List, q: List, out: List, stream=None) -> None:

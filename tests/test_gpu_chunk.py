@@ -117,9 +117,13 @@ def test_chunk_argument_errors():
     with pytest.raises(K.KVQError) as e:
         cache.chunk_attn(0, torch.zeros((1, 4, 11, 64), dtype=torch.float16, device="cuda"))
     assert e.value.status == 1  # more queries than tokens
+    ws = torch.empty(K.kvq_chunk_workspace_bytes(cache.h), dtype=torch.uint8, device="cuda")
     with pytest.raises(K.KVQError) as e:
-        K.kvq_chunk_attn(cache.h, 0, int(q.data_ptr()), 0, int(q.data_ptr()), 0)
+        K.kvq_chunk_attn(cache.h, 0, int(q.data_ptr()), 0, int(q.data_ptr()), int(ws.data_ptr()), ws.numel(), 0)
     assert e.value.status == 1
+    with pytest.raises(K.KVQError) as e:  # workspace one byte short
+        K.kvq_chunk_attn(cache.h, 0, int(q.data_ptr()), 1, int(q.data_ptr()), int(ws.data_ptr()), ws.numel() - 1, 0)
+    assert e.value.status == 4
     assert cache.device_error() == 0
     cache.close()
 
