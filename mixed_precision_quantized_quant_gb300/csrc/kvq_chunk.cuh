@@ -486,20 +486,27 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
       const uint32_t tSb = tS + 2 * kTile * bs;
       const __half2* szr = reinterpret_cast<const __half2*>(sm + L::stage + bs * T::bytes + T::sz);
 
-      // ---- online softmax of this thread's row: two passes over its scores
-      // in tensor memory (the max, then the probabilities 32 at a time)
+      // ---- online softmax of this thread's row: its 64 scores come from
+      // tensor memory in one batch of loads (a single wait)
       // tokens t0 .. t0 + nvis - 1 are visible to this row
       const int nvis = min(tend, lim + 1) - t0;
       const bool full = __all_sync(0xffffffffu, nvis >= kTile);
+      uint32_t x0[16], x1[16], x2[16], x3[16];
+      tmem_ld16(tSb, x0);
+      tmem_ld16(tSb + 16, x1);
+      tmem_ld16(tSb + 32, x2);
+      tmem_ld16(tSb + 48, x3);
+      tmem_ld_wait(x0);  // waits for all four
+      tmem_ld_wait(x1);
+      tmem_ld_wait(x2);
+      tmem_ld_wait(x3);
+      auto score = [&](int j) -> float {
+        const uint32_t v = j < 16 ? x0[j] : j < 32 ? x1[j - 16] : j < 48 ? x2[j - 32] : x3[j - 48];
+        return (full || j < nvis) ? __uint_as_float(v) : -INFINITY;
+      };
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTile; c += 16) {
-        uint32_t rr[16];
-        tmem_ld16(tSb + c, rr);
-        tmem_ld_wait(rr);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) mx = fmaxf(mx, (full || c + j < nvis) ? __uint_as_float(rr[j]) : -INFINITY);
-      }
+      for (int j = 0; j < kTile; ++j) mx = fmaxf(mx, score(j));
       // scores are raw q.k; the log2-domain max is m, in units of alpha * q.k
       mx *= p.alpha;
       const bool need = mx > m + 8.0f;
@@ -533,20 +540,13 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
       float ls = 0.0f, zsum = 0.0f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t ra[16], rb[16];
-        tmem_ld16(tSb + 32 * half, ra);
-        tmem_ld16(tSb + 32 * half + 16, rb);
-        tmem_ld_wait(ra);
-        tmem_ld_wait(rb);
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const int jj = 32 * half + j;
           const float2 sz0 = __half22float2(szr[jj]), sz1 = __half22float2(szr[jj + 1]);
-          const float x0 = j < 16 ? __uint_as_float(ra[j]) : __uint_as_float(rb[j - 16]);
-          const float x1 = j < 16 ? __uint_as_float(ra[j + 1]) : __uint_as_float(rb[j - 15]);
-          const float p0 = ex2(fmaf((full || jj < nvis) ? x0 : -INFINITY, p.alpha, nm));
-          const float p1 = ex2(fmaf((full || jj + 1 < nvis) ? x1 : -INFINITY, p.alpha, nm));
+          const float p0 = ex2(fmaf(score(jj), p.alpha, nm));
+          const float p1 = ex2(fmaf(score(jj + 1), p.alpha, nm));
           ls += p0 + p1;
           zsum = fmaf(p0, sz0.y, fmaf(p1, sz1.y, zsum));
           split_hi_lo(p0 * sz0.x, p1 * sz1.x, hi[j / 2], lo[j / 2]);
