@@ -369,9 +369,9 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
 
   if (warp == kChunkThreads / 32) {
     // ================= copy/MMA warp: its first thread issues every bulk
-    // copy and every MMA, in the order
-    //   S(it), then P.V(it-1), then the copies of tile it+1 into the stage
-    //   tile it-1 used (keys once S(it-1) is done, values once P.V(it-1) is)
+    // copy and every MMA.  Per tile it: S(it); the keys of tile it+1 into the
+    // other stage (freed by S(it-1)); the values and pairs of tile it into
+    // its stage (freed by P.V(it-2)); then P.V(it-1) once its softmax is done.
     if ((tid & 31) == 0) {
       const uint32_t sq = smem_u32(sm + L::q);
       const uint32_t sst = smem_u32(sm + L::stage);
@@ -415,10 +415,6 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
       bool bad = false;
       copy_k(0);
       copy_v(0);
-      if (ntiles > 1) {
-        copy_k(1);
-        copy_v(1);
-      }
 #pragma unroll 1
       for (int it = 0; it < ntiles && !bad; ++it) {
         const int bs = it & 1;
@@ -440,17 +436,20 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
           umma_commit(s_done + 2 * bs + g);
         }
         umma_commit(kfree + bs);
-        if (it >= 1) {
-          issue_pv(it - 1, bad);
+        // keys of tile it+1 into the other stage (its scores of tile it-1 are long done)
+        if (it + 1 < ntiles) {
+          if (it >= 1) bad = !mbar_wait(kfree + (bs ^ 1), ((it - 1) >> 1) & 1, p.err);
           if (bad) break;
-          if (it + 1 < ntiles) {  // tile it+1 goes into the stage of tile it-1
-            const int b1 = (it - 1) & 1, ph = ((it - 1) >> 1) & 1;
-            bad = !mbar_wait(kfree + b1, ph, p.err);
-            if (!bad) copy_k(it + 1);
-            bad = bad || !mbar_wait(vfree + b1, ph, p.err);
-            if (!bad) copy_v(it + 1);
-          }
+          copy_k(it + 1);
         }
+        // values and pairs of tile it (tile 0's were copied first); the stage's
+        // P.V of tile it-2 was issued an iteration ago
+        if (it >= 1) {
+          if (it >= 2) bad = !mbar_wait(vfree + bs, ((it - 2) >> 1) & 1, p.err);
+          if (bad) break;
+          copy_v(it);
+        }
+        if (it >= 1) issue_pv(it - 1, bad);
       }
       if (!bad && ntiles > 0) issue_pv(ntiles - 1, bad);
       // copies still in flight (only after a failed wait) must land before exit
