@@ -192,7 +192,9 @@ size_t kvq_chunk_workspace_bytes(const kvq_handle* h);
  * above (n_tokens = 1).  The launches of a step do not depend on the cache
  * state, so after the first call with a given set of pointers the step is
  * replayed from a CUDA graph the handle keeps (it is re-captured when the
- * pointers change).  KVQ_ERR_CAPACITY if any layer is full. */
+ * pointers change).  Inside the graph the appends run on a forked stream:
+ * decode l waits for append l (and for decode l-1), so later layers' appends
+ * overlap earlier layers' decodes.  KVQ_ERR_CAPACITY if any layer is full. */
 kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V,
                            const void* const* q, float* const* out, void* stream);
 

@@ -118,6 +118,10 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
 struct StepGraph {
   std::vector<const void*> key;
   cudaGraphExec_t exec = nullptr;
+  // capture helpers: the appends run on a forked stream, each decode waits
+  // for its own layer's append only
+  cudaStream_t aux = nullptr;
+  std::vector<cudaEvent_t> ev;  // [0]: fork, [1 + l]: append of layer l done
 };
 
 }  // namespace
@@ -404,10 +408,26 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
       h->graph.exec = nullptr;
     }
     std::vector<int64_t> saved = h->tokens;
+    if (!h->graph.aux) {
+      if (cudaStreamCreateWithFlags(&h->graph.aux, cudaStreamNonBlocking) != cudaSuccess) return KVQ_ERR_CUDA;
+      h->graph.ev.assign(L + 1, nullptr);
+      for (auto& e : h->graph.ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return KVQ_ERR_CUDA;
+    }
+    cudaStream_t a = h->graph.aux;
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return KVQ_ERR_CUDA;
     kvq_status st = KVQ_OK;
+    // appends of all layers on the forked stream (they touch only their own
+    // layer's records, ring and counters); decode l waits for append l and
+    // runs after decode l-1 (they share the split workspace)
+    if (cudaEventRecord(h->graph.ev[0], s) != cudaSuccess || cudaStreamWaitEvent(a, h->graph.ev[0], 0) != cudaSuccess)
+      st = KVQ_ERR_CUDA;
     for (int l = 0; l < L && st == KVQ_OK; ++l) {
-      st = launch_append(h, l, K[l], V[l], 1, s);
+      st = launch_append(h, l, K[l], V[l], 1, a);
+      if (st == KVQ_OK && cudaEventRecord(h->graph.ev[1 + l], a) != cudaSuccess) st = KVQ_ERR_CUDA;
+    }
+    for (int l = 0; l < L && st == KVQ_OK; ++l) {
+      if (cudaStreamWaitEvent(s, h->graph.ev[1 + l], 0) != cudaSuccess) st = KVQ_ERR_CUDA;
       if (st == KVQ_OK) st = launch_decode(h, l, q[l], out[l], s);
     }
     cudaGraph_t graph = nullptr;
@@ -500,6 +520,9 @@ kvq_status kvq_selftest_bounded_wait(kvq_handle* h, void* stream) {
 
 kvq_status kvq_destroy(kvq_handle* h) {
   if (!h) return KVQ_ERR_ARG;
+  for (cudaEvent_t e : h->graph.ev)
+    if (e) cudaEventDestroy(e);
+  if (h->graph.aux) cudaStreamDestroy(h->graph.aux);
   if (h->graph.exec) cudaGraphExecDestroy(h->graph.exec);
   delete h;
   return KVQ_OK;
