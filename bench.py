@@ -352,7 +352,7 @@ def run_gpu(args):
         h_k.copy_(kin.cpu())
         h_v.copy_(vin.cpu())
         h_q.copy_(qin.cpu())
-        h_out = torch.empty((L, B, Hq, D), dtype=torch.float32).pin_memory()
+        h_out = torch.empty((2, L, B, Hq, D), dtype=torch.float32).pin_memory()  # two readback slots
         e2e_cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, cap, device=dev)
         with torch.cuda.stream(stream):
             for l in range(L):
@@ -360,23 +360,59 @@ def run_gpu(args):
                 e2e_cache.append(l, k, v, stream=stream)
                 del k, v
             stream.synchronize()
+        # Pipelined through the public API: step s+1's inputs are uploaded
+        # from pinned memory on a copy stream while step s computes, and step
+        # s's outputs are staged on the device and read back while step s+1
+        # runs.  Every step still copies its inputs in and its outputs out.
+        copy = torch.cuda.Stream(device=dev)
+        st_k = [torch.empty_like(k_cur) for _ in range(2)]
+        st_v = [torch.empty_like(v_cur) for _ in range(2)]
+        st_q = [torch.empty_like(q_cur) for _ in range(2)]
+        st_o = [torch.empty_like(outs) for _ in range(2)]
+        up = [torch.cuda.Event() for _ in range(2)]     # inputs of a slot uploaded
+        used = [torch.cuda.Event() for _ in range(2)]   # inputs of a slot consumed by the step
+        done = [torch.cuda.Event() for _ in range(2)]   # outputs of a slot staged
+        down = [torch.cuda.Event() for _ in range(2)]   # outputs of a slot read back
 
-            def e2e_step(s):
-                k_cur.copy_(h_k[s], non_blocking=True)
-                v_cur.copy_(h_v[s], non_blocking=True)
-                q_cur.copy_(h_q[s], non_blocking=True)
-                e2e_cache.decode_step(Ks, Vs, Qs, Os, stream=stream)
-                h_out.copy_(outs, non_blocking=True)
-                stream.synchronize()
+        def upload(s):
+            b = s & 1
+            with torch.cuda.stream(copy):
+                copy.wait_event(used[b])
+                st_k[b].copy_(h_k[s], non_blocking=True)
+                st_v[b].copy_(h_v[s], non_blocking=True)
+                st_q[b].copy_(h_q[s], non_blocking=True)
+                up[b].record(copy)
 
-            for s in range(warm):
-                e2e_step(s)
-            _barrier(world)
-            t0 = time.perf_counter()
-            for s in range(warm, warm + steps):
-                e2e_step(s)
-            t1 = time.perf_counter()
-            _barrier(world)
+        def run(s, n):
+            upload(s)
+            for i in range(s, s + n):
+                b = i & 1
+                if i + 1 < s + n:
+                    upload(i + 1)
+                with torch.cuda.stream(stream):
+                    stream.wait_event(up[b])
+                    k_cur.copy_(st_k[b], non_blocking=True)
+                    v_cur.copy_(st_v[b], non_blocking=True)
+                    q_cur.copy_(st_q[b], non_blocking=True)
+                    used[b].record(stream)
+                    e2e_cache.decode_step(Ks, Vs, Qs, Os, stream=stream)
+                    stream.wait_event(down[b])  # the slot's previous readback has finished
+                    st_o[b].copy_(outs, non_blocking=True)
+                    done[b].record(stream)
+                with torch.cuda.stream(copy):
+                    copy.wait_event(done[b])
+                    h_out[b].copy_(st_o[b], non_blocking=True)  # slot b's previous result was synced
+                    down[b].record(copy)
+                if i >= s + 1:
+                    down[(i - 1) & 1].synchronize()  # step i-1's result is on the host
+            down[(s + n - 1) & 1].synchronize()
+
+        run(0, warm)
+        _barrier(world)
+        t0 = time.perf_counter()
+        run(warm, steps)
+        t1 = time.perf_counter()
+        _barrier(world)
         e2e_s = _max_over_ranks(t1 - t0, world)
         e2e_tps = world * B * steps / e2e_s
     h2d = L * (2 * B * Hkv * D * 2 + B * Hq * D * 2)
@@ -601,23 +637,54 @@ def run_chunk(args):
     e2e = None
     if not args.no_e2e:
         h_q = q.cpu().pin_memory()
-        h_out = torch.empty((B, Hq, n, D), dtype=torch.float32).pin_memory()
-        q_dev = torch.empty_like(q)
-        with torch.cuda.stream(stream):
-            def e2e_step():
-                for l in range(L):
-                    q_dev.copy_(h_q, non_blocking=True)
-                    cache.chunk_attn(l, q_dev, out, stream=stream)
-                    h_out.copy_(out, non_blocking=True)
-                stream.synchronize()
-            for _ in range(min(args.warmup, 3)):
-                e2e_step()
-            _barrier(world)
-            t0 = time.perf_counter()
-            for _ in range(args.steps):
-                e2e_step()
-            t1 = time.perf_counter()
-            _barrier(world)
+        h_out = torch.empty((2, B, Hq, n, D), dtype=torch.float32).pin_memory()  # two readback slots
+        # Pipelined: layer l+1's queries are uploaded on a copy stream while
+        # layer l computes, and layer l's outputs are read back while layer
+        # l+1 computes (two device slots each); every layer still copies its
+        # queries in and its outputs out.
+        copy = torch.cuda.Stream(device=dev)
+        q_dev = [torch.empty_like(q) for _ in range(2)]
+        o_dev = [torch.empty_like(out) for _ in range(2)]
+        up = [torch.cuda.Event() for _ in range(2)]
+        used = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        down = [torch.cuda.Event() for _ in range(2)]
+
+        def upload(i):
+            b = i & 1
+            with torch.cuda.stream(copy):
+                copy.wait_event(used[b])
+                q_dev[b].copy_(h_q, non_blocking=True)
+                up[b].record(copy)
+
+        def e2e_step():
+            upload(0)
+            for l in range(L):
+                b = l & 1
+                if l + 1 < L:
+                    upload(l + 1)
+                with torch.cuda.stream(stream):
+                    stream.wait_event(up[b])
+                    stream.wait_event(down[b])  # the slot's previous readback has finished
+                    cache.chunk_attn(l, q_dev[b], o_dev[b], stream=stream)
+                    used[b].record(stream)
+                    done[b].record(stream)
+                with torch.cuda.stream(copy):
+                    copy.wait_event(done[b])
+                    h_out[b].copy_(o_dev[b], non_blocking=True)
+                    down[b].record(copy)
+                if l >= 1:
+                    down[(l - 1) & 1].synchronize()  # layer l-1's result is on the host
+            down[(L - 1) & 1].synchronize()
+
+        for _ in range(min(args.warmup, 3)):
+            e2e_step()
+        _barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        t1 = time.perf_counter()
+        _barrier(world)
         e2e_s = _max_over_ranks(t1 - t0, world)
         e2e = {"value": round(world * L * flops_layer * args.steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": L * q.numel() * 2, "d2h_bytes_per_step": L * out.numel() * 4}
