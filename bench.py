@@ -175,6 +175,38 @@ class OracleSampler:
                      f"precision pair) at context {w.context}; per-unit time x {U} units x "
                      f"{w.num_layers} layers")
 
+    def errors(self):
+        """Quantization error of each distinct precision pair on the sampled
+        unit (KVTuner A3's metrics): e_k, e_v over the quantized tokens,
+        e_a = mean |a - a_hat| of the attention weights and e_o of the output
+        for the first query, against fp64 over the fp16 K and V."""
+        import numpy as np
+        from oracle import kvq_oracle as O
+        out = {}
+        for l in self.layers:
+            kb, vb = self.w.layers[l][:2]
+            ora = self.caches[l]
+            kh, vh = ora.dequantized(0)
+            k, v = (x.numpy()[0, 0].astype(np.float64) for x in self.W.gen_kv(self.unit_w, l, 0, self.w.context))
+            nq = ora.n_q
+            q = self.W.gen_q(self.unit_w, l, 0).numpy()[0].astype(np.float64)
+            T = kh.shape[0]
+            ea, o_ref, o_hat = [], [], []
+            for h in range(q.shape[0]):
+                def weights(kk):
+                    x = kk[:T] @ q[h] / np.sqrt(kk.shape[1])
+                    e = np.exp(x - x.max())
+                    return e / e.sum()
+                a, ah = weights(k), weights(kh)
+                ea.append(np.abs(a - ah).mean())
+                o_ref.append(O.attention_fp64(q[h], k[:T], v[:T]))
+                o_hat.append(O.attention_fp64(q[h], kh, vh))
+            out[f"K{kb}V{vb}"] = {"e_k": round(O.rel_error(k[:nq], kh[:nq]), 5),
+                                  "e_v": round(O.rel_error(v[:nq], vh[:nq]), 5),
+                                  "e_a": float(f"{np.mean(ea):.3e}"),
+                                  "e_o": round(O.rel_error(np.stack(o_ref), np.stack(o_hat)), 5)}
+        return out
+
     def step(self) -> float:
         """Seconds one full decode step would take, from one timed unit-step
         per distinct layer type."""
@@ -191,15 +223,16 @@ class OracleSampler:
 
 
 def oracle_sample(w, budget_s: float = 12.0):
-    """(tokens/s, seconds per full step, description) from repeated sampled
-    steps until about budget_s seconds of oracle work."""
+    """(tokens/s, seconds per full step, description, quantization errors)
+    from repeated sampled steps until about budget_s seconds of oracle work."""
     smp = OracleSampler(w)
+    errors = smp.errors()
     t_start = time.perf_counter()
     steps = []
     while len(steps) < 3 or (time.perf_counter() - t_start < budget_s and len(steps) < 64):
         steps.append(smp.step())
     step_s = statistics.median(steps)
-    return w.batch / step_s, step_s, smp.desc + f"; median over {len(steps)} sampled steps"
+    return w.batch / step_s, step_s, smp.desc + f"; median over {len(steps)} sampled steps", errors
 
 
 # ----------------------------------------------------------------------------
@@ -455,9 +488,13 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tps, step_s, desc = oracle_sample(w, budget_s=args.cpu_budget)
+        tps, step_s, desc, errors = oracle_sample(w, budget_s=args.cpu_budget)
         result["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                   "sample": desc, "seconds_per_step": round(step_s, 2)}
+        result["quant_error"] = {"per_pair": errors,
+                                 "of": "one sampled (batch, kv head) unit at full context, first query; "
+                                       "e_k, e_v over its quantized tokens, e_a and e_o against fp64 "
+                                       "attention over the fp16 K and V (KVTuner A3)"}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

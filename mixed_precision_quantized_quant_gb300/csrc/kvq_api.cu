@@ -11,10 +11,18 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/kvq.h"
 #include "kvq_kernels.h"
 
 namespace {
+
+// NVTX range around a C-ABI call (a no-op unless a profiler is attached)
+struct Trace {
+  explicit Trace(const char* name) { nvtxRangePushA(name); }
+  ~Trace() { nvtxRangePop(); }
+};
 
 using kvq::AppendParams;
 using kvq::DecodeParams;
@@ -296,6 +304,7 @@ size_t kvq_cache_bytes(const kvq_config* cfg) {
 }
 
 kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_handle** out) {
+  Trace trace("kvq_create");
   if (!out) return KVQ_ERR_ARG;
   *out = nullptr;
   Plan P;
@@ -341,6 +350,7 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
 }
 
 kvq_status kvq_append(kvq_handle* h, int layer, const void* K, const void* V, int n_tokens, void* stream) {
+  Trace trace("kvq_append");
   if (!h || layer < 0 || layer >= h->plan.L || n_tokens < 0) return KVQ_ERR_ARG;
   if (n_tokens == 0) return KVQ_OK;
   if (!K || !V) return KVQ_ERR_ARG;
@@ -350,6 +360,7 @@ kvq_status kvq_append(kvq_handle* h, int layer, const void* K, const void* V, in
 }
 
 kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, void* stream) {
+  Trace trace("kvq_decode_attn");
   if (!h || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
   if (!q || !out) return KVQ_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
@@ -365,6 +376,7 @@ size_t kvq_chunk_workspace_bytes(const kvq_handle* h) {
 
 kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries, float* out, void* workspace,
                           size_t workspace_bytes, void* stream) {
+  Trace trace("kvq_chunk_attn");
   if (!h || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
   if (!q || !out || !workspace) return KVQ_ERR_ARG;
   if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVQ_ERR_ALIGN;
@@ -377,6 +389,7 @@ kvq_status kvq_chunk_attn(kvq_handle* h, int layer, const void* q, int n_queries
 
 kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V, const void* const* q,
                            float* const* out, void* stream) {
+  Trace trace("kvq_decode_step");
   if (!h || !K || !V || !q || !out) return KVQ_ERR_ARG;
   const int L = h->plan.L;
   for (int l = 0; l < L; ++l) {
@@ -494,6 +507,7 @@ int64_t kvq_decode_bytes(const kvq_handle* h, int layer) {
 }
 
 kvq_status kvq_device_error(kvq_handle* h, int32_t* code, void* stream) {
+  Trace trace("kvq_device_error");
   if (!h || !code) return KVQ_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -505,6 +519,7 @@ kvq_status kvq_device_error(kvq_handle* h, int32_t* code, void* stream) {
 }
 
 kvq_status kvq_selftest_bounded_wait(kvq_handle* h, void* stream) {
+  Trace trace("kvq_selftest_bounded_wait");
   if (!h) return KVQ_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t before = 0;
@@ -519,6 +534,7 @@ kvq_status kvq_selftest_bounded_wait(kvq_handle* h, void* stream) {
 }
 
 kvq_status kvq_destroy(kvq_handle* h) {
+  Trace trace("kvq_destroy");
   if (!h) return KVQ_ERR_ARG;
   for (cudaEvent_t e : h->graph.ev)
     if (e) cudaEventDestroy(e);
@@ -576,6 +592,7 @@ kvq_status noalloc_scratch(uint8_t** out) {
 
 extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const void* q, float* out,
                                               void* stream) {
+  Trace trace("kvq_decode_attn_noalloc");
   if (!h || layer < 0 || layer >= h->plan.L) return KVQ_ERR_ARG;
   if (!q || !out) return KVQ_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
