@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
+# debug variant: every kernel checks its computed accesses against the buffers
+# it was given and records kErrBadAddress instead of touching memory outside them
+DEBUG_BUILD = os.path.join(ROOT, "_build", "debug")
+DEBUG_LIB = os.path.join(PKG, "libkvq_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 
@@ -46,8 +50,8 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str, obj: str, verbose: bool) -> str:
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, obj: str, verbose: bool, defines=()) -> str:
+    cmd = [nvcc(), *ARCH, *FLAGS, *defines, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -56,25 +60,29 @@ def _compile(src: str, obj: str, verbose: bool) -> str:
     return res.stderr
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    """Builds libkvq.so, or with debug=True libkvq_debug.so (compiled with
+    KVQ_DEBUG: device-side range checks of computed accesses)."""
+    bdir, lib = (DEBUG_BUILD, DEBUG_LIB) if debug else (BUILD, LIB)
+    defines = ("-DKVQ_DEBUG",) if debug else ()
+    os.makedirs(bdir, exist_ok=True)
     srcs = _sources()
     hdrs = _headers()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(bdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
     todo = [(s, o) for s, o in zip(srcs, objs) if force or _stale(o, [s, *hdrs])]
     if todo:
         with cf.ThreadPoolExecutor(max_workers=min(len(todo), os.cpu_count() or 4)) as ex:
-            logs = list(ex.map(lambda so: _compile(so[0], so[1], verbose), todo))
+            logs = list(ex.map(lambda so: _compile(so[0], so[1], verbose, defines), todo))
         if verbose:
             for (s, _), log in zip(todo, logs):
                 print(f"== {os.path.basename(s)}\n{log}", file=sys.stderr)
-    if force or todo or _stale(LIB, objs):
-        cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-lcudart"]
+    if force or todo or _stale(lib, objs):
+        cmd = [nvcc(), *ARCH, "-shared", "-o", lib, *objs, "-lcudart"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

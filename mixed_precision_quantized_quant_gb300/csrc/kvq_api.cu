@@ -182,6 +182,8 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   ap.tokens = unit_tokens(h, layer);
   ap.done_ctr = ctrl(h, layer);
   ap.err = errw(h);
+  ap.buf_lo = h->base;
+  ap.buf_hi = h->base + P.total;
   const size_t smem = kvq::append_smem_bytes(lp.kb, lp.vb, P.D, P.G, static_cast<int>(lp.rec_bytes));
   cudaError_t e = cudaSuccess;
   if (n == 1) {
@@ -233,6 +235,9 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   dp.rec_bytes = static_cast<int>(lp.rec_bytes);
   dp.grid = h->grid[layer];
   dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
+  dp.buf_lo = h->base;
+  dp.buf_hi = h->base + P.total;
+  dp.part_hi = reinterpret_cast<const uint8_t*>(dp.partials) + P.partial_floats * 4;
   const kvq::DecodeKernel& k = h->dec[layer];
   k.fn<<<h->grid[layer], k.threads, k.smem, s>>>(dp);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
@@ -276,6 +281,9 @@ kvq_status launch_chunk(kvq_handle* h, int layer, const void* q, int n, float* o
   cp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
   cp.ws = static_cast<uint8_t*>(ws);
   cp.ws_tiles = static_cast<int>(chunk_ws_tiles(P));
+  cp.ws_hi = cp.ws + static_cast<int64_t>(P.units) * cp.ws_tiles * static_cast<int64_t>(kvq::chunk_tile_bytes(P.D));
+  cp.buf_lo = h->base;
+  cp.buf_hi = h->base + P.total;
   const int tiles = (cp.n_q + 63) / 64 + (cp.T - cp.n_q + 63) / 64;
   if (kvq::chunk_attn_launch(lp.kb, lp.vb, P.D, cp, P.units, tiles, s) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
@@ -629,6 +637,9 @@ extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const vo
   dp.rec_bytes = static_cast<int>(lp.rec_bytes);
   dp.grid = grid;
   dp.alpha = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P.D)));
+  dp.buf_lo = h->base;
+  dp.buf_hi = h->base + P.total;
+  dp.part_hi = reinterpret_cast<const uint8_t*>(dp.partials) + partial_bytes;
   const kvq::DecodeKernel& k = h->dec[layer];
   k.fn<<<grid, k.threads, k.smem, s>>>(dp);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;

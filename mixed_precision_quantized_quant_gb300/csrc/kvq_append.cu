@@ -516,8 +516,9 @@ __device__ void write_residual(const AppendParams& p, int u, int64_t lo, int64_t
         const int rem = idx - tok * (2 * CH);
         __half* ring = rem >= CH ? p.res_v : p.res_k;
         const int slot = static_cast<int>((lo + tok) % p.R);
-        reinterpret_cast<uint4*>(ring + u * p.res_stride + static_cast<int64_t>(slot) * D)[(rem % CH) ^ (slot & 7)] =
-            v[r];
+        uint4* dst = reinterpret_cast<uint4*>(ring + u * p.res_stride + static_cast<int64_t>(slot) * D) +
+                     ((rem % CH) ^ (slot & 7));
+        if (in_range(dst, 16, p.buf_lo, p.buf_hi, p.err)) *dst = v[r];  // (checked in debug builds)
       }
     }
   }
@@ -559,6 +560,16 @@ __global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
       const int nring = T > t0 ? (T - t0 < p.G ? T - t0 : p.G) : 0;
       uint8_t* ks = smem + st * L.off_stage1;
       uint8_t* vs = ks + tile;
+      if (nring > 0) {
+        // (debug builds: ring rows outside the cache buffer are recorded; the
+        // stage's barrier completes without copies)
+        const int64_t r0 = u * p.res_stride + static_cast<int64_t>(t0 % p.R) * D;
+        const size_t rb = static_cast<size_t>(nring) * D * 2;
+        if (!in_range(p.res_k + r0, rb, p.buf_lo, p.buf_hi, p.err) || !in_range(p.res_v + r0, rb, p.buf_lo, p.buf_hi, p.err)) {
+          mbar_arrive(&bars[st]);
+          return;
+        }
+      }
       mbar_arrive_expect_tx(&bars[st], 2 * tile);
       if (nring > 0) {
         const int s0 = t0 % p.R;
@@ -601,7 +612,8 @@ __global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
       if (tid == 0) {
         fence_proxy_async_smem();
         uint8_t* dst = p.records + static_cast<int64_t>(u) * p.unit_rec_stride + static_cast<int64_t>(grp) * p.rec_bytes;
-        bulk_s2g(dst, smem + L.off_rec, static_cast<uint32_t>(p.rec_bytes));
+        if (in_range(dst, static_cast<size_t>(p.rec_bytes), p.buf_lo, p.buf_hi, p.err))  // debug builds
+          bulk_s2g(dst, smem + L.off_rec, static_cast<uint32_t>(p.rec_bytes));
         bulk_commit();
         const int jn = j + 2 * static_cast<int>(gridDim.x);
         if (jn < njobs) issue(jn, st);

@@ -135,11 +135,6 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
 // exact small integer code (< 1024) as fp32: 2^23 + code, minus 2^23
 __device__ __forceinline__ float code_f32(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
 
-// one arrival on an mbarrier (release: earlier writes are visible to its waiters)
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Unpack tile `blockIdx.x` of unit `blockIdx.y` into the workspace.
 template <int KB, int VB, int D>
@@ -156,6 +151,7 @@ __global__ void __launch_bounds__(kDequantThreads) chunk_dequant_kernel(ChunkPar
   const int tq_end = quant ? min(t0 + kTile, p.n_q) : min(t0 + kTile, p.T);  // tokens that exist
   const uint8_t* urec = p.records + static_cast<int64_t>(u) * p.unit_rec_stride;
   uint8_t* dst = p.ws + (static_cast<int64_t>(u) * p.ws_tiles + tile) * T::bytes;
+  if (!in_range(dst, T::bytes, p.ws, p.ws_hi, p.err)) return;  // debug builds (uniform over the CTA)
 
   // Thread (tid & 7) fills row tid & 7 of every core matrix it touches (8
   // consecutive threads write one whole 128-byte core matrix); its channel
@@ -184,6 +180,7 @@ __global__ void __launch_bounds__(kDequantThreads) chunk_dequant_kernel(ChunkPar
       if (t < tq_end) {
         const int gi = t >> gs, rr = t - (gi << gs);
         const uint8_t* rec = urec + static_cast<int64_t>(gi) * p.rec_bytes;
+        if (!in_range(rec, p.rec_bytes, p.buf_lo, p.buf_hi, p.err)) continue;  // debug builds
         const uint32_t* krow = reinterpret_cast<const uint32_t*>(rec) + rr * p.wk;
         const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec) + voff + rr * p.wv;
         kw0[j] = krow[ku.wa];
@@ -201,6 +198,8 @@ __global__ void __launch_bounds__(kDequantThreads) chunk_dequant_kernel(ChunkPar
     if (p.km == 0) {
       const uint8_t* recA = urec + static_cast<int64_t>(gA) * p.rec_bytes + p.off_kscale;
       const uint8_t* recB = urec + static_cast<int64_t>(gB) * p.rec_bytes + p.off_kscale;
+      if (!in_range(recA, 4 * D, p.buf_lo, p.buf_hi, p.err) || !in_range(recB, 4 * D, p.buf_lo, p.buf_hi, p.err))
+        return;  // debug builds
       const uint4 sa = *reinterpret_cast<const uint4*>(recA + c0 * 2);
       const uint4 za = *reinterpret_cast<const uint4*>(recA + D * 2 + c0 * 2);
       const uint4 sb = *reinterpret_cast<const uint4*>(recB + c0 * 2);
@@ -286,6 +285,8 @@ __global__ void __launch_bounds__(kDequantThreads) chunk_dequant_kernel(ChunkPar
       if (t < tq_end) {
         const int slot = t % p.R;
         const int64_t off = static_cast<int64_t>(slot) * D + ((kc ^ (slot & 7)) * 8);
+        if (!in_range(rk + off, 16, p.buf_lo, p.buf_hi, p.err) || !in_range(rv + off, 16, p.buf_lo, p.buf_hi, p.err))
+          continue;  // debug builds
         kr[j] = *reinterpret_cast<const uint4*>(rk + off);
         vr[j] = *reinterpret_cast<const uint4*>(rv + off);
       }
@@ -378,16 +379,27 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
       const uint32_t sph = smem_u32(sm + L::ph), spl = smem_u32(sm + L::pl);
       constexpr uint32_t idS = idesc_f16_f32(kChunkM, kTile);
       constexpr uint32_t idO = idesc_f16_f32(kChunkM, D) | (1u << 16);  // B (values) MN-major
+      // (debug builds: a source outside the workspace is recorded and skipped;
+      // the barrier still completes)
       auto copy_k = [&](int it) {
         uint64_t* bar = kfull + (it & 1);
+        const uint8_t* src = wsu + static_cast<int64_t>(it) * T::bytes;
+        if (!in_range(src, T::kbytes, p.ws, p.ws_hi, p.err)) {
+          mbar_arrive(bar);
+          return;
+        }
         mbar_arrive_expect_tx(bar, T::kbytes);
-        bulk_g2s(sm + L::stage + (it & 1) * T::bytes, wsu + static_cast<int64_t>(it) * T::bytes, T::kbytes, bar);
+        bulk_g2s(sm + L::stage + (it & 1) * T::bytes, src, T::kbytes, bar);
       };
       auto copy_v = [&](int it) {
         uint64_t* bar = vfull + (it & 1);
+        const uint8_t* src = wsu + static_cast<int64_t>(it) * T::bytes + T::v;
+        if (!in_range(src, T::vbytes, p.ws, p.ws_hi, p.err)) {
+          mbar_arrive(bar);
+          return;
+        }
         mbar_arrive_expect_tx(bar, T::vbytes);
-        bulk_g2s(sm + L::stage + (it & 1) * T::bytes + T::v, wsu + static_cast<int64_t>(it) * T::bytes + T::v,
-                 T::vbytes, bar);
+        bulk_g2s(sm + L::stage + (it & 1) * T::bytes + T::v, src, T::vbytes, bar);
       };
       auto issue_pv = [&](int it, bool& bad) {
         const int bs = it & 1;

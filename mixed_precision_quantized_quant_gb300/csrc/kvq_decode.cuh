@@ -581,7 +581,18 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         const int st = kiss & (kSlots - 1);
         const int u = iu, i = ii;
         uint8_t* dst = ring + off;
-        if (i < NG) {
+        // (debug builds: a source outside the cache buffer is recorded and
+        // skipped; the slot's barrier still completes)
+        if (i < NG && !in_range(p.records + u * p.unit_rec_stride + static_cast<int64_t>(i >> lgNS) * p.rec_bytes,
+                                static_cast<size_t>(p.rec_bytes), p.buf_lo, p.buf_hi, p.err)) {
+          mbar_arrive(&wbar[st]);
+        } else if (i >= NG &&
+                   (!in_range(p.res_k + u * p.res_stride + static_cast<int64_t>((nq + (i - NG) * kResTile) % p.R) * D,
+                              kResTile * D * 2, p.buf_lo, p.buf_hi, p.err) ||
+                    !in_range(p.res_v + u * p.res_stride + static_cast<int64_t>((nq + (i - NG) * kResTile) % p.R) * D,
+                              kResTile * D * 2, p.buf_lo, p.buf_hi, p.err))) {
+          mbar_arrive(&wbar[st]);
+        } else if (i < NG) {
           const uint8_t* rec = p.records + u * p.unit_rec_stride + static_cast<int64_t>(i >> lgNS) * p.rec_bytes;
           if (NS == 1) {
             mbar_arrive_expect_tx(&wbar[st], static_cast<uint32_t>(p.rec_bytes));
@@ -1182,7 +1193,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     const int64_t qrow = (static_cast<int64_t>(b) * p.kv_heads + kvh) * p.gqa;  // first query head row
     const int stride_slot = p.gqa * (D + 2);
     float* slot = p.partials + static_cast<int64_t>(pid + u) * stride_slot;
-    for (int idx = tid; idx < p.gqa * D; idx += TH) {
+    // (debug builds: a partial slot outside the cache buffer is recorded and not written)
+    const bool slot_ok = nparts == 1 || in_range(slot, static_cast<size_t>(stride_slot) * 4, p.partials, p.part_hi, p.err);
+    for (int idx = tid; idx < p.gqa * D && slot_ok; idx += TH) {
       const int h = idx / D, c = idx % D;
       float M = -INFINITY;
 #pragma unroll
@@ -1230,6 +1243,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
 #pragma unroll 4
         for (int sidx = pf; sidx <= pl; ++sidx) {
           const float* ps = p.partials + static_cast<int64_t>(sidx + u) * stride_slot;
+          if (!in_range(ps, static_cast<size_t>(stride_slot) * 4, p.partials, p.part_hi, p.err)) continue;  // debug builds
 #pragma unroll
           for (int k = 0; k < PER; ++k) {
             const int idx = tid + k * TH;

@@ -19,6 +19,7 @@ constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier waits
 // device error codes (written to the error word, never trapped)
 constexpr int32_t kErrWaitTimeout = 1;
 constexpr int32_t kErrBadState = 2;
+constexpr int32_t kErrBadAddress = 3;  // debug builds: a computed access fell outside its buffer
 
 // ---------------------------------------------------------------- state
 
@@ -50,6 +51,8 @@ struct AppendParams {
   int32_t* err;
   int mode;               // kFlush | kResidual | kUpdateState
   int ctas;               // CTAs in this launch (for the last-CTA count)
+  const uint8_t* buf_lo;  // the cache buffer [buf_lo, buf_hi) (checked in debug builds)
+  const uint8_t* buf_hi;
 };
 constexpr int kFlush = 1, kResidual = 2, kUpdateState = 4;
 // one CTA per unit (a single-token append): each CTA reads and advances its
@@ -75,6 +78,9 @@ struct DecodeParams {
   int rec_bytes;
   int grid;               // CTAs launched
   float alpha;            // log2(e) / sqrt(D)
+  const uint8_t* buf_lo;  // the cache buffer [buf_lo, buf_hi) (checked in debug builds)
+  const uint8_t* buf_hi;
+  const uint8_t* part_hi; // end of the partials buffer (checked in debug builds)
 };
 
 struct ChunkParams {
@@ -101,7 +107,28 @@ struct ChunkParams {
   float alpha;            // log2(e) / sqrt(D)
   uint8_t* ws;            // workspace: dequantized tiles, ws_tiles per unit
   int ws_tiles;
+  const uint8_t* ws_hi;   // end of the workspace (checked in debug builds)
+  const uint8_t* buf_lo;  // the cache buffer [buf_lo, buf_hi) (checked in debug builds)
+  const uint8_t* buf_hi;
 };
+
+// ---------------------------------------------------------------- debug checks
+
+// Debug builds (compiled with KVQ_DEBUG) check that [p, p + bytes) lies in
+// [lo, hi) before a computed access; a failed check records kErrBadAddress
+// in the error word and the caller skips the access.  Release builds
+// compile the check to `true`.
+__device__ __forceinline__ bool in_range(const void* p, size_t bytes, const void* lo, const void* hi, int32_t* err) {
+#ifdef KVQ_DEBUG
+  const uint8_t* a = static_cast<const uint8_t*>(p);
+  if (a >= static_cast<const uint8_t*>(lo) && a + bytes <= static_cast<const uint8_t*>(hi)) return true;
+  atomicExch(err, kErrBadAddress);
+  return false;
+#else
+  (void)p; (void)bytes; (void)lo; (void)hi; (void)err;
+  return true;
+#endif
+}
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -129,6 +156,11 @@ __device__ __forceinline__ void fence_mbar_init() {
 // make generic-proxy shared-memory writes visible to the async (TMA) proxy
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// one arrival on an mbarrier (release: earlier writes are visible to its waiters)
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {

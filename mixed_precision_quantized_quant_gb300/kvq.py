@@ -13,7 +13,9 @@ import os
 from typing import List, Optional, Sequence, Tuple
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvq.so")
+# KVQ_DEBUG_LIB=1 selects the debug build (device-side range checks of every
+# computed access, reported through the error word)
+LIB_PATH = os.path.join(_HERE, "libkvq_debug.so" if os.environ.get("KVQ_DEBUG_LIB") == "1" else "libkvq.so")
 
 STATUS = {
     0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_BITS", 3: "KVQ_ERR_ALIGN", 4: "KVQ_ERR_CAPACITY",
