@@ -123,11 +123,14 @@ def _dist():
 
 
 def _max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (timings: the slowest rank sets the
+    job's time).  NCCL reduces on the rank's GPU, gloo on the host."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
