@@ -237,3 +237,37 @@ def test_chunk_full_size_workloads_sampled(idx, key_mode, n):
                     got.append(on[b, h * rep + j, i])
             assert_attn_close(np.stack(got), np.stack(exp), f"workload {idx} layer {l} unit {u}")
         cache.close()
+
+
+def test_chunk_long_context_sampled():
+    """Llama-2-70B-shaped unit at 32K context (8 query heads per kv head,
+    G = R = 128): the largest workspace offsets and tile counts.  Sampled
+    rows of a 256-query chunk against fp64 attention."""
+    w = W.scaled(W.workload(5), batch=1, num_kv_heads=2, num_q_heads=16, decode_steps=1)
+    T, D, Hkv, Hq, G = w.context, w.head_dim, w.num_kv_heads, w.num_q_heads, w.group_size
+    rep = Hq // Hkv
+    n = 256
+    l = 0
+    kb, vb, R = w.layers[l][:3]
+    cache = K.KVQCache([w.layers[l]], 1, Hq, Hkv, D, G, T)
+    k, v = W.gen_kv(w, l, 0, T, device="cuda")
+    cache.append(0, k, v)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(41)
+    q = torch.randn((1, Hq, n, D), generator=gen, device="cuda").half()
+    out = cache.chunk_attn(0, q)
+    torch.cuda.synchronize()
+    assert cache.device_error() == 0
+    on, qn, kn, vn = out.cpu().numpy(), q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy()
+    for h in range(Hkv):
+        ora = O.OracleLayerCache(1, 1, D, G, kb, vb, R)
+        ora.append(kn[:, h:h + 1], vn[:, h:h + 1])
+        kh, vh = ora.dequantized(0)
+        got, exp = [], []
+        for j in (0, rep - 1):
+            for i in (0, 100, n - 1):
+                pos = T - n + i
+                exp.append(O.attention_fp64(qn[0, h * rep + j, i].astype(np.float64), kh[: pos + 1], vh[: pos + 1]))
+                got.append(on[0, h * rep + j, i])
+        assert_attn_close(np.stack(got), np.stack(exp), f"32K kv head {h}")
+    cache.close()
