@@ -212,7 +212,10 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   return KVQ_OK;
 }
 
-kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cudaStream_t s) {
+// Launches the layer's decode kernel.  pdl (see DecodeParams::pdl): 0 an
+// ordinary launch, 1 or 2 a programmatic dependent of the previous kernel of
+// the stream, so that its CTAs launch while that kernel drains.
+kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cudaStream_t s, int pdl) {
   const Plan& P = h->plan;
   const LayerPlan& lp = P.layers[layer];
   DecodeParams dp;
@@ -238,8 +241,19 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   dp.buf_lo = h->base;
   dp.buf_hi = h->base + P.total;
   dp.part_hi = reinterpret_cast<const uint8_t*>(dp.partials) + P.partial_floats * 4;
+  dp.pdl = pdl;
   const kvq::DecodeKernel& k = h->dec[layer];
-  k.fn<<<h->grid[layer], k.threads, k.smem, s>>>(dp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(h->grid[layer]));
+  cfg.blockDim = dim3(static_cast<unsigned>(k.threads));
+  cfg.dynamicSmemBytes = k.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, k.fn, dp) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
@@ -373,7 +387,7 @@ kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, 
   if (!q || !out) return KVQ_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
   if (h->tokens[layer] <= 0) return KVQ_ERR_STATE;
-  return launch_decode(h, layer, q, out, static_cast<cudaStream_t>(stream));
+  return launch_decode(h, layer, q, out, static_cast<cudaStream_t>(stream), 1);
 }
 
 size_t kvq_chunk_workspace_bytes(const kvq_handle* h) {
@@ -418,7 +432,7 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
     for (int l = 0; l < L; ++l) {
       kvq_status st = launch_append(h, l, K[l], V[l], 1, s);
       if (st != KVQ_OK) return st;
-      st = launch_decode(h, l, q[l], out[l], s);
+      st = launch_decode(h, l, q[l], out[l], s, 1);
       if (st != KVQ_OK) return st;
     }
     return KVQ_OK;
@@ -440,7 +454,10 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
     kvq_status st = KVQ_OK;
     // appends of all layers on the forked stream (they touch only their own
     // layer's records, ring and counters); decode l waits for append l and
-    // runs after decode l-1 (they share the split workspace)
+    // runs after decode l-1 (they share the split workspace).  Decode l is a
+    // programmatic dependent of decode l-1, which writes nothing of layer l's
+    // cache: it stages its first cache items while decode l-1 drains, and
+    // reads the query and touches the workspace only after decode l-1 is done.
     if (cudaEventRecord(h->graph.ev[0], s) != cudaSuccess || cudaStreamWaitEvent(a, h->graph.ev[0], 0) != cudaSuccess)
       st = KVQ_ERR_CUDA;
     for (int l = 0; l < L && st == KVQ_OK; ++l) {
@@ -449,7 +466,7 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
     }
     for (int l = 0; l < L && st == KVQ_OK; ++l) {
       if (cudaStreamWaitEvent(s, h->graph.ev[1 + l], 0) != cudaSuccess) st = KVQ_ERR_CUDA;
-      if (st == KVQ_OK) st = launch_decode(h, l, q[l], out[l], s);
+      if (st == KVQ_OK) st = launch_decode(h, l, q[l], out[l], s, 2);
     }
     cudaGraph_t graph = nullptr;
     const cudaError_t ec = cudaStreamEndCapture(s, &graph);
@@ -640,6 +657,7 @@ extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const vo
   dp.buf_lo = h->base;
   dp.buf_hi = h->base + P.total;
   dp.part_hi = reinterpret_cast<const uint8_t*>(dp.partials) + partial_bytes;
+  dp.pdl = 0;
   const kvq::DecodeKernel& k = h->dec[layer];
   k.fn<<<grid, k.threads, k.smem, s>>>(dp);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;

@@ -449,6 +449,14 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   // layer's decode bytes below 2^32), computed by every thread.  The token
   // count is read once per CTA, so every thread works from the same value
   // even if a misordered launch changes it meanwhile.
+  // programmatic dependent launch: the next layer's CTAs may take the SM
+  // slots this grid frees; this grid's own reads of anything the previous
+  // kernel writes come after its wait (mode 1: now; mode 2: once the first
+  // cache items are in flight)
+  if (p.pdl) {
+    grid_dep_launch();
+    if (p.pdl == 1) grid_dep_wait();
+  }
   __shared__ int t_shared;
   if (tid == 0) t_shared = __ldcg(p.tokens);
   __syncthreads();
@@ -526,12 +534,15 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     mbar_arrive_expect_tx(&qbar[buf], qbytes);
     bulk_g2s(qs + buf * H * D, p.q + static_cast<int64_t>(u) * p.gqa * D, qbytes, &qbar[buf]);
   };
+  auto issue_first_q = [&]() {
+    issue_q(u_first, 0);
+    if (u_first + 1 <= u_last) issue_q(u_first + 1, 1);
+  };
   if (tid == 0) {
     mbar_init(&qbar[0], 1);
     mbar_init(&qbar[1], 1);
     fence_mbar_init();
-    issue_q(u_first, 0);
-    if (u_first + 1 <= u_last) issue_q(u_first + 1, 1);
+    if (p.pdl != 2) issue_first_q();
   }
 
   // ---------------- per-warp ring of staged items (kSlots copies in flight)
@@ -631,6 +642,12 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     }
   };
   try_issue();
+  if (p.pdl == 2) {
+    // the query, the partials, the split counters and the output may belong
+    // to the previous kernel's work: everything after this waits for it
+    grid_dep_wait();
+    if (tid == 0) issue_first_q();
+  }
   __syncthreads();  // query barriers initialised before anyone waits on them
 
   const __half2 negmask = part ? __float2half2_rn(-1.0f) : __float2half2_rn(0.0f);

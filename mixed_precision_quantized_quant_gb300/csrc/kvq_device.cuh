@@ -81,6 +81,11 @@ struct DecodeParams {
   const uint8_t* buf_lo;  // the cache buffer [buf_lo, buf_hi) (checked in debug builds)
   const uint8_t* buf_hi;
   const uint8_t* part_hi; // end of the partials buffer (checked in debug builds)
+  // launch mode: 0 ordinary; 1 programmatic dependent that waits for the
+  // previous kernel of the stream before its first read; 2 programmatic
+  // dependent that stages its first cache items before that wait (only where
+  // the previous kernel writes neither this layer's cache nor its counters)
+  int pdl;
 };
 
 struct ChunkParams {
@@ -144,6 +149,14 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
+
+// Programmatic dependent launch.  grid_dep_launch lets the next kernel of the
+// stream (if launched as a programmatic dependent) start its CTAs while this
+// grid still runs; grid_dep_wait returns once the previous kernel of the
+// stream has completed and its memory writes are visible.  Both are no-ops
+// for an ordinary launch.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
