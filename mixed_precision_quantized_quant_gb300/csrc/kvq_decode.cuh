@@ -563,8 +563,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     ++iu;
   }
   int ci = ii;
-  auto try_issue = [&]() {
-    while (nin < kSlots) {
+  auto try_issue = [&](int cap = kSlots) {  // stage items while fewer than cap are in flight
+    while (nin < cap) {
       const int f = f0 + warp + W * kiss;
       if (f >= f1) break;
       const uint32_t sz = ii < NG ? cq : cr;
@@ -641,12 +641,15 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
       }
     }
   };
-  try_issue();
+  // (mode 2: one item per warp before the wait, so that the query copy
+  // issued after it does not queue behind a full ring of every CTA)
+  try_issue(p.pdl == 2 ? 1 : kSlots);
   if (p.pdl == 2) {
     // the query, the partials, the split counters and the output may belong
     // to the previous kernel's work: everything after this waits for it
     grid_dep_wait();
     if (tid == 0) issue_first_q();
+    try_issue();
   }
   __syncthreads();  // query barriers initialised before anyone waits on them
 
