@@ -524,8 +524,15 @@ __device__ void write_residual(const AppendParams& p, int u, int64_t lo, int64_t
   }
 }
 
-template <int KB, int VB, int D>
-__global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
+// Register budget of the 128-thread launches (G = 32 flushes, single-token
+// appends, window writes): five CTAs per SM where five fit in shared memory
+// (records without 8-bit codes), so that more independent CTAs cover each
+// other's barrier waits; larger CTAs (G = 64, 128) take the 512-thread bound.
+template <int KB, int VB>
+__host__ __device__ constexpr int append_min_ctas_128() { return (KB == 8 || VB == 8) ? 4 : 5; }
+
+template <int KB, int VB, int D, int TPB, int MINB>
+__global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const bool per_unit = (p.mode & kPerUnit) != 0;
@@ -663,7 +670,8 @@ __global__ void __launch_bounds__(512) append_kernel(AppendParams p) {
 
 template <int KB, int VB, int D>
 static cudaError_t launch_append(const AppendParams& p, dim3 grid, int threads, size_t smem, cudaStream_t s) {
-  auto k = append_kernel<KB, VB, D>;
+  auto k = threads <= 128 ? append_kernel<KB, VB, D, 128, append_min_ctas_128<KB, VB>()>
+                          : append_kernel<KB, VB, D, 512, 1>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -674,7 +682,8 @@ static cudaError_t launch_append(const AppendParams& p, dim3 grid, int threads, 
 
 template <int KB, int VB, int D>
 static int occupancy_append(int threads, size_t smem) {
-  auto k = append_kernel<KB, VB, D>;
+  auto k = threads <= 128 ? append_kernel<KB, VB, D, 128, append_min_ctas_128<KB, VB>()>
+                          : append_kernel<KB, VB, D, 512, 1>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return 0;
   int occ = 0;
