@@ -459,7 +459,8 @@ def run_gpu(args):
 
     peak, peak_kind = _peaks()
     achieved = dec_bytes_per_launch / (dec_ms_per_launch / 1e3) / 1e9
-    traffic = _ncu_traffic(w.name)
+    # the committed capture covers every layer of the workload: no figure for a layer subset
+    traffic = None if args.layers else _ncu_traffic(w.name)
     result = {
         "metric": METRIC,
         "value": round(tokens_per_s, 1),
