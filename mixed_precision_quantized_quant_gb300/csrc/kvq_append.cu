@@ -1,7 +1,7 @@
 // Fused quantize + pack + append for one layer of the mixed-precision KV cache.
 //
 // A unit is one (batch, kv head).  Key groups to quantize ("flush jobs") are
-// spread over persistent CTAs of 4 warps: each CTA stages the K and V rows of
+// spread over persistent CTAs of 4*G threads: each CTA stages the K and V rows of
 // its next group in shared memory with bulk (TMA) copies while it quantizes
 // the current one.  New tokens that stay in the FP16 residual window are
 // copied into the unit's ring by the same launch (one token per unit in a

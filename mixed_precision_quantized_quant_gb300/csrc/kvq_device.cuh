@@ -11,8 +11,6 @@ namespace kvq {
 
 // ---------------------------------------------------------------- constants
 
-constexpr int kThreads = 128;          // append kernels run 4 warps per CTA
-constexpr int kWarps = kThreads / 32;
 constexpr int kResTile = 16;           // residual tokens per decode work item
 constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier waits
 
