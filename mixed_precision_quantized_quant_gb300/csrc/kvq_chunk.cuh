@@ -412,14 +412,15 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
           tc_fence_after_sync();
           const uint32_t dO = tb + 4 * kTile + D * g;
           const uint32_t pg = g * L::pgroup;
+          // descriptors of k-step 0; a k-step moves the address field (bytes / 16)
+          const uint64_t dph = smem_desc(sph + pg, 128, (kTile / 8) * 128);
+          const uint64_t dpl = smem_desc(spl + pg, 128, (kTile / 8) * 128);
+          const uint64_t dv = smem_desc(vb_, KC * 128, 128);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            umma_f16(dO, smem_desc(sph + pg + ks * 256, 128, (kTile / 8) * 128),
-                     smem_desc(vb_ + ks * 2 * KC * 128, KC * 128, 128), idO, (it > 0 || ks > 0) ? 1u : 0u);
+            umma_f16(dO, dph + 16 * ks, dv + 2 * KC * 8 * ks, idO, (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            umma_f16(dO, smem_desc(spl + pg + ks * 256, 128, (kTile / 8) * 128),
-                     smem_desc(vb_ + ks * 2 * KC * 128, KC * 128, 128), idO, 1u);
+          for (int ks = 0; ks < kTile / 16; ++ks) umma_f16(dO, dpl + 16 * ks, dv + 2 * KC * 8 * ks, idO, 1u);
           umma_commit(o_done + g);
         }
         umma_commit(vfree + bs);
@@ -438,13 +439,12 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
         for (int g = 0; g < 2; ++g) {
           const uint32_t qg = sq + g * (kChunkM * D * 2);
           const uint32_t dS = tb + kTile * (2 * bs + g);
+          const uint64_t dq = smem_desc(qg, 128, KC * 128);
+          const uint64_t dkh = smem_desc(kb_h, 128, KC * 128), dkl = smem_desc(kb_l, 128, KC * 128);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            umma_f16(dS, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(kb_h + ks * 256, 128, KC * 128), idS,
-                     ks > 0);
+          for (int ks = 0; ks < D / 16; ++ks) umma_f16(dS, dq + 16 * ks, dkh + 16 * ks, idS, ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            umma_f16(dS, smem_desc(qg + ks * 256, 128, KC * 128), smem_desc(kb_l + ks * 256, 128, KC * 128), idS, 1u);
+          for (int ks = 0; ks < D / 16; ++ks) umma_f16(dS, dq + 16 * ks, dkl + 16 * ks, idS, 1u);
           umma_commit(s_done + 2 * bs + g);
         }
         umma_commit(kfree + bs);
