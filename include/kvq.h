@@ -157,7 +157,10 @@ kvq_status kvq_append(kvq_handle* h, int layer, const void* K, const void* V, in
  * q: device fp16 [batch][num_q_heads][head_dim]; query head j reads kv head
  *    j / (num_q_heads / num_kv_heads).
  * out: device fp32 [batch][num_q_heads][head_dim], written entirely.
- * Scores are scaled by 1/sqrt(head_dim).  KVQ_ERR_STATE if the layer is empty. */
+ * Scores are scaled by 1/sqrt(head_dim).  KVQ_ERR_STATE if the layer is empty.
+ * The kernel is launched as a programmatic dependent of the previous kernel on
+ * the stream: its CTAs may start while that kernel drains, but each waits for
+ * it to complete before its first read, so stream order holds as usual. */
 kvq_status kvq_decode_attn(kvq_handle* h, int layer, const void* q, float* out, void* stream);
 
 /* Causal attention of the queries of the n_queries newest tokens over `layer`
@@ -194,7 +197,10 @@ size_t kvq_chunk_workspace_bytes(const kvq_handle* h);
  * replayed from a CUDA graph the handle keeps (it is re-captured when the
  * pointers change).  Inside the graph the appends run on a forked stream:
  * decode l waits for append l (and for decode l-1), so later layers' appends
- * overlap earlier layers' decodes.  KVQ_ERR_CAPACITY if any layer is full. */
+ * overlap earlier layers' decodes.  Decode l is a programmatic dependent of
+ * decode l-1: it stages its first items of layer l's cache (which decode l-1
+ * does not write) while decode l-1 drains, and reads q[l] and writes out[l]
+ * only after it.  KVQ_ERR_CAPACITY if any layer is full. */
 kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* const* V,
                            const void* const* q, float* const* out, void* stream);
 
