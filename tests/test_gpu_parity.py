@@ -172,6 +172,49 @@ def test_decode_step_graph_matches_layer_calls(layers):
         c.close()
 
 
+
+def test_decode_step_graph_replay_fixed_buffers():
+    """The step graph captured once and replayed with the same input and
+    output buffers every step (the launch configuration the benchmark times:
+    every decode a programmatic dependent of the previous layer's), bit for
+    bit against per-layer calls, across group flushes."""
+    layers = ((8, 4, 32), (4, 2, 32), (4, 2, 32), (2, 2, 64))
+    w = W.scaled(W.workload(2), batch=3, num_layers=4, context=190, decode_steps=80, layers=layers)
+    L = w.num_layers
+    stream = torch.cuda.Stream()
+    caches = []
+    for _ in range(2):
+        c = K.KVQCache(w.layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.group_size,
+                       w.total_tokens)
+        for l in range(L):
+            k, v = W.gen_kv(w, l, 0, w.context, device="cuda")
+            c.append(l, k, v)
+        caches.append(c)
+    k_cur = torch.empty((L, w.batch, w.num_kv_heads, 1, w.head_dim), dtype=torch.float16, device="cuda")
+    v_cur = torch.empty_like(k_cur)
+    q_cur = torch.empty((L, w.batch, w.num_q_heads, w.head_dim), dtype=torch.float16, device="cuda")
+    outs_a = torch.empty((L, w.batch, w.num_q_heads, w.head_dim), device="cuda")
+    outs_b = torch.empty_like(outs_a)
+    torch.cuda.synchronize()
+    for step in range(70):
+        for l in range(L):
+            k, v = W.gen_kv(w, l, w.context + step, 1, device="cuda")
+            k_cur[l].copy_(k)
+            v_cur[l].copy_(v)
+            q_cur[l].copy_(W.gen_q(w, l, step, device="cuda"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            caches[0].decode_step([k_cur[l] for l in range(L)], [v_cur[l] for l in range(L)],
+                                  [q_cur[l] for l in range(L)], [outs_a[l] for l in range(L)], stream=stream)
+            for l in range(L):
+                caches[1].append(l, k_cur[l], v_cur[l], stream=stream)
+                caches[1].decode_attn(l, q_cur[l], outs_b[l], stream=stream)
+        stream.synchronize()
+        assert torch.equal(outs_a, outs_b), step
+    for c in caches:
+        assert c.device_error() == 0
+        c.close()
+
 def _unit_stream(k, v, u, Hkv):
     b, h = divmod(u, Hkv)
     return k[b:b + 1, h:h + 1].cpu().numpy(), v[b:b + 1, h:h + 1].cpu().numpy()
