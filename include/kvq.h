@@ -226,9 +226,12 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
  *     bytes, where units = batch * num_kv_heads and grid is the layer's
  *     launch width (at most 1024 CTAs); a layer needing more returns
  *     KVQ_ERR_CAPACITY and launches nothing.
- *   - The first call on a device (the device current at the call) looks up the
- *     array's device address with cudaGetSymbolAddress and keeps it; make that
- *     first call before any stream capture.  KVQ_ERR_CUDA if the lookup fails.
+ *   - The current device must be the one that was current at kvq_create()
+ *     (the device holding the handle's buffer); otherwise KVQ_ERR_ARG and
+ *     nothing is launched.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress and keeps it; make that first call before any
+ *     stream capture.  KVQ_ERR_CUDA if the lookup fails.
  *   - Each call clears the counters on `stream` (an asynchronous memset of
  *     units * 4 bytes) before it launches the kernel.
  *   - Every call on a device shares the one array: calls that overlap on the

@@ -136,6 +136,7 @@ struct StepGraph {
 
 struct kvq_handle {
   Plan plan;
+  int device = 0;  // the device current at kvq_create (the buffer's device)
   uint8_t* base = nullptr;
   std::vector<int64_t> tokens;  // host mirror of each layer's appended tokens
   std::vector<kvq::DecodeKernel> dec;
@@ -341,6 +342,7 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
   kvq_handle* h = new (std::nothrow) kvq_handle;
   if (!h) return KVQ_ERR_ARG;
   h->plan = P;
+  h->device = dev;
   h->base = static_cast<uint8_t*>(dev_buf);
   h->tokens.assign(P.L, 0);
   for (int l = 0; l < P.L; ++l) {
@@ -600,9 +602,11 @@ constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 uint8_t* g_noalloc_ptr[kMaxDevices] = {};
 
-kvq_status noalloc_scratch(uint8_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+// The array's address on `dev`, which must be the current device (host code
+// sees the array only through a stand-in symbol; the runtime resolves it for
+// the current device).
+kvq_status noalloc_scratch(int dev, uint8_t** out) {
+  if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
@@ -628,8 +632,13 @@ extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const vo
   const int64_t counter_bytes = align_up(static_cast<int64_t>(P.units) * 4, 256);
   const int64_t partial_bytes = static_cast<int64_t>(grid + P.units) * P.gqa * (P.D + 2) * 4;
   if (counter_bytes + partial_bytes > static_cast<int64_t>(KVQ_NOALLOC_SCRATCH_BYTES)) return KVQ_ERR_CAPACITY;
+  // the array is looked up (and the kernel launched) on the device that holds
+  // the handle's buffer: a different current device is refused
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cur != h->device) return KVQ_ERR_ARG;
   uint8_t* scratch = nullptr;
-  const kvq_status st = noalloc_scratch(&scratch);
+  const kvq_status st = noalloc_scratch(cur, &scratch);
   if (st != KVQ_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* counters = reinterpret_cast<int32_t*>(scratch);

@@ -11,8 +11,9 @@
 //   code  = clamp(rint((x - min) / scale), 0, 2^b - 1)
 // ("KVTuner ...", section A3 quantizer; "KVmix ...", 关键设计 2; "LLM 量化精读笔记
 // · 08 ...", sections 6.1-6.2).  The division is the IEEE fp32 one: a
-// reciprocal estimate decides the code unless the quotient lies within 2^-14
-// of a rounding boundary, where the correctly rounded __fdiv_rn decides.
+// reciprocal estimate decides the code unless the product lies near a
+// rounding boundary (kNearHalf states the band and why it suffices), where
+// the correctly rounded __fdiv_rn decides.
 //
 // Per-channel min/max runs over the staged rows, per-token min/max uses warp
 // shuffles; each scale is computed once, by one thread; packed codes are
@@ -53,8 +54,8 @@ __device__ __forceinline__ Scale make_scale(__half mn, __half mx, bool slot10) {
     sc.qmax = 3.0f;
   }
   sc.s = s;
-  // 1/s only steers the fast path of the code computation (see kNearHalf);
-  // an approximate reciprocal (relative error below 2^-22) is enough
+  // 1/s only steers the fast path of the code computation: kNearHalf's band
+  // covers a reciprocal with relative error up to 2^-22
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
   sc.r = (s > 0.0f) ? r : 0.0f;
@@ -131,19 +132,26 @@ __host__ __device__ inline AppendSmem append_smem_layout(int D, int G, int rec_b
   return a;
 }
 
-// The fast path computes y = (x - min) * r with r within 2^-22 (relative) of
-// 1/s, so y is within 2^-22 * y of the correctly rounded quotient; y stays
-// below 1.5 * 255 < 512 (the fp16 scale is at least s32 / 1.5, and far closer
-// for normal scales).  A y within 2^-13 of a rounding boundary is redone
-// with the IEEE division, which covers every case where the two could round
-// to different integers.
-constexpr float kNearHalf = 0.5f - 1.220703125e-04f;  // 2^-13 from a rounding boundary
+// The band of the fast path, stated once.  It computes y = fl((x - min) * r)
+// with r = rcp.approx(s); the code must equal rint(fl((x - min) / s)).
+//   * r = (1/s)(1 + e1) with |e1| <= 2^-22 (the PTX ISA gives rcp.approx.f32
+//     a 1-ulp bound, about 2^-23; the argument only needs twice that);
+//   * the product's rounding adds |e2| <= 2^-24, so |y - a/s| <= (a/s) *
+//     (2^-22 + 2^-24 + 2^-46), a = x - min;
+//   * the IEEE quotient is within 2^-24 * (a/s) of a/s;
+//   * a/s <= 1.5 * 255 < 383 (the fp16 scale is at least s32 / 1.5, and
+//     far closer for normal scales).
+// So |y - fl(a/s)| <= 383 * (2^-22 + 2^-23 + 2^-46) < 1.37e-4 < 2^-12.  If y
+// is at least 2^-12 away from every rounding boundary k + 1/2, the IEEE
+// quotient lies on the same side of it and both round to the same integer;
+// every y inside the band is redone with the IEEE division.  (fp32 resolves
+// the band: below 512 the spacing of y is at most 2^-15.)
+constexpr float kNearHalf = 0.5f - 2.44140625e-04f;  // within 2^-12 of a boundary: exact path
 
 // code = min(rint((x - min) / s), qmax) with IEEE fp32 subtraction and
-// division: the product with 1/s decides unless it lies within 2^-14 of a
-// rounding boundary, where the correctly rounded quotient decides.  x >= min
-// always, so no lower clamp.  sc = {min, s, 1/s, qmax}; s == 0 carries
-// 1/s == 0 and gives code 0.
+// division: the product with 1/s decides outside kNearHalf's band, the
+// correctly rounded quotient inside it.  x >= min always, so no lower clamp.
+// sc = {min, s, 1/s, qmax}; s == 0 carries 1/s == 0 and gives code 0.
 __device__ __forceinline__ uint32_t quant_fast(float x, const float4& sc) {
   const float a = __fsub_rn(x, sc.x);
   const float y = __fmul_rn(a, sc.z);

@@ -104,6 +104,40 @@ def test_quantizer_worked_examples(golden_dir):
     assert n == 5
 
 
+def test_quantizer_inexact_fp16_scale_worked(golden_dir):
+    # the fp32 scale is not an fp16 value: the codes follow the stored fp16 scale,
+    # and on these inputs they differ from codes taken with the fp32 scale
+    n = 0
+    for line in _lines(os.path.join(golden_dir, "quantizer_fp16_scale_worked.txt")):
+        parts = [p.strip() for p in line.split("|")]
+        bits, x, codes, s, z = _parse_q("|".join(parts[:5]))
+        codes32 = [int(t) for t in parts[5].split()]
+        c, s16, z16 = O.quantize_values_tokens(x[None, :], bits)
+        assert list(c[0]) == list(codes), line
+        assert float(s16[0]) == s and float(z16[0]) == z
+        ck, sk, zk = O.quantize_keys_group(x[:, None], bits)
+        assert list(ck[:, 0]) == list(codes)
+        assert float(sk[0]) == s and float(zk[0]) == z
+        assert list(codes) != codes32  # the fixture separates the two readings
+        n += 1
+    assert n == 2
+
+
+def _parse_rows(field):
+    return np.array([[float(t) for t in r.split()] for r in field.split(";")], dtype=np.float64)
+
+
+def test_rel_error_worked(golden_dir):
+    from fractions import Fraction
+    n = 0
+    for line in _lines(os.path.join(golden_dir, "rel_error_worked.txt")):
+        xs, xh, frac = (p.strip() for p in line.split("|"))
+        x, x_hat = _parse_rows(xs), _parse_rows(xh)
+        assert O.rel_error(x, x_hat) == pytest.approx(float(Fraction(frac)), rel=1e-12, abs=0.0), line
+        n += 1
+    assert n == 2
+
+
 def test_key_group_worked(golden_dir):
     lines = list(_lines(os.path.join(golden_dir, "key_group_worked.txt")))
     bits = int(lines[0].split()[1])
