@@ -2,20 +2,28 @@
 
 A step is one decode step of the whole hot path over every layer of the
 workload: append the new token (FP16 window; a group flush with quantize +
-pack every G steps) and run decode attention over the quantized cache plus
-the window.  The default workload is the Llama-3.1-8B-shaped decode: 32
-layers, 32 q / 8 kv heads, head_dim 128, batch 16, context 4096, G = R = 32,
-K8V4 on layers 0-1 and 29-31 and K4V2 elsewhere.
+pack when a layer's window fills) and run decode attention over the quantized
+cache plus the window.  The default workload is the largest one, the
+Llama-2-70B-shaped 32K-context decode: 80 layers, 64 q / 8 kv heads, head_dim
+128, batch 8, G = R = 128, K8V4 on layers 0-1 and 77-79 and K4V2 elsewhere.
+The prefill stops short of the context by the offset that makes the middle
+timed step flush a key group on every layer, so the quantize + pack half of
+the decode step is inside the timed window whatever --steps is.
 
 Reported:
-  value       decode tokens/s (batch x ranks / step time), device-timed with
-              CUDA events around K replays of the step's CUDA graph
+  value       decode tokens/s (batch x ranks x steps / time), device-timed
+              with CUDA events around the K timed replays of the step's CUDA
+              graph (an event after each step gives the per-step times; the
+              flush step is reported separately)
   e2e         the same metric through KVQCache.decode_step with every step's
               inputs copied from pinned host memory and its outputs read back
-  roofline    decode-attention kernel: algorithmic bytes per launch / average
-              launch duration (a second timed pass replaying a decode-only
-              graph of all layers) against the measured HBM copy bandwidth
-  cpu_baseline  the oracle timed on the host cores on a bounded sample
+  roofline    decode-attention kernel: algorithmic bytes per launch / launch
+              duration, from a second pass replaying a decode-only graph of
+              all layers (median of >= 10 replays, one event pair each)
+              against the measured HBM copy bandwidth
+  other_workloads  the same figures (no end-to-end leg) for --extra-workloads
+  cpu_baseline  the oracle on the host cores (one worker process per core) on
+              a bounded sample of the step's (layer, unit) pairs
 
 --impl reference times the oracle (the plain CPU statement of the method) on
 the same workload, one bounded sample per step.
@@ -143,100 +151,178 @@ def _barrier(world):
 
 
 # ----------------------------------------------------------------------------
-# CPU oracle timing (bounded sample)
+# CPU oracle timing (bounded sample, one worker process per host core)
 # ----------------------------------------------------------------------------
 
-class OracleSampler:
-    """Times the oracle's decode step (append one token, then fp64 attention
-    over the dequantized cache) for one (batch, kv head) unit of each distinct
-    precision pair, at full context, and extrapolates to the whole step
-    (all units of all layers).  The oracle runs as it stands, single-threaded
-    numpy."""
+def _oracle_worker(conn, jobs):
+    """One host core: prefill the oracle caches of its (layer, unit) pairs,
+    then run a decode step on each of them per request (append the step's
+    token, then fp64 attention over the dequantized cache)."""
+    from oracle import kvq_oracle as O
+    caches = []
+    for d, G, kb, vb, R, km, k, v in jobs:
+        c = O.OracleLayerCache(1, 1, d, G, kb, vb, R, km)
+        c.append(k, v)
+        caches.append(c)
+    conn.send("ready")
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            break
+        for c, (k1, v1, q) in zip(caches, msg):
+            c.append(k1, v1)
+            c.attend(q)
+        conn.send("done")
+    conn.close()
 
-    def __init__(self, w):
+
+class OracleSampler:
+    """Times the oracle's decode step on a bounded sample of the workload: n_s
+    of the step's L x U (layer, (batch, kv head) unit) pairs, on layers spread
+    evenly over the model (so the precision pairs appear in about their
+    proportions), each at the full prefill length.  Each pair lives in one of
+    `procs` worker processes (spawned, one host core each, single-threaded
+    numpy); a sample step sends every worker its pairs' next token and query
+    and waits for all of them.  The oracle runs as it stands.
+
+    tokens/s = batch x (n_s / (L x U)) / (wall time of a sample step)."""
+
+    def __init__(self, w, prefill=None, procs=None):
+        import multiprocessing as mp
+        import numpy as np
         from mixed_precision_quantized_quant_gb300 import workloads as W
-        from oracle import kvq_oracle as O
         self.W, self.w = W, w
-        seen, self.layers = set(), []
-        for l, p in enumerate(w.layers):
-            if p not in seen:
-                seen.add(p)
-                self.layers.append(l)
+        L, U = w.num_layers, w.batch * w.num_kv_heads
+        ncpu = os.cpu_count() or 1
+        self.procs = max(1, min(procs or ncpu, L))
+        n_s = self.procs
+        self.layers = sorted({(i * L) // n_s for i in range(n_s)})
+        self.n_s = len(self.layers)
+        self.fraction = self.n_s / (L * U)
+        self.S = w.context if prefill is None else prefill
         self.unit_w = W.scaled(w, batch=1, num_kv_heads=1, num_q_heads=w.num_q_heads // w.num_kv_heads)
-        self.caches = {}
-        for l in self.layers:
+        per = [[] for _ in range(self.procs)]
+        self.owner = []
+        for i, l in enumerate(self.layers):
             kb, vb, R = w.layers[l][:3]
             km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
-            ora = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km)
-            k, v = W.gen_kv(self.unit_w, l, 0, w.context)
-            ora.append(k.numpy(), v.numpy())
-            self.caches[l] = ora
+            k, v = W.gen_kv(self.unit_w, l, 0, self.S)
+            per[i % self.procs].append((w.head_dim, w.group_size, kb, vb, R, km, k.numpy(), v.numpy()))
+            self.owner.append(i % self.procs)
+        self.per = [[i for i in range(self.n_s) if self.owner[i] == p] for p in range(self.procs)]
+        # spawned workers, single-threaded numpy (a forked child of a CUDA
+        # process can hang; spawn starts clean)
+        ctx = mp.get_context("spawn")
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.conns, self.workers = [], []
+            for pidx in range(self.procs):
+                a, b = ctx.Pipe()
+                pr = ctx.Process(target=_oracle_worker, args=(b, per[pidx]), daemon=True)
+                pr.start()
+                self.conns.append(a)
+                self.workers.append(pr)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for c in self.conns:
+            if c.recv() != "ready":
+                raise RuntimeError("oracle worker failed to start")
         self.pos = 0
-        U = w.batch * w.num_kv_heads
-        self.count = {l: sum(1 for p in w.layers if p == w.layers[l]) * U for l in self.layers}
-        self.desc = (f"oracle decode step (append 1 token + fp64 attention over the dequantized cache) "
-                     f"for 1 of {U} (batch, kv head) units on layers {self.layers} (one per distinct "
-                     f"precision pair) at context {w.context}; per-unit time x {U} units x "
-                     f"{w.num_layers} layers")
-
-    def errors(self):
-        """Quantization error of each distinct precision pair on the sampled
-        unit (KVTuner A3's metrics): e_k, e_v over the quantized tokens,
-        e_a = mean |a - a_hat| of the attention weights and e_o of the output
-        for the first query, against fp64 over the fp16 K and V."""
-        import numpy as np
-        from oracle import kvq_oracle as O
-        out = {}
-        for l in self.layers:
-            kb, vb = self.w.layers[l][:2]
-            ora = self.caches[l]
-            kh, vh = ora.dequantized(0)
-            k, v = (x.numpy()[0, 0].astype(np.float64) for x in self.W.gen_kv(self.unit_w, l, 0, self.w.context))
-            nq = ora.n_q
-            q = self.W.gen_q(self.unit_w, l, 0).numpy()[0].astype(np.float64)
-            T = kh.shape[0]
-            ea, o_ref, o_hat = [], [], []
-            for h in range(q.shape[0]):
-                def weights(kk):
-                    x = kk[:T] @ q[h] / np.sqrt(kk.shape[1])
-                    e = np.exp(x - x.max())
-                    return e / e.sum()
-                a, ah = weights(k), weights(kh)
-                ea.append(np.abs(a - ah).mean())
-                o_ref.append(O.attention_fp64(q[h], k[:T], v[:T]))
-                o_hat.append(O.attention_fp64(q[h], kh, vh))
-            out[f"K{kb}V{vb}"] = {"e_k": round(O.rel_error(k[:nq], kh[:nq]), 5),
-                                  "e_v": round(O.rel_error(v[:nq], vh[:nq]), 5),
-                                  "e_a": float(f"{np.mean(ea):.3e}"),
-                                  "e_o": round(O.rel_error(np.stack(o_ref), np.stack(o_hat)), 5)}
-        return out
+        self.desc = (f"oracle decode step (append 1 token, then fp64 attention over the dequantized cache) on "
+                     f"{self.n_s} of the step's {L * U} (layer, unit) pairs (layers {self.layers}, one unit each, "
+                     f"prefill {self.S}), spread over {self.procs} worker processes of one host core each; "
+                     f"tokens/s = batch x {self.n_s}/{L * U} / sample-step wall time")
 
     def step(self) -> float:
-        """Seconds one full decode step would take, from one timed unit-step
-        per distinct layer type."""
-        total = 0.0
-        for l in self.layers:
-            k1, v1 = self.W.gen_kv(self.unit_w, l, self.w.context + self.pos, 1)
+        """Wall seconds of one sample step (inputs drawn before the clock starts)."""
+        msgs = [[] for _ in range(self.procs)]
+        for i, l in enumerate(self.layers):
+            k1, v1 = self.W.gen_kv(self.unit_w, l, self.S + self.pos, 1)
             q = self.W.gen_q(self.unit_w, l, self.pos).numpy()
-            t0 = time.perf_counter()
-            self.caches[l].append(k1.numpy(), v1.numpy())
-            self.caches[l].attend(q)
-            total += (time.perf_counter() - t0) * self.count[l]
+            msgs[self.owner[i]].append((k1.numpy(), v1.numpy(), q))
+        t0 = time.perf_counter()
+        for c, m in zip(self.conns, msgs):
+            c.send(m)
+        for c in self.conns:
+            if c.recv() != "done":
+                raise RuntimeError("oracle worker failed")
+        dt = time.perf_counter() - t0
         self.pos += 1
-        return total
+        return dt
+
+    def tokens_per_s(self, seconds_per_step: float) -> float:
+        return self.w.batch * self.fraction / seconds_per_step
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except Exception:
+                pass
+        for pr in self.workers:
+            pr.join(timeout=10)
+            if pr.is_alive():
+                pr.terminate()
 
 
-def oracle_sample(w, budget_s: float = 12.0):
-    """(tokens/s, seconds per full step, description, quantization errors)
-    from repeated sampled steps until about budget_s seconds of oracle work."""
-    smp = OracleSampler(w)
-    errors = smp.errors()
-    t_start = time.perf_counter()
-    steps = []
-    while len(steps) < 3 or (time.perf_counter() - t_start < budget_s and len(steps) < 64):
-        steps.append(smp.step())
-    step_s = statistics.median(steps)
-    return w.batch / step_s, step_s, smp.desc + f"; median over {len(steps)} sampled steps", errors
+def quant_errors(w):
+    """Quantization error of each distinct precision pair on one (batch, kv
+    head) unit at full context (KVTuner A3's metrics): e_k, e_v over the
+    quantized tokens, e_a = mean |a - a_hat| of the attention weights and e_o
+    of the output for the first query, against fp64 over the fp16 K and V."""
+    import numpy as np
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    from oracle import kvq_oracle as O
+    unit_w = W.scaled(w, batch=1, num_kv_heads=1, num_q_heads=w.num_q_heads // w.num_kv_heads)
+    out, seen = {}, set()
+    for l, spec in enumerate(w.layers):
+        if spec in seen:
+            continue
+        seen.add(spec)
+        kb, vb, R = spec[:3]
+        km = spec[3] if len(spec) > 3 else 0
+        ora = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km)
+        k16, v16 = W.gen_kv(unit_w, l, 0, w.context)
+        ora.append(k16.numpy(), v16.numpy())
+        kh, vh = ora.dequantized(0)
+        k, v = (x.numpy()[0, 0].astype(np.float64) for x in (k16, v16))
+        q = W.gen_q(unit_w, l, 0).numpy()[0].astype(np.float64)
+        ea, o_ref, o_hat = [], [], []
+        for h in range(q.shape[0]):
+            def weights(kk):
+                x = kk @ q[h] / np.sqrt(kk.shape[1])
+                e = np.exp(x - x.max())
+                return e / e.sum()
+            ea.append(np.abs(weights(k) - weights(kh)).mean())
+            o_ref.append(O.attention_fp64(q[h], k, v))
+            o_hat.append(O.attention_fp64(q[h], kh, vh))
+        nq = ora.n_q
+        out[f"K{kb}V{vb}"] = {"e_k": round(O.rel_error(k[:nq], kh[:nq]), 5),
+                              "e_v": round(O.rel_error(v[:nq], vh[:nq]), 5),
+                              "e_a": float(f"{np.mean(ea):.3e}"),
+                              "e_o": round(O.rel_error(np.stack(o_ref), np.stack(o_hat)), 5)}
+    return out
+
+
+def oracle_sample(w, budget_s: float = 20.0, prefill=None):
+    """(tokens/s, median seconds per sample step, cores, description) from
+    sample steps repeated until about budget_s seconds of oracle work."""
+    smp = OracleSampler(w, prefill=prefill)
+    try:
+        t_start = time.perf_counter()
+        steps = []
+        while len(steps) < 3 or (time.perf_counter() - t_start < budget_s and len(steps) < 200):
+            steps.append(smp.step())
+        step_s = statistics.median(steps)
+        return smp.tokens_per_s(step_s), step_s, smp.procs, smp.desc + f"; median over {len(steps)} sample steps"
+    finally:
+        smp.close()
 
 
 # ----------------------------------------------------------------------------
@@ -254,36 +340,40 @@ def _with_key_mode(w, args):
     return W.scaled(w, name=w.name + "-per-token-keys", layers=tuple((kb, vb, r, 1) for kb, vb, r in w.layers))
 
 
-def run_gpu(args):
-    import numpy as np
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal: context for the measured-copy fraction
+
+
+def _prefill_length(w, warm, steps):
+    """Prefill length: the context, less an offset that puts a key-group flush
+    on every layer at the middle timed step.  A step appends one token, so
+    step k (1-based, warm-up included) brings the cache to prefill + k tokens;
+    a layer whose window is a multiple of G flushes when that count is a
+    multiple of G."""
+    mid = warm + (steps + 1) // 2
+    return w.context - (mid % w.group_size), mid
+
+
+def measure_decode(w, args, dev, world, e2e=True):
+    """One workload's decode step on this GPU: prefill, warm-up, the timed
+    window (per-step CUDA events), the decode-only roofline replays and the
+    end-to-end leg.  Returns a dict of figures."""
     import torch
 
     from mixed_precision_quantized_quant_gb300 import kvq as K
     from mixed_precision_quantized_quant_gb300 import workloads as W
 
-    world, rank, local = _dist()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    K.load()
-    w = _with_key_mode(W.workload(args.workload), args)
-    if args.layers:  # profiling runs: the workload's first N layers
-        w = W.scaled(w, num_layers=args.layers, layers=tuple(w.layers[:args.layers]))
     L, B, Hq, Hkv, D = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
     steps, warm = args.steps, args.warmup
-    cap = w.context + warm + steps
+    S0, mid = _prefill_length(w, warm, steps)
+    cap = S0 + warm + steps
     stream = torch.cuda.Stream(device=dev)
-
     cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, cap, device=dev)
 
-    # ---- prefill (timed separately: append GB/s)
-    prefill_ms = 0.0
-    prefill_bytes = 0
+    # ---- prefill (timed per layer: append GB/s)
+    prefill_ms, prefill_bytes = 0.0, 0
     with torch.cuda.stream(stream):
         for l in range(L):
-            k, v = W.gen_kv(w, l, 0, w.context, device=dev)
+            k, v = W.gen_kv(w, l, 0, S0, device=dev)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             cache.append(l, k, v, stream=stream)
@@ -303,7 +393,7 @@ def run_gpu(args):
     qin = torch.empty((nst, L, B, Hq, D), dtype=torch.float16, device=dev)
     for s in range(nst):
         for l in range(L):
-            k1, v1 = W.gen_kv(w, l, w.context + s, 1, device=dev)
+            k1, v1 = W.gen_kv(w, l, S0 + s, 1, device=dev)
             kin[s, l].copy_(k1)
             vin[s, l].copy_(v1)
             qin[s, l].copy_(W.gen_q(w, l, s, device=dev))
@@ -313,12 +403,8 @@ def run_gpu(args):
     v_cur = torch.empty_like(k_cur)
     q_cur = torch.empty((L, B, Hq, D), dtype=torch.float16, device=dev)
     torch.cuda.synchronize()
-
-    def step_lists():
-        return ([k_cur[l] for l in range(L)], [v_cur[l] for l in range(L)], [q_cur[l] for l in range(L)],
-                [outs[l] for l in range(L)])
-
-    Ks, Vs, Qs, Os = step_lists()
+    Ks, Vs = [k_cur[l] for l in range(L)], [v_cur[l] for l in range(L)]
+    Qs, Os = [q_cur[l] for l in range(L)], [outs[l] for l in range(L)]
 
     def run_step(s):
         k_cur.copy_(kin[s], non_blocking=True)
@@ -326,7 +412,7 @@ def run_gpu(args):
         q_cur.copy_(qin[s], non_blocking=True)
         cache.decode_step(Ks, Vs, Qs, Os, stream=stream)
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
     with torch.cuda.stream(stream):
@@ -335,25 +421,29 @@ def run_gpu(args):
         stream.synchronize()
         _barrier(world)
         torch.cuda.synchronize()
-        bytes_step = sum(cache.decode_bytes(l) for l in range(L))  # at the first timed step
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nq_before = [cache.view(l)["quantized_tokens"] for l in range(L)]
+        bytes_first = sum(cache.decode_bytes(l) for l in range(L))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
         t0 = time.time()
-        ev0.record(stream)
-        for s in range(warm, warm + steps):
+        evs[0].record(stream)
+        for i, s in enumerate(range(warm, warm + steps)):
             run_step(s)
-        ev1.record(stream)
+            evs[i + 1].record(stream)
         stream.synchronize()
         t1 = time.time()
         sampler.mark(t0, t1)
         torch.cuda.synchronize()
         _barrier(world)
-    ms_total = ev0.elapsed_time(ev1)
-    ms_total = _max_over_ranks(ms_total, world)
+        bytes_last = sum(cache.decode_bytes(l) for l in range(L))
+        flushed = sum(1 for l in range(L) if cache.view(l)["quantized_tokens"] > nq_before[l])
+    ms_total = _max_over_ranks(evs[0].elapsed_time(evs[-1]), world)
+    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
     ms_step = ms_total / steps
-    tokens_per_s = world * B * steps / (ms_total / 1e3)
-    gpu_launches = steps * 2 * L
+    flush_i = mid - warm - 1  # 0-based index of the flush step inside the window
+    others = [t for i, t in enumerate(step_ms) if i != flush_i] or step_ms
 
-    # ---- decode-attention roofline: replay a decode-only graph of all layers
+    # ---- decode-attention roofline: replays of a decode-only graph of all
+    # layers, one CUDA event pair per replay, median replay
     dec_bytes = [cache.decode_bytes(l) for l in range(L)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -366,34 +456,59 @@ def run_gpu(args):
         for _ in range(3):
             g.replay()
         stream.synchronize()
-        reps = max(10, min(200, int(200 / max(ms_step, 0.05))))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(10, min(100, int(100 / max(ms_step, 0.05))))
+        rev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
         t0 = time.time()
-        e0.record(stream)
-        for _ in range(reps):
+        rev[0].record(stream)
+        for r in range(reps):
             g.replay()
-        e1.record(stream)
+            rev[r + 1].record(stream)
         stream.synchronize()
         sampler.mark(t0, time.time())
-    dec_ms_per_launch = e0.elapsed_time(e1) / reps / L
+    replay_ms = sorted(rev[r].elapsed_time(rev[r + 1]) for r in range(reps))
+    dec_ms_per_launch = statistics.median(replay_ms) / L
     dec_bytes_per_launch = sum(dec_bytes) / L
     clocks = sampler.stop()
+    err = cache.device_error(stream)
+    if err:
+        raise RuntimeError(f"device error word {err}")
+    res = {
+        "w": w, "steps": steps, "warmup": warm, "ms_total": ms_total, "ms_step": ms_step,
+        "tokens_per_s": world * B * steps / (ms_total / 1e3),
+        "step_ms": {"median": round(statistics.median(step_ms), 4), "mean": round(ms_step, 4),
+                    "flush_step": round(step_ms[flush_i], 4) if 0 <= flush_i < steps else None,
+                    "median_without_flush_step": round(statistics.median(others), 4),
+                    "min": round(min(step_ms), 4), "max": round(max(step_ms), 4),
+                    "flush_step_index": flush_i, "layers_flushed_in_window": flushed},
+        "prefill": S0, "bytes_step": (bytes_first + bytes_last) / 2,
+        "append_gbs": prefill_bytes / (prefill_ms / 1e3) / 1e9,
+        "dec_ms_per_launch": dec_ms_per_launch, "dec_bytes_per_launch": dec_bytes_per_launch,
+        "replays": reps, "clocks": clocks, "equivalent_bits": cache.equivalent_bits(),
+    }
+    del kin, vin, qin, g
 
     # ---- end to end through the public API, pinned host copies every step
-    e2e_tps = None
-    e2e_cache = None
-    if not args.no_e2e:
+    res["e2e_tps"] = None
+    res["h2d"] = L * (2 * B * Hkv * D * 2 + B * Hq * D * 2)
+    res["d2h"] = L * B * Hq * D * 4
+    if e2e:
+        cache.close()
+        del cache
+        torch.cuda.empty_cache()
         h_k = torch.empty((nst, L, B, Hkv, 1, D), dtype=torch.float16).pin_memory()
         h_v = torch.empty_like(h_k).pin_memory()
         h_q = torch.empty((nst, L, B, Hq, D), dtype=torch.float16).pin_memory()
-        h_k.copy_(kin.cpu())
-        h_v.copy_(vin.cpu())
-        h_q.copy_(qin.cpu())
+        for s in range(nst):
+            for l in range(L):
+                k1, v1 = W.gen_kv(w, l, S0 + s, 1, device=dev)
+                h_k[s, l].copy_(k1)
+                h_v[s, l].copy_(v1)
+                h_q[s, l].copy_(W.gen_q(w, l, s, device=dev))
         h_out = torch.empty((2, L, B, Hq, D), dtype=torch.float32).pin_memory()  # two readback slots
         e2e_cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, cap, device=dev)
         with torch.cuda.stream(stream):
             for l in range(L):
-                k, v = W.gen_kv(w, l, 0, w.context, device=dev)
+                k, v = W.gen_kv(w, l, 0, S0, device=dev)
                 e2e_cache.append(l, k, v, stream=stream)
                 del k, v
             stream.synchronize()
@@ -451,58 +566,106 @@ def run_gpu(args):
         t1 = time.perf_counter()
         _barrier(world)
         e2e_s = _max_over_ranks(t1 - t0, world)
-        e2e_tps = world * B * steps / e2e_s
-    h2d = L * (2 * B * Hkv * D * 2 + B * Hq * D * 2)
-    d2h = L * B * Hq * D * 4
-    err = cache.device_error(stream) | (e2e_cache.device_error(stream) if e2e_cache is not None else 0)
-    if err:
-        raise RuntimeError(f"device error word {err}")
+        res["e2e_tps"] = world * B * steps / e2e_s
+        if e2e_cache.device_error(stream):
+            raise RuntimeError("device error word set (end-to-end leg)")
+        e2e_cache.close()
+    else:
+        cache.close()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_gpu(args):
+    import torch
+
+    from mixed_precision_quantized_quant_gb300 import kvq as K
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K.load()
+    w = _with_key_mode(W.workload(args.workload), args)
+    if args.layers:  # profiling runs: the workload's first N layers
+        w = W.scaled(w, num_layers=args.layers, layers=tuple(w.layers[:args.layers]))
+    m = measure_decode(w, args, dev, world, e2e=not args.no_e2e)
 
     peak, peak_kind = _peaks()
-    achieved = dec_bytes_per_launch / (dec_ms_per_launch / 1e3) / 1e9
+    achieved = m["dec_bytes_per_launch"] / (m["dec_ms_per_launch"] / 1e3) / 1e9
     # the committed capture covers every layer of the workload: no figure for a layer subset
     traffic = None if args.layers else _ncu_traffic(w.name)
+    L = w.num_layers
+    bytes_step = m["bytes_step"]
     result = {
         "metric": METRIC,
-        "value": round(tokens_per_s, 1),
+        "value": round(m["tokens_per_s"], 1),
         "unit": "tokens/s",
         "n_gpus": world,
-        "steps": steps,
-        "warmup": warm,
-        "ms_per_step": round(ms_step, 5),
+        "steps": m["steps"],
+        "warmup": m["warmup"],
+        "ms_per_step": round(m["ms_step"], 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16 codes/fp32 accumulate",
         "data": "synthetic (seeded: keys N(mu_c, sigma_c) with channel outliers, values with drifting mean)",
-        "config": {**w.describe(), "equivalent_bits": round(cache.equivalent_bits(), 5),
+        "config": {**w.describe(), "prefill": m["prefill"], "equivalent_bits": round(m["equivalent_bits"], 5),
                    "parallelism": f"replicas x{world} (independent (batch, kv head) units, no collective)",
+                   "window": (f"steps {m['warmup'] + 1}..{m['warmup'] + m['steps']} after a {m['prefill']}-token "
+                              f"prefill; step {m['warmup'] + m['step_ms']['flush_step_index'] + 1} brings every "
+                              f"layer to a multiple of G tokens and flushes a key group (quantize + pack)"),
                    "l2": ("inputs larger than L2: %.2f GB of cache read per step" % (bytes_step / 1e9)
                           if bytes_step > L2_BYTES else
                           "cache smaller than L2 (%.3f MB read per step), not flushed: a latency figure"
                           % (bytes_step / 1e6))},
-        "cache_read_gbs": round(bytes_step / (ms_step / 1e3) / 1e9, 1),
-        "cache_read_frac_of_peak": round(bytes_step / (ms_step / 1e3) / 1e9 / peak, 4),
-        "append_prefill_gbs": round(prefill_bytes / (prefill_ms / 1e3) / 1e9, 1),
+        "step_ms": m["step_ms"],
+        "cache_read_gbs": round(bytes_step / (m["ms_step"] / 1e3) / 1e9, 1),
+        "cache_read_frac_of_peak": round(bytes_step / (m["ms_step"] / 1e3) / 1e9 / peak, 4),
+        "append_prefill_gbs": round(m["append_gbs"], 1),
+        "append_prefill_frac_of_peak": round(m["append_gbs"] / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_kernel (all layers, decode-only graph replay)",
-                     "bytes_per_launch": int(dec_bytes_per_launch),
-                     "us_per_launch": round(dec_ms_per_launch * 1e3, 3),
-                     "peak_source": f"{peak_kind} HBM copy bandwidth"},
-        "e2e": None if e2e_tps is None else {"value": round(e2e_tps, 1), "unit": "tokens/s",
-                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": gpu_launches,
-        "clocks": clocks,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "kernel": "decode_kernel (all layers, decode-only graph replay, median of "
+                               f"{m['replays']} replays)",
+                     "bytes_per_launch": int(m["dec_bytes_per_launch"]),
+                     "us_per_launch": round(m["dec_ms_per_launch"] * 1e3, 3),
+                     "peak_source": f"{peak_kind} HBM copy bandwidth (frac); frac_of_nominal against the "
+                                    f"{NOMINAL_HBM_GBS:.0f} GB/s HBM3e nominal"},
+        "e2e": None if m["e2e_tps"] is None else {"value": round(m["e2e_tps"], 1), "unit": "tokens/s",
+                                                  "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"]},
+        "gpu_launches": m["steps"] * 2 * L,
+        "clocks": m["clocks"],
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        tps, step_s, desc, errors = oracle_sample(w, budget_s=args.cpu_budget)
-        result["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                  "sample": desc, "seconds_per_step": round(step_s, 2)}
-        result["quant_error"] = {"per_pair": errors,
-                                 "of": "one sampled (batch, kv head) unit at full context, first query; "
-                                       "e_k, e_v over its quantized tokens, e_a and e_o against fp64 "
-                                       "attention over the fp16 K and V (KVTuner A3)"}
+    # the other decode workloads, measured in the same run (no end-to-end leg)
+    extra = {}
+    if not args.layers:
+        for idx in args.extra_workloads:
+            if idx == args.workload:
+                continue
+            wx = _with_key_mode(W.workload(idx), args)
+            mx = measure_decode(wx, args, dev, world, e2e=False)
+            ax = mx["dec_bytes_per_launch"] / (mx["dec_ms_per_launch"] / 1e3) / 1e9
+            extra[wx.name] = {"tokens_per_s": round(mx["tokens_per_s"], 1), "ms_per_step": round(mx["ms_step"], 5),
+                              "step_ms": mx["step_ms"], "prefill": mx["prefill"],
+                              "decode_kernel_gbs": round(ax, 1), "decode_kernel_frac": round(ax / peak, 4),
+                              "append_prefill_gbs": round(mx["append_gbs"], 1),
+                              "append_prefill_frac_of_peak": round(mx["append_gbs"] / peak, 4),
+                              "clocks": mx["clocks"]}
+    if extra:
+        result["other_workloads"] = extra
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, step_s, cores, desc = oracle_sample(w, budget_s=args.cpu_budget, prefill=m["prefill"])
+        result["cpu_baseline"] = {"value": round(tps, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                  "sample": desc, "seconds_per_sample_step": round(step_s, 3)}
+        result["quant_error"] = {"per_pair": quant_errors(w),
+                                 "of": "one (batch, kv head) unit at full context, first query; e_k, e_v over "
+                                       "its quantized tokens, e_a and e_o against fp64 attention over the fp16 "
+                                       "K and V (KVTuner A3)"}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -775,22 +938,26 @@ def run_reference(args):
     if rank != 0:
         return
     w = _with_key_mode(W.workload(args.workload), args)
-    smp = OracleSampler(w)
-    vals = []
-    for s in range(args.warmup + args.steps):
-        step_s = smp.step()
-        if s >= args.warmup:
-            vals.append(step_s)
-    step_s = statistics.median(vals)
-    v = w.batch / step_s
+    S0, _ = _prefill_length(w, args.warmup, args.steps)
+    smp = OracleSampler(w, prefill=S0)
+    try:
+        for _ in range(args.warmup):
+            smp.step()
+        vals = [smp.step() for _ in range(args.steps)]
+    finally:
+        smp.close()
+    total = sum(vals)
+    step_s = total / args.steps
+    v = smp.tokens_per_s(step_s)
     print(json.dumps({
         "impl": "reference",
         "metric": METRIC, "value": round(v, 6), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 1), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 quantizer / f64 attention",
-        "data": "synthetic", "config": w.describe(),
-        "cpu_baseline": {"value": round(v, 6), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": smp.desc + "; each step is one sampled unit-step per layer type"},
+        "data": "synthetic (seeded: keys N(mu_c, sigma_c) with channel outliers, values with drifting mean)",
+        "config": {**w.describe(), "prefill": S0},
+        "cpu_baseline": {"value": round(v, 6), "unit": "tokens/s", "cores": smp.procs, "kind": "oracle",
+                         "sample": smp.desc + f"; {args.steps} timed sample steps after {args.warmup} warm-up"},
         "e2e": {"value": round(v, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -825,8 +992,13 @@ def main():
     ap.add_argument("--steps", type=int, default=120)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    ap.add_argument("--workload", type=int, default=2, help="1..5; 2 is the Llama-3.1-8B-shaped decode")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--workload", type=int, default=None,
+                    help="1..6; decode default 5, the Llama-2-70B-shaped 32K-context decode (the largest); "
+                         "chunk default 2, the Llama-3.1-8B-shaped prefill")
+    ap.add_argument("--extra-workloads", type=lambda x: [int(t) for t in x.split(",") if t], default=[2],
+                    help="comma-separated workloads measured after the main one and reported under "
+                         "other_workloads (decode only; empty to skip)")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="profiling runs: skip the end-to-end leg")
     ap.add_argument("--layers", type=int, default=0, help="profiling runs: only the workload's first N layers")
@@ -840,6 +1012,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload is None:
+        args.workload = 2 if args.op == "chunk" else 5
     if args.op == "chunk" and args.steps == 120:
         args.steps = 5  # a chunk step is a whole-model prefill attention
     if args.impl == "reference":

@@ -105,3 +105,20 @@ def test_peaks_measured_and_fallback(tmp_path, monkeypatch):
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6770.5, "bf16_tflops": 1890.1}))
     assert bench._peaks() == (6770.5, "measured")
     assert bench._tensor_peak() == (1890.1, "measured")
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("warm,steps", [(3, 1), (3, 2), (5, 20), (8, 120), (3, 300)])
+def test_prefill_offset_puts_a_flush_of_every_layer_in_the_window(index, warm, steps):
+    # the middle timed step quantizes a key group on every layer (flush rule
+    # replayed by the oracle's token-by-token state machine)
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+    from oracle import kvq_oracle as O
+    w = W.workload(index)
+    S0, mid = bench._prefill_length(w, warm, steps)
+    assert warm < mid <= warm + steps
+    assert 0 <= w.context - S0 < w.group_size
+    for R in {spec[2] for spec in w.layers}:
+        before, _ = O.flush_state(S0 + mid - 1, R, w.group_size)
+        after, _ = O.flush_state(S0 + mid, R, w.group_size)
+        assert after == before + w.group_size
