@@ -37,6 +37,15 @@ design notes):
 * streaming: tokens enter an FP16 residual window of R_l tokens; whenever the
   window holds R_l or more tokens the oldest G are quantized as one key group
   (keys per channel over those G tokens, values per token).
+* KVmix's dynamic window (RPC: num_RPC = floor(r x current_RPC), shrinking as
+  decoding proceeds): a layer with an RPC ratio of p percent keeps a window
+  bound C, first R_l (the prefill's p% of the prompt).  When a single-token
+  (decode) append brings the window to C or more tokens, the bound becomes
+  C' = G * max(1, floor(p * C / (100 * G))) -- the ratio applied to the FP16
+  tokens held, rounded down to whole key groups and never below one group --
+  and then the oldest G are quantized while the window holds C' or more.
+  Multi-token appends (prefill, chunks) keep the current bound.  The ring
+  keeps its R_l slots (token i in slot i mod R_l), since C <= R_l.
 
 Layout of the quantized cache (mirrored by the CUDA path):
 
@@ -275,6 +284,13 @@ def gqa_attention_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarra
 # Streaming state machine ([KIVI notes] 6.2; [KVmix] 关键设计 3)
 # --------------------------------------------------------------------------
 
+def shrink_bound(bound: int, rpc_percent: int, group: int) -> int:
+    """KVmix 关键设计 3: num_RPC = floor(r x current_RPC) with r the layer's RPC
+    ratio (percent here) and current_RPC the FP16 tokens held (the bound C when
+    a decode step reaches it), rounded down to whole key groups, at least one."""
+    return group * max(1, (rpc_percent * bound) // (100 * group))
+
+
 def flush_state(total: int, residual: int, group: int) -> Tuple[int, int]:
     """(quantized tokens, residual tokens) after ``total`` appended tokens,
     found by replaying the rule token by token: append, then while the
@@ -357,12 +373,17 @@ class OracleLayerCache:
     units, fed in token order."""
 
     def __init__(self, batch: int, n_kv_heads: int, head_dim: int, group: int,
-                 k_bits: int, v_bits: int, residual: int, key_mode: int = KEY_PER_CHANNEL):
+                 k_bits: int, v_bits: int, residual: int, key_mode: int = KEY_PER_CHANNEL,
+                 rpc_percent: int = 0):
         if residual < group:
             raise ValueError("residual window must hold at least one key group")
+        if not 0 <= rpc_percent <= 100:
+            raise ValueError("RPC ratio is a percentage")
         self.B, self.H, self.d, self.G = batch, n_kv_heads, head_dim, group
-        self.kb, self.vb, self.R = k_bits, v_bits, residual
+        self.kb, self.vb, self.R = k_bits, v_bits, residual  # R: ring slots, the first bound
         self.key_mode = key_mode
+        self.rpc = rpc_percent  # 0: static window of R tokens
+        self.bound = residual   # the window bound C
         self.total = 0
         self.n_q = 0
         # per unit: list of group records; pending fp16 tokens (oldest first)
@@ -378,7 +399,9 @@ class OracleLayerCache:
         self.pend_k = np.concatenate([self.pend_k, k], axis=1)
         self.pend_v = np.concatenate([self.pend_v, v], axis=1)
         self.total += n
-        while self.pend_k.shape[1] >= self.R:
+        if n == 1 and self.rpc > 0 and self.pend_k.shape[1] >= self.bound:
+            self.bound = shrink_bound(self.bound, self.rpc, self.G)  # a decode step reached the bound
+        while self.pend_k.shape[1] >= self.bound:
             for u in range(self.B * self.H):
                 self.records[u].append(build_group_record(
                     self.pend_k[u, : self.G], self.pend_v[u, : self.G], self.kb, self.vb, self.key_mode))

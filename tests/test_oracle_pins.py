@@ -59,7 +59,7 @@ def test_equivalent_bits(golden_dir):
 
 def test_equivalent_bits_workloads():
     from mixed_precision_quantized_quant_gb300 import workloads as W
-    eq = [O.equivalent_bits([(kb, vb) for kb, vb, _ in W.workload(i).layers]) for i in range(1, 6)]
+    eq = [O.equivalent_bits([tuple(p[:2]) for p in W.workload(i).layers]) for i in range(1, 6)]
     assert eq[0] == 3.0
     assert eq[1] == 111 / 32 and round(eq[1], 2) == 3.47
     assert eq[2] == 4.0
@@ -622,3 +622,78 @@ def test_chunk_attention_rejects_bad_lengths():
     c.append(np.zeros((1, 1, 5, 64), np.float16), np.zeros((1, 1, 5, 64), np.float16))
     with pytest.raises(ValueError):
         c.attend_chunk(np.zeros((1, 1, 6, 64), np.float16))
+
+
+# ---------------------------------------------------------------- KVmix dynamic window
+
+def test_rpc_window_worked(golden_dir):
+    # token-by-token state of one unit against the hand-worked sequence; the
+    # cache holds tiny rows (d = 64) since only the counts are checked
+    rows = [tuple(int(t) for t in line.split("|")) for line in _lines(os.path.join(golden_dir, "rpc_window_worked.txt"))]
+    assert len(rows) == 11
+    for pct, R in sorted({(r[0], r[1]) for r in rows}):
+        want = {r[2]: r[3:] for r in rows if r[:2] == (pct, R)}
+        c = O.OracleLayerCache(1, 1, 64, 32, 2, 2, R, rpc_percent=pct)
+        rng = np.random.default_rng(pct)
+        c.append(rng.standard_normal((1, 1, 4096, 64)).astype(np.float16),
+                 rng.standard_normal((1, 1, 4096, 64)).astype(np.float16))
+        for step in range(max(want) + 1):
+            if step:
+                c.append(rng.standard_normal((1, 1, 1, 64)).astype(np.float16),
+                         rng.standard_normal((1, 1, 1, 64)).astype(np.float16))
+            if step in want:
+                assert (c.n_q, c.r, c.bound) == want[step], (pct, step)
+            assert c.r < c.bound and c.n_q + c.r == 4096 + step
+
+
+def test_rpc_shrink_bound_closed_form():
+    # G * max(1, floor(p * C / (100 G))): a multiple of G, at least G, at most C
+    for G in (32, 64, 128):
+        for p in (1, 10, 20, 50, 100):
+            for C in range(G, 40 * G + 1, G):
+                b = O.shrink_bound(C, p, G)
+                assert b % G == 0 and G <= b <= C
+                assert b == G * max(1, (p * C) // (100 * G))
+    assert O.shrink_bound(800, 20, 32) == 160 and O.shrink_bound(384, 10, 32) == 32
+
+
+def test_rpc_zero_is_the_static_window():
+    # p = 0 keeps the bound at R: the same records and window as the plain cache
+    rng = np.random.default_rng(3)
+    a = O.OracleLayerCache(1, 2, 64, 32, 4, 2, 96)
+    b = O.OracleLayerCache(1, 2, 64, 32, 4, 2, 96, rpc_percent=0)
+    for n in [100, 1, 1, 40, 1] + [1] * 70:
+        k = rng.standard_normal((1, 2, n, 64)).astype(np.float16)
+        v = rng.standard_normal((1, 2, n, 64)).astype(np.float16)
+        a.append(k, v)
+        b.append(k, v)
+        assert (a.n_q, a.r) == (b.n_q, b.r) == O.flush_state(a.total, 96, 32)
+    assert a.records == b.records and b.bound == 96
+
+
+def test_rpc_records_and_ring_after_a_shrink():
+    # the groups quantized in one shrinking step are the oldest window tokens in
+    # order, each a plain group record; the live window keeps ring slots i mod R
+    rng = np.random.default_rng(5)
+    G, R, d = 32, 160, 64
+    c = O.OracleLayerCache(1, 1, d, G, 4, 2, R, rpc_percent=20)
+    toks_k, toks_v = [], []
+    def push(n):
+        k = rng.standard_normal((1, 1, n, d)).astype(np.float16)
+        v = rng.standard_normal((1, 1, n, d)).astype(np.float16)
+        toks_k.append(k[0, 0]); toks_v.append(v[0, 0])
+        c.append(k, v)
+    push(300)                      # 300 - 32k < 160 at k = 5: quantized 160, window 140
+    assert (c.n_q, c.r, c.bound) == (160, 140, 160)
+    for _ in range(20):            # the 20th step brings the window to 160 -> bound 32, 5 groups
+        push(1)
+    assert (c.n_q, c.r, c.bound) == (320, 0, 32)
+    allk, allv = np.concatenate(toks_k), np.concatenate(toks_v)
+    for j, rec in enumerate(c.records[0]):
+        assert rec == O.build_group_record(allk[j * G:(j + 1) * G], allv[j * G:(j + 1) * G], 4, 2)
+    push(1)
+    push(1)
+    allk = np.concatenate(toks_k)
+    rk, _ = c.residual_ring(0)
+    assert (c.n_q, c.r) == (320, 2)
+    assert (rk[320 % R] == allk[320]).all() and (rk[321 % R] == allk[321]).all()
