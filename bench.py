@@ -160,8 +160,8 @@ def _oracle_worker(conn, jobs):
     token, then fp64 attention over the dequantized cache)."""
     from oracle import kvq_oracle as O
     caches = []
-    for d, G, kb, vb, R, km, k, v in jobs:
-        c = O.OracleLayerCache(1, 1, d, G, kb, vb, R, km)
+    for d, G, kb, vb, R, km, rpc, k, v in jobs:
+        c = O.OracleLayerCache(1, 1, d, G, kb, vb, R, km, rpc)
         c.append(k, v)
         caches.append(c)
     conn.send("ready")
@@ -204,10 +204,9 @@ class OracleSampler:
         per = [[] for _ in range(self.procs)]
         self.owner = []
         for i, l in enumerate(self.layers):
-            kb, vb, R = w.layers[l][:3]
-            km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
+            kb, vb, R, km, rpc = W.spec_fields(w.layers[l])
             k, v = W.gen_kv(self.unit_w, l, 0, self.S)
-            per[i % self.procs].append((w.head_dim, w.group_size, kb, vb, R, km, k.numpy(), v.numpy()))
+            per[i % self.procs].append((w.head_dim, w.group_size, kb, vb, R, km, rpc, k.numpy(), v.numpy()))
             self.owner.append(i % self.procs)
         self.per = [[i for i in range(self.n_s) if self.owner[i] == p] for p in range(self.procs)]
         # spawned workers, single-threaded numpy (a forked child of a CUDA
@@ -285,9 +284,8 @@ def quant_errors(w):
         if spec in seen:
             continue
         seen.add(spec)
-        kb, vb, R = spec[:3]
-        km = spec[3] if len(spec) > 3 else 0
-        ora = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km)
+        kb, vb, R, km, rpc = W.spec_fields(spec)
+        ora = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km, rpc)
         k16, v16 = W.gen_kv(unit_w, l, 0, w.context)
         ora.append(k16.numpy(), v16.numpy())
         kh, vh = ora.dequantized(0)
@@ -337,7 +335,8 @@ def _with_key_mode(w, args):
     from mixed_precision_quantized_quant_gb300 import workloads as W
     if any(l[0] == 3 for l in w.layers):
         raise SystemExit("per-token keys need 2, 4 or 8-bit keys; this workload has 3-bit keys")
-    return W.scaled(w, name=w.name + "-per-token-keys", layers=tuple((kb, vb, r, 1) for kb, vb, r in w.layers))
+    return W.scaled(w, name=w.name + "-per-token-keys",
+                    layers=tuple((kb, vb, r, 1, rpc) for kb, vb, r, _, rpc in map(W.spec_fields, w.layers)))
 
 
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal: context for the measured-copy fraction
@@ -737,9 +736,8 @@ class ChunkOracleSampler:
         self.caches, self.q = {}, {}
         rng = np.random.default_rng(7)
         for l in self.layers:
-            kb, vb, R = w.layers[l][:3]
-            km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
-            ora = O.OracleLayerCache(1, 1, D, w.group_size, kb, vb, R, km)
+            kb, vb, R, km, rpc = W.spec_fields(w.layers[l])
+            ora = O.OracleLayerCache(1, 1, D, w.group_size, kb, vb, R, km, rpc)
             k, v = W.gen_kv(uw, l, 0, T)
             ora.append(k.numpy(), v.numpy())
             self.caches[l] = ora

@@ -16,7 +16,9 @@
  *     KV Cache 量化：KIVI 与误差累积", sections 6.1 and 6.2);
  *   - the most recent tokens stay in an FP16 residual window of R_l tokens;
  *     when the window holds R_l or more tokens the oldest G are quantized as one
- *     key group (KIVI notes section 6.2; KVmix 关键设计 3);
+ *     key group (KIVI notes section 6.2; KVmix 关键设计 3); with an RPC ratio
+ *     (KVmix 关键设计 3, num_RPC = floor(r x current_RPC)) the window bound
+ *     shrinks as decoding proceeds (see kvq_layer_cfg.rpc_percent);
  *   - decode attention a = softmax(q K^T / sqrt(d)), o = a V runs over the
  *     quantized tokens (dequantized on the fly) and the FP16 window, after the
  *     new token has been appended (KVTuner section A3 equation).
@@ -68,12 +70,22 @@ typedef enum {
 
 /* One layer's static precision pair, key mode and FP16 residual window (tokens).
  * k_bits, v_bits in {2, 3, 4, 8}; residual >= group_size and a multiple of it.
- * key_mode KVQ_KEY_PER_TOKEN with k_bits = 3 is KVQ_ERR_UNSUPPORTED. */
+ * key_mode KVQ_KEY_PER_TOKEN with k_bits = 3 is KVQ_ERR_UNSUPPORTED.
+ *
+ * rpc_percent (0..100; KVQ_ERR_ARG above 100) is KVmix's RPC ratio (关键设计 3:
+ * num_RPC = floor(r x current_RPC), 20% on its high-precision layers, 10% on
+ * the others, the full-precision count shrinking as decoding proceeds).  0
+ * keeps a static window of `residual` tokens.  Otherwise the layer keeps a
+ * window bound C, first `residual` (the prompt's share): any append quantizes
+ * the oldest group_size window tokens while the window holds C or more, and a
+ * single-token append that brings the window to C first sets
+ * C = group_size * max(1, floor(rpc_percent * C / (100 * group_size))).
+ * Multi-token appends keep C.  The ring keeps `residual` slots. */
 typedef struct {
   uint8_t k_bits;
   uint8_t v_bits;
-  uint8_t key_mode;  /* KVQ_KEY_PER_CHANNEL or KVQ_KEY_PER_TOKEN */
-  uint8_t reserved;  /* must be 0 */
+  uint8_t key_mode;     /* KVQ_KEY_PER_CHANNEL or KVQ_KEY_PER_TOKEN */
+  uint8_t rpc_percent;  /* 0: static window; else the RPC ratio in percent */
   int32_t residual;
 } kvq_layer_cfg;
 
@@ -112,7 +124,8 @@ typedef struct kvq_handle kvq_handle;
  *   for b = 3 word w holds channels 11w .. 11w+10, fields 0..9 3-bit at bit 3j
  *   and field 10 2-bit at bits 30..31.
  *   residual_k + u * residual_stride (and residual_v likewise) is a ring of
- *   `residual` slots of head_dim fp16; token i sits in slot i % residual, and
+ *   `residual` slots of head_dim fp16 holding the window tokens
+ *   [quantized_tokens, tokens); token i sits in slot i % residual, and
  *   the 16-byte chunk c of a slot s is stored at chunk position c ^ (s & 7). */
 typedef struct {
   int32_t k_bits, v_bits, residual, group_size, head_dim;
@@ -127,6 +140,8 @@ typedef struct {
   const void* records;
   const void* residual_k;
   const void* residual_v;
+  int32_t window_bound;              /* current window bound C (<= residual) */
+  int32_t rpc_percent;               /* the layer's RPC ratio (0: static)     */
 } kvq_layer_view;
 
 /* Bytes of device memory the caller must provide for `cfg` (0 if cfg is
@@ -143,8 +158,9 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
 
 /* Append n_tokens (>= 0) new tokens to `layer`, oldest first.
  * K, V: device, fp16, [batch][num_kv_heads][n_tokens][head_dim] contiguous,
- * read-only, caller-owned.  New tokens enter the FP16 window; every time the
- * window reaches the layer's `residual` the oldest group_size tokens are
+ * read-only, caller-owned.  New tokens enter the FP16 window; while the
+ * window holds the layer's bound (`residual`, or less after an RPC shrink,
+ * see kvq_layer_cfg) or more tokens, the oldest group_size tokens are
  * quantized (keys per channel, values per token), packed and stored as the
  * next group record, all in the launched kernels.  Used for prefill
  * (n_tokens = prompt length) and for decode (n_tokens = 1).

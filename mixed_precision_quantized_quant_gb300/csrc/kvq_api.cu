@@ -35,7 +35,8 @@ int words_per_row(int d, int b) { return b == 3 ? (d + 10) / 11 : d * b / 32; }
 bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 8; }
 
 struct LayerPlan {
-  int kb, vb, R;
+  int kb, vb, R;  // R: ring slots, the window's first bound
+  int rpc;        // RPC ratio in percent (0: static window)
   int km;  // key mode: 0 per channel over key groups, 1 per token
   int wk, wv;
   int64_t rec_bytes;
@@ -72,8 +73,9 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
   P->gqa = gqa;
   P->units = cfg->batch * cfg->num_kv_heads;
   int64_t off = 0;
-  // per layer: {append done-counter, padding to 64 B, appended-token counter per unit}
-  P->ctrl_stride = align_up(64 + static_cast<int64_t>(P->units) * 4, kAlign);
+  // per layer: {append done-counter, padding to 64 B, then per unit: appended
+  // tokens, quantized tokens, window bound}
+  P->ctrl_stride = align_up(64 + 3 * static_cast<int64_t>(P->units) * 4, kAlign);
   P->off_ctrl = off;
   off += P->ctrl_stride * P->L;
   P->off_err = off;
@@ -86,7 +88,7 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
   P->layers.clear();
   for (int l = 0; l < P->L; ++l) {
     const kvq_layer_cfg& lc = cfg->layers[l];
-    if (lc.reserved != 0) return KVQ_ERR_ARG;
+    if (lc.rpc_percent > 100) return KVQ_ERR_ARG;
     if (!bits_ok(lc.k_bits) || !bits_ok(lc.v_bits)) return KVQ_ERR_BITS;
     if (lc.key_mode != KVQ_KEY_PER_CHANNEL && lc.key_mode != KVQ_KEY_PER_TOKEN) return KVQ_ERR_ARG;
     if (lc.key_mode == KVQ_KEY_PER_TOKEN && lc.k_bits == 3) return KVQ_ERR_UNSUPPORTED;
@@ -95,6 +97,7 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
     lp.kb = lc.k_bits;
     lp.vb = lc.v_bits;
     lp.R = lc.residual;
+    lp.rpc = lc.rpc_percent;
     lp.wk = words_per_row(P->D, lp.kb);
     lp.wv = words_per_row(P->D, lp.vb);
     lp.km = lc.key_mode;
@@ -138,7 +141,10 @@ struct kvq_handle {
   Plan plan;
   int device = 0;  // the device current at kvq_create (the buffer's device)
   uint8_t* base = nullptr;
-  std::vector<int64_t> tokens;  // host mirror of each layer's appended tokens
+  // host mirror of each layer's window state (every unit of a layer agrees)
+  std::vector<int64_t> tokens;  // appended tokens
+  std::vector<int64_t> nq;      // tokens held as quantized groups
+  std::vector<int32_t> bound;   // window bound
   std::vector<kvq::DecodeKernel> dec;
   std::vector<int> grid;
   std::vector<int> app_grid;  // persistent CTAs of a prefill flush launch
@@ -150,8 +156,25 @@ namespace {
 int32_t* ctrl(kvq_handle* h, int layer) {
   return reinterpret_cast<int32_t*>(h->base + h->plan.off_ctrl + static_cast<int64_t>(layer) * h->plan.ctrl_stride);
 }
-// per-unit appended-token counters of a layer (16 ints past its done-counter)
+// per-unit counters of a layer: appended tokens (16 ints past its
+// done-counter), then quantized tokens, then the window bound
 int32_t* unit_tokens(kvq_handle* h, int layer) { return ctrl(h, layer) + 16; }
+int32_t* unit_nq(kvq_handle* h, int layer) { return unit_tokens(h, layer) + h->plan.units; }
+int32_t* unit_bound(kvq_handle* h, int layer) { return unit_nq(h, layer) + h->plan.units; }
+
+// The layer's window state after appending n tokens (host mirror).
+kvq::WindowState mirror_after(const kvq_handle* h, int layer, int n) {
+  kvq::WindowState w;
+  w.nq = h->nq[layer];
+  w.bound = h->bound[layer];
+  return kvq::window_after_append(h->tokens[layer], w, n, h->plan.G, h->plan.layers[layer].rpc);
+}
+void mirror_advance(kvq_handle* h, int layer, int n) {
+  const kvq::WindowState w = mirror_after(h, layer, n);
+  h->tokens[layer] += n;
+  h->nq[layer] = w.nq;
+  h->bound[layer] = w.bound;
+}
 int32_t* errw(kvq_handle* h) { return reinterpret_cast<int32_t*>(h->base + h->plan.off_err); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -160,8 +183,8 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   const Plan& P = h->plan;
   const LayerPlan& lp = P.layers[layer];
   const int64_t T = h->tokens[layer];
-  const int64_t nq0 = kvq::quantized_after(T, lp.R, P.G);
-  const int64_t nq1 = kvq::quantized_after(T + n, lp.R, P.G);
+  const int64_t nq0 = h->nq[layer];
+  const int64_t nq1 = mirror_after(h, layer, n).nq;
   const int64_t nflush = (nq1 - nq0) / P.G;
   const int64_t first_res = T > nq1 ? T : nq1;
   const int64_t nres = T + n - first_res;
@@ -173,6 +196,10 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   ap.units = P.units;
   ap.G = P.G;
   ap.R = lp.R;
+  ap.rpc = lp.rpc;
+  ap.T0 = static_cast<int>(T);
+  ap.nq0 = static_cast<int>(nq0);
+  ap.nq1 = static_cast<int>(nq1);
   ap.rec_bytes = static_cast<int>(lp.rec_bytes);
   ap.key_mode = lp.km;
   ap.unit_rec_stride = lp.unit_rec_stride;
@@ -181,6 +208,8 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   ap.res_v = reinterpret_cast<__half*>(h->base + lp.off_res_v);
   ap.res_stride = lp.res_stride_elems;
   ap.tokens = unit_tokens(h, layer);
+  ap.nq = unit_nq(h, layer);
+  ap.bound = unit_bound(h, layer);
   ap.done_ctr = ctrl(h, layer);
   ap.err = errw(h);
   ap.buf_lo = h->base;
@@ -188,7 +217,7 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
   const size_t smem = kvq::append_smem_bytes(lp.kb, lp.vb, P.D, P.G, static_cast<int>(lp.rec_bytes));
   cudaError_t e = cudaSuccess;
   if (n == 1) {
-    // one CTA per unit: its flush job (if a group fills) and its new token
+    // one CTA per unit: its flush jobs (if the window reaches its bound) and its new token
     ap.mode = kvq::kFlush | kvq::kResidual | kvq::kUpdateState | kvq::kPerUnit;
     ap.ctas = P.units;
     e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(P.units, 1), kvq::append_block_threads(P.G), smem, s);
@@ -209,7 +238,7 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
     }
   }
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
-  h->tokens[layer] = T + n;
+  mirror_advance(h, layer, n);
   return KVQ_OK;
 }
 
@@ -228,6 +257,7 @@ kvq_status launch_decode(kvq_handle* h, int layer, const void* q, float* out, cu
   dp.res_v = reinterpret_cast<const __half*>(h->base + lp.off_res_v);
   dp.res_stride = lp.res_stride_elems;
   dp.tokens = unit_tokens(h, layer);
+  dp.nq = unit_nq(h, layer);
   dp.partials = reinterpret_cast<float*>(h->base + P.off_partials);
   dp.counters = reinterpret_cast<int32_t*>(h->base + P.off_counters);
   dp.err = errw(h);
@@ -277,7 +307,7 @@ kvq_status launch_chunk(kvq_handle* h, int layer, const void* q, int n, float* o
   cp.err = errw(h);
   cp.n = n;
   cp.T = static_cast<int>(h->tokens[layer]);
-  cp.n_q = static_cast<int>(kvq::quantized_after(h->tokens[layer], lp.R, P.G));
+  cp.n_q = static_cast<int>(h->nq[layer]);
   cp.Hq = P.Hq;
   cp.kv_heads = P.Hkv;
   cp.gqa = P.gqa;
@@ -345,6 +375,9 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
   h->device = dev;
   h->base = static_cast<uint8_t*>(dev_buf);
   h->tokens.assign(P.L, 0);
+  h->nq.assign(P.L, 0);
+  h->bound.assign(P.L, 0);
+  for (int l = 0; l < P.L; ++l) h->bound[l] = P.layers[l].R;
   for (int l = 0; l < P.L; ++l) {
     const LayerPlan& lp = P.layers[l];
     kvq::DecodeKernel k = kvq::decode_select(lp.kb, lp.vb, P.D, P.gqa, lp.km);
@@ -364,7 +397,13 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
     }
     h->app_grid.push_back(sms * aocc);
   }
+  // zero everything, then set every unit's window bound to its layer's R_l
+  std::vector<int32_t> ctrl_init(static_cast<size_t>(P.ctrl_stride * P.L / 4), 0);
+  for (int l = 0; l < P.L; ++l)
+    for (int u = 0; u < P.units; ++u)
+      ctrl_init[static_cast<size_t>(l * P.ctrl_stride / 4 + 16 + 2 * P.units + u)] = P.layers[l].R;
   if (cudaMemset(dev_buf, 0, static_cast<size_t>(P.total)) != cudaSuccess ||
+      cudaMemcpy(h->base + P.off_ctrl, ctrl_init.data(), ctrl_init.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     delete h;
     return KVQ_ERR_CUDA;
@@ -444,7 +483,8 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
       cudaGraphExecDestroy(h->graph.exec);
       h->graph.exec = nullptr;
     }
-    std::vector<int64_t> saved = h->tokens;
+    const std::vector<int64_t> saved_t = h->tokens, saved_q = h->nq;
+    const std::vector<int32_t> saved_b = h->bound;
     if (!h->graph.aux) {
       if (cudaStreamCreateWithFlags(&h->graph.aux, cudaStreamNonBlocking) != cudaSuccess) return KVQ_ERR_CUDA;
       h->graph.ev.assign(L + 1, nullptr);
@@ -472,7 +512,9 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
     }
     cudaGraph_t graph = nullptr;
     const cudaError_t ec = cudaStreamEndCapture(s, &graph);
-    h->tokens = saved;
+    h->tokens = saved_t;
+    h->nq = saved_q;
+    h->bound = saved_b;
     if (st != KVQ_OK || ec != cudaSuccess) {
       if (graph) cudaGraphDestroy(graph);
       return st != KVQ_OK ? st : KVQ_ERR_CUDA;
@@ -486,7 +528,7 @@ kvq_status kvq_decode_step(kvq_handle* h, const void* const* K, const void* cons
     h->graph.key = key;
   }
   if (cudaGraphLaunch(h->graph.exec, s) != cudaSuccess) return KVQ_ERR_CUDA;
-  for (int l = 0; l < L; ++l) h->tokens[l] += 1;
+  for (int l = 0; l < L; ++l) mirror_advance(h, l, 1);
   return KVQ_OK;
 }
 
@@ -507,8 +549,10 @@ kvq_status kvq_layer_view_get(const kvq_handle* h, int layer, kvq_layer_view* v)
   v->unit_record_stride = lp.unit_rec_stride;
   v->residual_stride = lp.res_stride_elems * 2;
   v->tokens = h->tokens[layer];
-  v->quantized_tokens = kvq::quantized_after(h->tokens[layer], lp.R, P.G);
+  v->quantized_tokens = h->nq[layer];
   v->residual_tokens = v->tokens - v->quantized_tokens;
+  v->window_bound = h->bound[layer];
+  v->rpc_percent = lp.rpc;
   v->records = h->base + lp.off_records;
   v->residual_k = h->base + lp.off_res_k;
   v->residual_v = h->base + lp.off_res_v;
@@ -527,7 +571,7 @@ int64_t kvq_decode_bytes(const kvq_handle* h, int layer) {
   const Plan& P = h->plan;
   const LayerPlan& lp = P.layers[layer];
   const int64_t T = h->tokens[layer];
-  const int64_t nq = kvq::quantized_after(T, lp.R, P.G);
+  const int64_t nq = h->nq[layer];
   const int64_t r = T - nq;
   const int64_t per_unit = (nq / P.G) * lp.rec_bytes + r * 4LL * P.D;
   return P.units * per_unit + static_cast<int64_t>(P.B) * P.Hq * P.D * (2 + 4);
@@ -652,6 +696,7 @@ extern "C" kvq_status kvq_decode_attn_noalloc(kvq_handle* h, int layer, const vo
   dp.res_v = reinterpret_cast<const __half*>(h->base + lp.off_res_v);
   dp.res_stride = lp.res_stride_elems;
   dp.tokens = unit_tokens(h, layer);
+  dp.nq = unit_nq(h, layer);
   dp.partials = reinterpret_cast<float*>(scratch + counter_bytes);
   dp.counters = counters;
   dp.err = errw(h);

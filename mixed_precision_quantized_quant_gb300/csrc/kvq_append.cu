@@ -551,27 +551,65 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
     const __half* in = tid >= CH ? p.V : p.K;
     newrow = __ldg(reinterpret_cast<const uint4*>(in + static_cast<int64_t>(blockIdx.x) * D) + (tid % CH));
   }
-  // the token count, read once per CTA so that every thread works from the
-  // same value even if a misordered launch changes it meanwhile
-  __shared__ int t_shared;
-  if (tid == 0) t_shared = __ldcg(p.tokens + (per_unit ? blockIdx.x : 0));
+  // The window state.  A single-token append (one CTA per unit) reads its
+  // unit's (tokens, quantized, bound) once per CTA, so that every thread works
+  // from the same values even if a misordered launch changes them meanwhile,
+  // and steps it (a decode step may shrink the bound and quantize several
+  // groups).  A multi-token append takes the host's state.
+  __shared__ int st_shared[4];
+  if (tid == 0) {
+    if (per_unit) {
+      const int u = blockIdx.x;
+      const int t = __ldcg(p.tokens + u);
+      WindowState w0;
+      w0.nq = __ldcg(p.nq + u);
+      w0.bound = __ldcg(p.bound + u);
+      const WindowState w1 = window_after_append(t, w0, 1, p.G, p.rpc);
+      st_shared[0] = t;
+      st_shared[1] = static_cast<int>(w0.nq);
+      st_shared[2] = static_cast<int>(w1.nq);
+      st_shared[3] = w1.bound;
+    } else {
+      st_shared[0] = p.T0;
+      st_shared[1] = p.nq0;
+      st_shared[2] = p.nq1;
+      st_shared[3] = 0;
+    }
+  }
   __syncthreads();
-  const int T = t_shared;
-  const int nq0 = static_cast<int>(quantized_after(T, p.R, p.G));
-  const int nq1 = static_cast<int>(quantized_after(T + p.n, p.R, p.G));
+  const int T = st_shared[0];
+  const int nq0 = st_shared[1];
+  const int nq1 = st_shared[2];
 
   if (p.mode & kFlush) {
-    // jobs j = (unit j / nflush, group nq0/G + j % nflush), CTA-strided
+    // jobs: a single-token append's CTA quantizes its unit's groups nq0/G ..
+    // nq1/G - 1 in order; a multi-token append's job j is (unit j / nflush,
+    // group nq0/G + j % nflush), CTA-strided.  job(k) is this CTA's k-th job.
     const AppendSmem L = append_smem_layout(D, p.G, p.rec_bytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
     const int nflush = (nq1 - nq0) / p.G;
-    const int njobs = nflush * p.units;
+    const int njobs = per_unit ? nflush : nflush * p.units;
     const uint32_t tile = static_cast<uint32_t>(L.tile);
-    // stage the K and V rows of job j: ring rows first (slots of a group are
+    auto job_valid = [&](int k) {
+      return per_unit ? k < njobs : static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x) < njobs;
+    };
+    auto job_of = [&](int k, int& u, int& grp) {
+      if (per_unit) {
+        u = blockIdx.x;
+        grp = nq0 / p.G + k;
+      } else {
+        const int j = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+        u = j / nflush;
+        grp = nq0 / p.G + (j - u * nflush);
+      }
+    };
+    // stage the K and V rows of job k: ring rows first (slots of a group are
     // contiguous: the group starts at a multiple of G and R is one too), then
     // rows of this call's input
-    auto issue = [&](int j, int st) {
-      const int u = j / nflush, t0 = (nq0 / p.G + (j - u * nflush)) * p.G;
+    auto issue = [&](int k, int st) {
+      int u, grp;
+      job_of(k, u, grp);
+      const int t0 = grp * p.G;
       const int nring = T > t0 ? (T - t0 < p.G ? T - t0 : p.G) : 0;
       uint8_t* ks = smem + st * L.off_stage1;
       uint8_t* vs = ks + tile;
@@ -604,14 +642,14 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
       mbar_init(&bars[0], 1);
       mbar_init(&bars[1], 1);
       fence_mbar_init();
-      if (static_cast<int>(blockIdx.x) < njobs) issue(blockIdx.x, 0);
-      if (static_cast<int>(blockIdx.x + gridDim.x) < njobs) issue(blockIdx.x + gridDim.x, 1);
+      if (job_valid(0)) issue(0, 0);
+      if (job_valid(1)) issue(1, 1);
     }
     __syncthreads();
-    int k = 0;
-    for (int j = blockIdx.x; j < njobs; j += gridDim.x, ++k) {
+    for (int k = 0; job_valid(k); ++k) {
       const int st = k & 1;
-      const int u = j / nflush, grp = nq0 / p.G + (j - u * nflush);
+      int u, grp;
+      job_of(k, u, grp);
       const int t0 = grp * p.G;
       const int nring = T > t0 ? (T - t0 < p.G ? T - t0 : p.G) : 0;
       const bool ok = mbar_wait(&bars[st], static_cast<uint32_t>((k >> 1) & 1), p.err);
@@ -619,8 +657,7 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
       if (!flush_group<KB, VB, D>(p, kt, kt + p.G * D, nring, smem, L, ok)) {
         // a copy never landed (all threads agree): give the other stage's copy
         // its bounded wait, then stop
-        const int jn = j + static_cast<int>(gridDim.x);
-        if (jn < njobs) mbar_wait(&bars[st ^ 1], static_cast<uint32_t>(((k + 1) >> 1) & 1), p.err);
+        if (job_valid(k + 1)) mbar_wait(&bars[st ^ 1], static_cast<uint32_t>(((k + 1) >> 1) & 1), p.err);
         break;
       }
       __syncthreads();  // stage and record staging complete
@@ -630,8 +667,7 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
         if (in_range(dst, static_cast<size_t>(p.rec_bytes), p.buf_lo, p.buf_hi, p.err))  // debug builds
           bulk_s2g(dst, smem + L.off_rec, static_cast<uint32_t>(p.rec_bytes));
         bulk_commit();
-        const int jn = j + 2 * static_cast<int>(gridDim.x);
-        if (jn < njobs) issue(jn, st);
+        if (job_valid(k + 2)) issue(k + 2, st);
       }
     }
     if (tid == 0) bulk_wait_all();
@@ -656,7 +692,11 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
   if (p.mode & kUpdateState) {
     if (per_unit) {
       // the next kernel on the stream sees it; no CTA of this launch reads it again
-      if (tid == 0) p.tokens[blockIdx.x] = T + p.n;
+      if (tid == 0) {
+        p.tokens[blockIdx.x] = T + p.n;
+        p.nq[blockIdx.x] = nq1;
+        p.bound[blockIdx.x] = st_shared[3];
+      }
     } else {
       // the last CTA to finish advances every unit's counter
       __shared__ int last;
@@ -666,8 +706,11 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
         last = atomicAdd(p.done_ctr, 1) == p.ctas - 1;
       }
       __syncthreads();
-      if (last) {
-        for (int u = tid; u < p.units; u += blockDim.x) p.tokens[u] = T + p.n;
+      if (last) {  // (a multi-token append keeps the bound)
+        for (int u = tid; u < p.units; u += blockDim.x) {
+          p.tokens[u] = T + p.n;
+          p.nq[u] = nq1;
+        }
         if (tid == 0) *p.done_ctr = 0;
       }
     }

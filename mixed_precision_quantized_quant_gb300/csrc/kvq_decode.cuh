@@ -457,14 +457,16 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     grid_dep_launch();
     if (p.pdl == 1) grid_dep_wait();
   }
-  __shared__ int t_shared;
-  if (tid == 0) t_shared = __ldcg(p.tokens);
+  __shared__ int t_shared[2];
+  if (tid == 0) {
+    t_shared[0] = __ldcg(p.tokens);
+    t_shared[1] = __ldcg(p.nq);
+  }
   __syncthreads();
-  const int T = t_shared;
+  const int T = t_shared[0];
   if (T <= 0) return;
-  const int lgG = 31 - __clz(p.G);        // G is 32, 64 or 128
-  const int nq = T < p.R ? 0 : (((T - p.R) >> lgG) + 1) << lgG;  // tokens in key groups
-  const int r = T - nq;
+  const int nq = t_shared[1];             // tokens in key groups (a multiple of G)
+  const int r = T - nq;                   // tokens in the FP16 window (at most R)
   const int NS = p.G / kSlice;            // slices per key group (1, 2 or 4)
   const int lgNS = NS == 4 ? 2 : NS - 1;
   const int NG = nq / kSlice;             // quantized work items (slices)

@@ -21,12 +21,36 @@ constexpr int32_t kErrBadAddress = 3;  // debug builds: a computed access fell o
 
 // ---------------------------------------------------------------- state
 
-// Tokens held after `total` appended tokens, with a residual window of R
-// tokens and key groups of G: whenever the window holds R or more tokens the
-// oldest G are quantized.  R is a multiple of G.
-__host__ __device__ __forceinline__ int64_t quantized_after(int64_t total, int R, int G) {
-  if (total < R) return 0;
-  return (int64_t)G * ((total - R) / G + 1);
+// Window state of one (batch, kv head) unit of a layer: `nq` tokens held as
+// quantized key groups, the rest of the appended tokens in the FP16 window,
+// and the window bound (R_l at first).  After appending n tokens to T:
+//   * a single-token (decode) append that brings the window to the bound on
+//     a layer with an RPC ratio of rpc percent first shrinks the bound to
+//     G * max(1, floor(rpc * bound / (100 G))) (KVmix, 关键设计 3:
+//     num_RPC = floor(r x current_RPC), the full-precision window shrinking
+//     as decoding proceeds);
+//   * then the oldest G window tokens are quantized while the window holds
+//     the bound or more ("LLM 量化精读笔记 · 08", section 6.2: segment, then
+//     quantize).
+// The bound and R_l are multiples of G, so every group starts at a multiple
+// of G.  The host mirror and the single-token append kernel both step the
+// state with this function.
+struct WindowState {
+  int64_t nq;
+  int32_t bound;
+};
+__host__ __device__ __forceinline__ WindowState window_after_append(int64_t T, WindowState s, int n, int G,
+                                                                    int rpc) {
+  const int64_t r = T + n - s.nq;
+  int64_t b = s.bound;
+  if (n == 1 && rpc > 0 && r >= b) {
+    const int64_t k = (static_cast<int64_t>(rpc) * b) / (100LL * G);
+    b = static_cast<int64_t>(G) * (k > 1 ? k : 1);
+  }
+  WindowState o;
+  o.nq = s.nq + (r >= b ? static_cast<int64_t>(G) * ((r - b) / G + 1) : 0);
+  o.bound = static_cast<int32_t>(b);
+  return o;
 }
 
 // ---------------------------------------------------------------- params
@@ -36,7 +60,11 @@ struct AppendParams {
   const __half* V;
   int n;                  // tokens appended by this call
   int units;              // batch * kv heads
-  int G, R;
+  int G, R;               // key group; ring slots (the window's first bound, R_l)
+  int rpc;                // RPC ratio in percent (0: static window)
+  // multi-token appends: the state before the call (host mirror) and the
+  // quantized tokens after it; single-token appends read the state per unit
+  int T0, nq0, nq1;
   int rec_bytes;
   int key_mode;           // 0: keys per channel over each group; 1: keys per token
   int64_t unit_rec_stride;   // bytes
@@ -44,7 +72,9 @@ struct AppendParams {
   __half* res_k;          // [units][R][D] ring (chunk-swizzled)
   __half* res_v;
   int64_t res_stride;     // elements between units' rings
-  int32_t* tokens;        // device state: tokens appended so far, one counter per unit
+  int32_t* tokens;        // device state per unit: tokens appended so far,
+  int32_t* nq;            //   tokens held as quantized groups,
+  int32_t* bound;         //   the window bound
   int32_t* done_ctr;      // last-CTA counter of this launch
   int32_t* err;
   int mode;               // kFlush | kResidual | kUpdateState
@@ -66,13 +96,14 @@ struct DecodeParams {
   const __half* res_v;
   int64_t res_stride;     // elements
   const int32_t* tokens;  // device state: unit 0's appended-token counter (all units agree)
+  const int32_t* nq;      //   and its quantized-token counter
   float* partials;        // [slots][gqa][D + 2]
   int32_t* counters;      // [units]
   int32_t* err;
   int units;
   int kv_heads;
   int gqa;                // query heads per kv head
-  int G, R;
+  int G, R;               // key group; ring slots
   int rec_bytes;
   int grid;               // CTAs launched
   float alpha;            // log2(e) / sqrt(D)

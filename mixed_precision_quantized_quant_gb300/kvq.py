@@ -41,7 +41,7 @@ KEY_PER_CHANNEL, KEY_PER_TOKEN = 0, 1
 
 class LayerCfg(ctypes.Structure):
     _fields_ = [("k_bits", ctypes.c_uint8), ("v_bits", ctypes.c_uint8), ("key_mode", ctypes.c_uint8),
-                ("reserved", ctypes.c_uint8), ("residual", ctypes.c_int32)]
+                ("rpc_percent", ctypes.c_uint8), ("residual", ctypes.c_int32)]
 
 
 class Config(ctypes.Structure):
@@ -59,7 +59,8 @@ class LayerView(ctypes.Structure):
                 ("residual_stride", ctypes.c_int64), ("tokens", ctypes.c_int64),
                 ("quantized_tokens", ctypes.c_int64), ("residual_tokens", ctypes.c_int64),
                 ("records", ctypes.c_void_p), ("residual_k", ctypes.c_void_p),
-                ("residual_v", ctypes.c_void_p)]
+                ("residual_v", ctypes.c_void_p), ("window_bound", ctypes.c_int32),
+                ("rpc_percent", ctypes.c_int32)]
 
 
 _lib = None
@@ -116,12 +117,13 @@ def _check(st: int, where: str) -> None:
 
 def make_config(layers: Sequence[Tuple[int, ...]], batch: int, num_q_heads: int, num_kv_heads: int,
                 head_dim: int, group_size: int, max_tokens: int):
-    """layers: (k_bits, v_bits, residual) or (k_bits, v_bits, residual, key_mode) per layer."""
+    """layers: (k_bits, v_bits, residual[, key_mode[, rpc_percent]]) per layer."""
     arr = (LayerCfg * len(layers))()
     for i, spec in enumerate(layers):
         kb, vb, r = spec[:3]
         km = spec[3] if len(spec) > 3 else KEY_PER_CHANNEL
-        arr[i].k_bits, arr[i].v_bits, arr[i].key_mode, arr[i].reserved, arr[i].residual = kb, vb, km, 0, r
+        rpc = spec[4] if len(spec) > 4 else 0
+        arr[i].k_bits, arr[i].v_bits, arr[i].key_mode, arr[i].rpc_percent, arr[i].residual = kb, vb, km, rpc, r
     cfg = Config(len(layers), batch, num_q_heads, num_kv_heads, head_dim, group_size, max_tokens,
                  ctypes.cast(arr, ctypes.POINTER(LayerCfg)))
     cfg._keep = arr  # keep the layer array alive with the struct

@@ -1,7 +1,7 @@
 """Seeded synthetic workloads: per-layer precision tables and fp16 K/V/q generators.
 
 This module holds no arithmetic of the quantization method itself.  It only
-describes the five model-shaped workloads and draws their random inputs, so that
+describes the six model-shaped workloads and draws their random inputs, so that
 the CUDA path, the oracle, the tests and the benchmark all see the same bytes.
 
 Distributions (stand-ins for real-model KV, which needs weights and datasets):
@@ -30,8 +30,17 @@ from typing import List, Optional, Sequence, Tuple
 import numpy as np
 import torch
 
-# (k_bits, v_bits, residual window R_l)
-LayerSpec = Tuple[int, int, int]
+# (k_bits, v_bits, residual window R_l[, key mode[, RPC ratio in percent]])
+LayerSpec = Tuple[int, ...]
+
+
+def spec_fields(spec: Sequence[int]) -> Tuple[int, int, int, int, int]:
+    """(k_bits, v_bits, R_l, key_mode, rpc_percent) of a layer spec; the key
+    mode defaults to per channel (0) and the RPC ratio to 0 (a static window)."""
+    kb, vb, r = spec[:3]
+    km = spec[3] if len(spec) > 3 else 0
+    rpc = spec[4] if len(spec) > 4 else 0
+    return int(kb), int(vb), int(r), int(km), int(rpc)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -112,15 +121,19 @@ def qwen_like_table(seed: int, n_layers: int = 28, residual: int = 64) -> Tuple[
 
 
 def kvmix_table(seed: int, n_layers: int = 32, n_high: int = 6, context: int = 4096,
-                group_size: int = 32, high_pair: Tuple[int, int] = (4, 3)) -> Tuple[LayerSpec, ...]:
+                group_size: int = 32, high_pair: Tuple[int, int] = (4, 3),
+                ratios: Tuple[int, int] = (20, 10), dynamic: bool = True) -> Tuple[LayerSpec, ...]:
     """KVmix-style table: a seeded pick of high-precision layers (high_pair,
-    K4V3 by default) and the rest K2V2, with a per-layer FP16 residual of
-    20% / 10% of the prefill context rounded down to whole key groups."""
+    K4V3 by default) and the rest K2V2.  Each layer's FP16 window starts at its
+    RPC ratio (percent: 20 high, 10 low) of the prefill context, rounded down to
+    whole key groups; with ``dynamic`` the ratio rides along as the fifth field
+    and the window shrinks during decoding, otherwise it stays fixed."""
     rng = np.random.Generator(np.random.PCG64(seed))
     hi = set(int(x) for x in rng.choice(n_layers, n_high, replace=False))
-    r_hi = group_size * int((0.2 * context) // group_size)
-    r_lo = group_size * int((0.1 * context) // group_size)
-    return tuple((*high_pair, r_hi) if l in hi else (2, 2, r_lo) for l in range(n_layers))
+    r_hi = group_size * ((ratios[0] * context) // (100 * group_size))
+    r_lo = group_size * ((ratios[1] * context) // (100 * group_size))
+    p_hi, p_lo = ratios if dynamic else (0, 0)
+    return tuple((*high_pair, r_hi, 0, p_hi) if l in hi else (2, 2, r_lo, 0, p_lo) for l in range(n_layers))
 
 
 def _make_workloads() -> List[Workload]:

@@ -54,7 +54,7 @@ def test_cache_bytes_rejects_bad_configs(lib):
     bad = [dict(head_dim=96), dict(group_size=48), dict(num_q_heads=6, num_kv_heads=4),
            dict(num_q_heads=32, num_kv_heads=2), dict(layers=[(5, 2, 32)]), dict(layers=[(4, 2, 48)]),
            dict(layers=[(4, 2, 16)]), dict(batch=0), dict(max_tokens=0),
-           dict(layers=[(3, 2, 32, 1)]), dict(layers=[(4, 2, 32, 2)])]
+           dict(layers=[(3, 2, 32, 1)]), dict(layers=[(4, 2, 32, 2)]), dict(layers=[(4, 2, 32, 0, 101)])]
     for b in bad:
         assert K.kvq_cache_bytes(_cfg(**b)) == 0, b
 
@@ -68,7 +68,7 @@ def test_cache_bytes_covers_layout(lib):
         nb = K.kvq_cache_bytes(cfg)
         U = w.batch * w.num_kv_heads
         need = 0
-        for kb, vb, R in w.layers:
+        for kb, vb, R, _, _ in map(W.spec_fields, w.layers):
             rec = O.record_layout(w.head_dim, w.group_size, kb, vb)["bytes"]
             need += U * (w.total_tokens // w.group_size) * rec + 2 * U * R * w.head_dim * 2
         assert need <= nb <= need * 1.02 + (64 << 20), (idx, nb, need)
@@ -102,3 +102,35 @@ def test_per_token_key_layout(lib):
             lay = O.record_layout(128, 32, kb, vb, O.KEY_PER_TOKEN)
             lay0 = O.record_layout(128, 32, kb, vb)
             assert lay["bytes"] == lay0["bytes"] - 4 * 128 + 4 * 32
+
+
+def test_rpc_ratio_accepted_up_to_100(lib):
+    for pct in (0, 1, 10, 20, 100):
+        assert K.kvq_cache_bytes(_cfg(layers=[(4, 2, 160, 0, pct)])) > 0
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    # sizes and field offsets of the public structs as a C compiler lays them
+    # out from include/kvq.h, against the ctypes mirrors in the binding
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"kvq_layer_cfg": K.LayerCfg, "kvq_layer_view": K.LayerView, "kvq_config": K.Config}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "kvq.h"', "int main(void) {"]
+    for cname, py in fields.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("  return 0;\n}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l}
+    for cname, py in fields.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)

@@ -200,7 +200,7 @@ def test_chunk_full_size_workloads_sampled(idx, key_mode, n):
     its K3V4 orientation.  Sampled (unit, query) rows against fp64."""
     w = W.workload(idx)
     if key_mode:
-        w = W.scaled(w, layers=tuple((kb, vb, r, key_mode) for kb, vb, r in w.layers))
+        w = W.scaled(w, layers=tuple((kb, vb, r, key_mode, rpc) for kb, vb, r, _, rpc in map(W.spec_fields, w.layers)))
     w = W.scaled(w, batch=2)
     seen, layers = set(), []
     for l, lay in enumerate(w.layers):
@@ -212,8 +212,7 @@ def test_chunk_full_size_workloads_sampled(idx, key_mode, n):
     gen = torch.Generator(device="cuda")
     gen.manual_seed(31)
     for l in layers[:3]:
-        kb, vb, R = w.layers[l][:3]
-        km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
+        kb, vb, R, km, rpc = W.spec_fields(w.layers[l])
         cache = K.KVQCache([w.layers[l]], w.batch, Hq, Hkv, D, w.group_size, T)
         k, v = W.gen_kv(w, l, 0, T, device="cuda")
         cache.append(0, k, v)
@@ -226,7 +225,7 @@ def test_chunk_full_size_workloads_sampled(idx, key_mode, n):
         U = w.batch * Hkv
         for u in sorted({0, U - 1}):
             b, h = divmod(u, Hkv)
-            ora = O.OracleLayerCache(1, 1, D, w.group_size, kb, vb, R, km)
+            ora = O.OracleLayerCache(1, 1, D, w.group_size, kb, vb, R, km, rpc)
             ora.append(kn[b:b + 1, h:h + 1], vn[b:b + 1, h:h + 1])
             kh, vh = ora.dequantized(0)
             got, exp = [], []

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 def test_bounded_wait_reports_timeout_and_context_stays_usable():
     w = W.workload(1)
-    kb, vb, R = w.layers[0]
+    kb, vb, R = w.layers[0][:3]
     cache = K.KVQCache(w.layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.group_size, w.total_tokens)
     stream = torch.cuda.current_stream()
     for _ in range(2):

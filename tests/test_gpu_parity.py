@@ -34,12 +34,12 @@ def _rand_kv(gen, B, H, n, d, t0, total, outlier_ch=(3, 17), device="cuda"):
     return k.half().contiguous(), v.half().contiguous()
 
 
-def _run_stream(kb, vb, D, G, R, gqa, schedule, B=2, Hkv=2, attn_every=1, seed=0, key_mode=0):
+def _run_stream(kb, vb, D, G, R, gqa, schedule, B=2, Hkv=2, attn_every=1, seed=0, key_mode=0, rpc=0):
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     total = sum(schedule)
-    cache = K.KVQCache([(kb, vb, R, key_mode)], B, Hkv * gqa, Hkv, D, G, total)
-    ora = O.OracleLayerCache(B, Hkv, D, G, kb, vb, R, key_mode)
+    cache = K.KVQCache([(kb, vb, R, key_mode, rpc)], B, Hkv * gqa, Hkv, D, G, total)
+    ora = O.OracleLayerCache(B, Hkv, D, G, kb, vb, R, key_mode, rpc)
     pos = 0
     for step, n in enumerate(schedule):
         k, v = _rand_kv(gen, B, Hkv, n, D, pos, total)
@@ -48,6 +48,7 @@ def _run_stream(kb, vb, D, G, R, gqa, schedule, B=2, Hkv=2, attn_every=1, seed=0
         pos += n
         torch.cuda.synchronize()
         compare_layer(cache, 0, ora)
+        assert cache.view(0)["window_bound"] == ora.bound
         if step % attn_every == 0 or step == len(schedule) - 1:
             q = torch.randn((B, Hkv * gqa, D), generator=gen, device="cuda").half()
             out = cache.decode_attn(0, q)
@@ -98,6 +99,26 @@ def test_group_sizes_flush_boundaries(G):
         _run_stream(4, 4, 128, G, G, 4, [n0] + [1] * (G + 2), attn_every=7, seed=n0)
 
 
+@pytest.mark.parametrize("kb,vb,key_mode", [(4, 3, 0), (2, 2, 0), (3, 4, 0), (8, 4, 1)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_rpc_dynamic_window_stream(kb, vb, key_mode, D):
+    # KVmix's shrinking window: R = 160 at 20%, a prefill that leaves 140 window
+    # tokens, then decode steps: the 20th brings the window to 160, the bound
+    # becomes 32 and five groups are quantized in that one step; later steps
+    # flush one group every 32.  A 45-token chunk keeps the bound.  Records,
+    # window, bound and attention against the oracle after every call.
+    sched = [300] + [1] * 19 + [1] + [1] * 40 + [45] + [1] * 30
+    _run_stream(kb, vb, D, 32, 160, 4, sched, attn_every=3, seed=kb * 16 + vb + D, key_mode=key_mode, rpc=20)
+
+
+@pytest.mark.parametrize("G,R,rpc", [(64, 320, 10), (128, 640, 20), (32, 800, 20)])
+def test_rpc_group_sizes(G, R, rpc):
+    # shrinks at other group sizes and ratios; a prefill shorter than the
+    # window first, so the first flushes come from decode steps alone
+    sched = [R - 3] + [1] * (2 * G + 7)
+    _run_stream(4, 2, 128, G, R, 8, sched, attn_every=11, seed=G + rpc, rpc=rpc)
+
+
 def test_prefill_shorter_than_window():
     _run_stream(4, 2, 128, 32, 128, 4, [50, 1, 1, 1], attn_every=1)
 
@@ -137,7 +158,8 @@ def test_capacity_and_argument_errors():
 
 
 @pytest.mark.parametrize("layers", [((8, 4, 32), (4, 2, 32), (2, 2, 64)),
-                                    ((8, 4, 32, 1), (4, 2, 32, 0), (4, 4, 64, 1))])
+                                    ((8, 4, 32, 1), (4, 2, 32, 0), (4, 4, 64, 1)),
+                                    ((4, 3, 160, 0, 20), (2, 2, 96, 0, 10), (8, 4, 32))])
 def test_decode_step_graph_matches_layer_calls(layers):
     w = W.scaled(W.workload(2), batch=2, num_layers=3, context=200, decode_steps=40, layers=layers)
     stream = torch.cuda.Stream()
@@ -167,6 +189,9 @@ def test_decode_step_graph_matches_layer_calls(layers):
         stream.synchronize()
         for l in range(w.num_layers):
             assert torch.equal(outs_a[l], outs_b[l]), (step, l)
+            va, vb = caches[0].view(l), caches[1].view(l)
+            assert [va[k] for k in ("tokens", "quantized_tokens", "window_bound")] == \
+                [vb[k] for k in ("tokens", "quantized_tokens", "window_bound")], (step, l)
     for c in caches:
         assert c.device_error() == 0
         c.close()
@@ -225,7 +250,7 @@ def test_workload_tiny_every_step(idx):
     w = W.workload(idx)
     cache = K.KVQCache(w.layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.group_size,
                        w.total_tokens)
-    kb, vb, R = w.layers[0]
+    kb, vb, R = w.layers[0][:3]
     ora = O.OracleLayerCache(w.batch, w.num_kv_heads, w.head_dim, w.group_size, kb, vb, R)
     k, v = W.gen_kv(w, 0, 0, w.context, device="cuda")
     cache.append(0, k, v)
@@ -262,7 +287,7 @@ def test_workload_full_size_sampled(idx, key_mode):
     6: the KVmix page's own K3V4 orientation.)"""
     w = W.workload(idx)
     if key_mode:
-        w = W.scaled(w, layers=tuple((kb, vb, r, key_mode) for kb, vb, r in w.layers))
+        w = W.scaled(w, layers=tuple((kb, vb, r, key_mode, rpc) for kb, vb, r, _, rpc in map(W.spec_fields, w.layers)))
     layers = _layers_to_check(w)
     steps = min(w.decode_steps, 40)
     sub = [w.layers[l] for l in layers]
@@ -272,13 +297,12 @@ def test_workload_full_size_sampled(idx, key_mode):
     units = sorted({0, U - 1, U // 2, (U * 7) // 11})
     rep = w.num_q_heads // w.num_kv_heads
     for li, l in enumerate(layers):
-        kb, vb, R = w.layers[l][:3]
-        km = w.layers[l][3] if len(w.layers[l]) > 3 else 0
+        kb, vb, R, km, rpc = W.spec_fields(w.layers[l])
         k, v = W.gen_kv(w, l, 0, w.context, device="cuda")
         cache.append(li, k, v)
         oras = {}
         for u in units:
-            o = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km)
+            o = O.OracleLayerCache(1, 1, w.head_dim, w.group_size, kb, vb, R, km, rpc)
             o.append(*_unit_stream(k, v, u, w.num_kv_heads))
             oras[u] = o
         del k, v
