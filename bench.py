@@ -414,29 +414,44 @@ def measure_decode(w, args, dev, world, e2e=True):
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
+    # The timed window (steps warm .. warm+steps-1) runs args.reps times: the
+    # cache state after the warm-up is saved once (kvq_state_save) and restored
+    # before every repetition, so each one decodes the same tokens from the
+    # same state, flush step included.
+    reps = max(10, args.reps)
+    win_ms, step_rows = [], []
     with torch.cuda.stream(stream):
         for s in range(warm):
             run_step(s)
+        snapshot = cache.save_state(stream=stream)
         stream.synchronize()
-        _barrier(world)
-        torch.cuda.synchronize()
         nq_before = [cache.view(l)["quantized_tokens"] for l in range(L)]
         bytes_first = sum(cache.decode_bytes(l) for l in range(L))
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-        t0 = time.time()
-        evs[0].record(stream)
-        for i, s in enumerate(range(warm, warm + steps)):
-            run_step(s)
-            evs[i + 1].record(stream)
-        stream.synchronize()
-        t1 = time.time()
-        sampler.mark(t0, t1)
-        torch.cuda.synchronize()
-        _barrier(world)
+        for r in range(reps):
+            if r:
+                cache.restore_state(snapshot, stream=stream)
+            stream.synchronize()
+            _barrier(world)
+            torch.cuda.synchronize()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+            t0 = time.time()
+            evs[0].record(stream)
+            for i, s in enumerate(range(warm, warm + steps)):
+                run_step(s)
+                evs[i + 1].record(stream)
+            stream.synchronize()
+            t1 = time.time()
+            sampler.mark(t0, t1)
+            torch.cuda.synchronize()
+            _barrier(world)
+            win_ms.append(_max_over_ranks(evs[0].elapsed_time(evs[-1]), world))
+            step_rows.append([evs[i].elapsed_time(evs[i + 1]) for i in range(steps)])
         bytes_last = sum(cache.decode_bytes(l) for l in range(L))
         flushed = sum(1 for l in range(L) if cache.view(l)["quantized_tokens"] > nq_before[l])
-    ms_total = _max_over_ranks(evs[0].elapsed_time(evs[-1]), world)
-    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+        del snapshot
+    ms_total = statistics.median(win_ms)
+    # per step position: the median over the repetitions
+    step_ms = [statistics.median(row[i] for row in step_rows) for i in range(steps)]
     ms_step = ms_total / steps
     flush_i = mid - warm - 1  # 0-based index of the flush step inside the window
     others = [t for i, t in enumerate(step_ms) if i != flush_i] or step_ms
@@ -474,6 +489,8 @@ def measure_decode(w, args, dev, world, e2e=True):
     res = {
         "w": w, "steps": steps, "warmup": warm, "ms_total": ms_total, "ms_step": ms_step,
         "tokens_per_s": world * B * steps / (ms_total / 1e3),
+        "window_ms": {"median": round(ms_total, 4), "min": round(min(win_ms), 4), "max": round(max(win_ms), 4),
+                      "repetitions": reps},
         "step_ms": {"median": round(statistics.median(step_ms), 4), "mean": round(ms_step, 4),
                     "flush_step": round(step_ms[flush_i], 4) if 0 <= flush_i < steps else None,
                     "median_without_flush_step": round(statistics.median(others), 4),
@@ -559,13 +576,23 @@ def measure_decode(w, args, dev, world, e2e=True):
             down[(s + n - 1) & 1].synchronize()
 
         run(0, warm)
-        _barrier(world)
-        t0 = time.perf_counter()
-        run(warm, steps)
-        t1 = time.perf_counter()
-        _barrier(world)
-        e2e_s = _max_over_ranks(t1 - t0, world)
+        e2e_snap = e2e_cache.save_state(stream=stream)
+        e2e_win = []
+        for r in range(reps):
+            if r:
+                e2e_cache.restore_state(e2e_snap, stream=stream)
+            stream.synchronize()
+            _barrier(world)
+            t0 = time.perf_counter()
+            run(warm, steps)
+            t1 = time.perf_counter()
+            _barrier(world)
+            e2e_win.append(_max_over_ranks(t1 - t0, world))
+        del e2e_snap
+        e2e_s = statistics.median(e2e_win)
         res["e2e_tps"] = world * B * steps / e2e_s
+        res["e2e_window_s"] = {"median": round(e2e_s, 5), "min": round(min(e2e_win), 5),
+                               "max": round(max(e2e_win), 5), "repetitions": reps}
         if e2e_cache.device_error(stream):
             raise RuntimeError("device error word set (end-to-end leg)")
         e2e_cache.close()
@@ -622,6 +649,7 @@ def run_gpu(args):
                           "cache smaller than L2 (%.3f MB read per step), not flushed: a latency figure"
                           % (bytes_step / 1e6))},
         "step_ms": m["step_ms"],
+        "window_ms": m["window_ms"],
         "cache_read_gbs": round(bytes_step / (m["ms_step"] / 1e3) / 1e9, 1),
         "cache_read_frac_of_peak": round(bytes_step / (m["ms_step"] / 1e3) / 1e9 / peak, 4),
         "append_prefill_gbs": round(m["append_gbs"], 1),
@@ -636,8 +664,12 @@ def run_gpu(args):
                      "peak_source": f"{peak_kind} HBM copy bandwidth (frac); frac_of_nominal against the "
                                     f"{NOMINAL_HBM_GBS:.0f} GB/s HBM3e nominal"},
         "e2e": None if m["e2e_tps"] is None else {"value": round(m["e2e_tps"], 1), "unit": "tokens/s",
-                                                  "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"]},
+                                                  "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
+                                                  "window_s": m["e2e_window_s"]},
         "gpu_launches": m["steps"] * 2 * L,
+        "timing": (f"median of {m['window_ms']['repetitions']} repetitions of the {m['steps']}-step window, each "
+                   "from the cache state saved after the warm-up (kvq_state_save / kvq_state_restore); "
+                   "gpu_launches counts one window"),
         "clocks": m["clocks"],
     }
     # the other decode workloads, measured in the same run (no end-to-end leg)
@@ -997,6 +1029,8 @@ def main():
                     help="comma-separated workloads measured after the main one and reported under "
                          "other_workloads (decode only; empty to skip)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--reps", type=int, default=10,
+                    help="repetitions of the timed window (at least 10), each from the same saved cache state")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="profiling runs: skip the end-to-end leg")
     ap.add_argument("--layers", type=int, default=0, help="profiling runs: only the workload's first N layers")

@@ -278,6 +278,39 @@ kvq_status kvq_device_error(kvq_handle* h, int32_t* code, void* stream);
  * `stream`; changes nothing else. */
 kvq_status kvq_selftest_bounded_wait(kvq_handle* h, void* stream);
 
+/* Snapshots of the streaming state, to rewind a cache to an earlier point
+ * (re-running a window of decode steps, or dropping tokens decoded after the
+ * snapshot).  A snapshot holds every layer's token counters (appended tokens,
+ * quantized tokens, window bound, of every (batch, kv head) unit) and its FP16
+ * residual window ring; it does not hold the quantized groups.  That is enough:
+ * an append only writes groups at or past the quantized-token count it starts
+ * from, and attention reads only groups below the current count, so a group
+ * the snapshot does not hold is written again before anything reads it
+ * (the cache is the groups quantized so far plus the FP16 window: KIVI notes
+ * section 6.2, KVmix 关键设计 3).
+ *
+ * kvq_state_bytes: bytes of a snapshot of `h` (0 if h is null).
+ *
+ * kvq_state_save: copies the state into `dst`, a caller-owned device buffer of
+ * kvq_state_bytes(h) bytes, 16-byte aligned, on `stream` after the work already
+ * queued there (plain device-to-device copies, one per layer plus one for the
+ * counters).  KVQ_ERR_ARG if h or dst is null, KVQ_ERR_ALIGN if dst is not
+ * 16-byte aligned.
+ *
+ * kvq_state_restore: makes `src` (a snapshot saved from `h`, or from a handle
+ * created with the same configuration) the cache's state.  It first reads the
+ * snapshot's counters to the host (synchronizing `stream`) and checks that they
+ * describe a state the cache can be in: every unit of a layer agrees, the
+ * quantized count is a multiple of G and at most the appended count, which is
+ * at most max_tokens, the window holds fewer tokens than its bound, and the
+ * bound is a multiple of G between G and R_l (R_l itself on a static window).
+ * KVQ_ERR_STATE if not, and nothing changes.  Otherwise the copies back are
+ * queued on `stream` and the host mirror is set from the snapshot.  A captured
+ * decode step stays valid (its launches read the state from the device). */
+size_t kvq_state_bytes(const kvq_handle* h);
+kvq_status kvq_state_save(kvq_handle* h, void* dst, void* stream);
+kvq_status kvq_state_restore(kvq_handle* h, const void* src, void* stream);
+
 /* Release the handle (host memory and any captured graph).  The device buffer
  * stays the caller's. */
 kvq_status kvq_destroy(kvq_handle* h);

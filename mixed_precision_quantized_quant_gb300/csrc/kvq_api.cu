@@ -604,6 +604,83 @@ kvq_status kvq_selftest_bounded_wait(kvq_handle* h, void* stream) {
   return code == kvq::kErrWaitTimeout ? KVQ_OK : KVQ_ERR_STATE;
 }
 
+namespace {
+
+// Bytes of the counters region and of one layer's window ring (keys then
+// values, adjacent in the buffer) in a snapshot.
+int64_t ctrl_bytes(const Plan& P) { return P.ctrl_stride * P.L; }
+int64_t ring_bytes(const Plan& P, const LayerPlan& lp) {
+  return lp.off_res_v - lp.off_res_k + align_up(lp.res_stride_elems * 2 * P.units, kAlign);
+}
+
+}  // namespace
+
+size_t kvq_state_bytes(const kvq_handle* h) {
+  if (!h) return 0;
+  int64_t n = ctrl_bytes(h->plan);
+  for (const LayerPlan& lp : h->plan.layers) n += ring_bytes(h->plan, lp);
+  return static_cast<size_t>(n);
+}
+
+kvq_status kvq_state_save(kvq_handle* h, void* dst, void* stream) {
+  Trace trace("kvq_state_save");
+  if (!h || !dst) return KVQ_ERR_ARG;
+  if (!aligned16(dst)) return KVQ_ERR_ALIGN;
+  const Plan& P = h->plan;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* d = static_cast<uint8_t*>(dst);
+  if (cudaMemcpyAsync(d, h->base + P.off_ctrl, ctrl_bytes(P), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  d += ctrl_bytes(P);
+  for (const LayerPlan& lp : P.layers) {
+    if (cudaMemcpyAsync(d, h->base + lp.off_res_k, ring_bytes(P, lp), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    d += ring_bytes(P, lp);
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_state_restore(kvq_handle* h, const void* src, void* stream) {
+  Trace trace("kvq_state_restore");
+  if (!h || !src) return KVQ_ERR_ARG;
+  if (!aligned16(src)) return KVQ_ERR_ALIGN;
+  const Plan& P = h->plan;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::vector<int32_t> c(static_cast<size_t>(ctrl_bytes(P) / 4));
+  if (cudaMemcpyAsync(c.data(), src, ctrl_bytes(P), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  std::vector<int64_t> tokens(P.L), nq(P.L);
+  std::vector<int32_t> bound(P.L);
+  for (int l = 0; l < P.L; ++l) {
+    const LayerPlan& lp = P.layers[l];
+    const int32_t* cl = c.data() + l * P.ctrl_stride / 4;
+    if (cl[0] != 0) return KVQ_ERR_STATE;  // an append's last-CTA counter mid-launch
+    const int32_t t = cl[16], q = cl[16 + P.units], b = cl[16 + 2 * P.units];
+    for (int u = 1; u < P.units; ++u)
+      if (cl[16 + u] != t || cl[16 + P.units + u] != q || cl[16 + 2 * P.units + u] != b) return KVQ_ERR_STATE;
+    if (q < 0 || q % P.G != 0 || q > t || t > P.max_tokens) return KVQ_ERR_STATE;
+    if (b < P.G || b > lp.R || b % P.G != 0 || (lp.rpc == 0 && b != lp.R)) return KVQ_ERR_STATE;
+    if (t - q >= b) return KVQ_ERR_STATE;
+    tokens[l] = t;
+    nq[l] = q;
+    bound[l] = b;
+  }
+  const uint8_t* d = static_cast<const uint8_t*>(src);
+  if (cudaMemcpyAsync(h->base + P.off_ctrl, d, ctrl_bytes(P), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  d += ctrl_bytes(P);
+  for (const LayerPlan& lp : P.layers) {
+    if (cudaMemcpyAsync(h->base + lp.off_res_k, d, ring_bytes(P, lp), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    d += ring_bytes(P, lp);
+  }
+  h->tokens = tokens;
+  h->nq = nq;
+  h->bound = bound;
+  return KVQ_OK;
+}
+
 kvq_status kvq_destroy(kvq_handle* h) {
   Trace trace("kvq_destroy");
   if (!h) return KVQ_ERR_ARG;

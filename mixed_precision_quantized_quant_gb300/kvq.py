@@ -26,7 +26,8 @@ EXPORTS = (
     "kvq_cache_bytes", "kvq_create", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
     "kvq_layer_view_get", "kvq_equivalent_bits", "kvq_decode_bytes", "kvq_device_error",
     "kvq_destroy", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_chunk_attn",
-    "kvq_selftest_bounded_wait", "kvq_chunk_workspace_bytes",
+    "kvq_selftest_bounded_wait", "kvq_chunk_workspace_bytes", "kvq_state_bytes", "kvq_state_save",
+    "kvq_state_restore",
 )
 
 
@@ -102,6 +103,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.kvq_device_error.restype = ctypes.c_int
     L.kvq_selftest_bounded_wait.argtypes = [vp, vp]
     L.kvq_selftest_bounded_wait.restype = ctypes.c_int
+    L.kvq_state_bytes.argtypes = [vp]
+    L.kvq_state_bytes.restype = ctypes.c_size_t
+    L.kvq_state_save.argtypes = [vp, vp, vp]
+    L.kvq_state_save.restype = ctypes.c_int
+    L.kvq_state_restore.argtypes = [vp, vp, vp]
+    L.kvq_state_restore.restype = ctypes.c_int
     L.kvq_destroy.argtypes = [vp]
     L.kvq_destroy.restype = ctypes.c_int
     L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -194,6 +201,18 @@ def kvq_device_error(h: int, stream: int) -> int:
 
 def kvq_selftest_bounded_wait(h: int, stream: int) -> None:
     _check(load().kvq_selftest_bounded_wait(h, stream), "kvq_selftest_bounded_wait")
+
+
+def kvq_state_bytes(h: int) -> int:
+    return int(load().kvq_state_bytes(h))
+
+
+def kvq_state_save(h: int, dst: int, stream: int) -> None:
+    _check(load().kvq_state_save(h, dst, stream), "kvq_state_save")
+
+
+def kvq_state_restore(h: int, src: int, stream: int) -> None:
+    _check(load().kvq_state_restore(h, src, stream), "kvq_state_restore")
 
 
 def kvq_destroy(h: int) -> None:
@@ -295,6 +314,22 @@ class KVQCache:
 
     def device_error(self, stream=None) -> int:
         return kvq_device_error(self.h, _stream_ptr(stream))
+
+    def save_state(self, snapshot=None, stream=None):
+        """Snapshot of the streaming state (token counters and FP16 windows of
+        every layer) into a uint8 device tensor of kvq_state_bytes bytes,
+        allocated if not given; returns it."""
+        import torch
+        n = kvq_state_bytes(self.h)
+        if snapshot is None:
+            snapshot = torch.empty(n, dtype=torch.uint8, device=self.buf.device)
+        kvq_state_save(self.h, _dev_ptr(snapshot, "snapshot", torch.uint8, (n,)), _stream_ptr(stream))
+        return snapshot
+
+    def restore_state(self, snapshot, stream=None) -> None:
+        import torch
+        n = kvq_state_bytes(self.h)
+        kvq_state_restore(self.h, _dev_ptr(snapshot, "snapshot", torch.uint8, (n,)), _stream_ptr(stream))
 
     def close(self) -> None:
         if getattr(self, "h", None):

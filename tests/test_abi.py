@@ -91,6 +91,9 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.kvq_destroy(None) == 1
     assert lib.kvq_equivalent_bits(None) == 0.0
     assert lib.kvq_decode_bytes(None, 0) == -1
+    assert lib.kvq_state_bytes(None) == 0
+    assert lib.kvq_state_save(None, None, None) == 1
+    assert lib.kvq_state_restore(None, None, None) == 1
 
 
 def test_per_token_key_layout(lib):

@@ -697,3 +697,94 @@ def test_rpc_records_and_ring_after_a_shrink():
     rk, _ = c.residual_ring(0)
     assert (c.n_q, c.r) == (320, 2)
     assert (rk[320 % R] == allk[320]).all() and (rk[321 % R] == allk[321]).all()
+
+
+# ---------------------------------------------------------------- decode attention of the cache model
+
+def _sdpa_fp64(q, k, v):
+    """torch's attention in fp64: q [Hq, d], k/v [T, d] shared by every head."""
+    import torch
+    qt = torch.from_numpy(np.asarray(q, dtype=np.float64))[:, None, :]
+    kt = torch.from_numpy(np.asarray(k, dtype=np.float64))[None].expand(qt.shape[0], -1, -1)
+    vt = torch.from_numpy(np.asarray(v, dtype=np.float64))[None].expand(qt.shape[0], -1, -1)
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, 0].numpy()
+
+
+@pytest.mark.parametrize("kb,vb,km", [(4, 2, 0), (3, 3, 0), (8, 4, 1), (2, 2, 0)])
+def test_attend_exact_grid_equals_library_attention(kb, vb, km):
+    # [KVTuner] A3 attention over the cache: with every key group and value
+    # token on a grid its quantizer reconstructs exactly (min, max and the
+    # values in between multiples of a power-of-two step), the dequantized
+    # cache is the fp16 K and V themselves, so the cache model's decode
+    # attention (append, then attend over groups and window) must equal
+    # torch's fp64 attention over the raw K and V, head mapping included.
+    rng = np.random.default_rng(21)
+    B, H, rep, d, G, R, T = 2, 2, 3, 64, 32, 64, 150
+    qk, qv = (1 << kb) - 1, (1 << vb) - 1
+    # keys: per channel over each group (or per token) a grid of step 2^-2,
+    # every channel of every group touching both ends of its code range
+    codes_k = rng.integers(0, qk + 1, (B, H, T, d))
+    codes_v = rng.integers(0, qv + 1, (B, H, T, d))
+    if km == 0:
+        for g0 in range(0, T, G):
+            codes_k[:, :, g0, :] = 0
+            codes_k[:, :, min(g0 + 1, T - 1), :] = qk
+    else:
+        codes_k[..., 0] = 0
+        codes_k[..., 1] = qk
+    codes_v[..., 0] = 0
+    codes_v[..., 1] = qv
+    # 3-bit words: the 2-bit field (channel 11j + 10) is scaled by s2 = 7s/3,
+    # not a power of two, so it holds only its range's minimum here
+    slot10 = (np.arange(d) % 11) == 10
+    if kb == 3:
+        codes_k[..., slot10] = 0
+    if vb == 3:
+        codes_v[..., slot10] = 0
+    # per channel keys: a per-channel offset; per-token keys and values: a
+    # per-token offset (the minimum of each quantized row or column)
+    base_k = rng.integers(-8, 8, (B, H, 1, d) if km == 0 else (B, H, T, 1)) * 0.5
+    base_v = rng.integers(-8, 8, (B, H, T, 1)) * 0.5
+    k = (base_k + codes_k * 0.25).astype(np.float16)
+    v = (base_v + codes_v * 0.25).astype(np.float16)
+    q = rng.standard_normal((B, H * rep, d)).astype(np.float16)
+    c = O.OracleLayerCache(B, H, d, G, kb, vb, R, km)
+    c.append(k[:, :, :100], v[:, :, :100])
+    c.append(k[:, :, 100:], v[:, :, 100:])
+    assert c.n_q > 0 and c.r > 0
+    got = c.attend(q)
+    for b in range(B):
+        for h in range(H):
+            exp = _sdpa_fp64(q[b, h * rep:(h + 1) * rep], k[b, h], v[b, h])
+            np.testing.assert_allclose(got[b, h * rep:(h + 1) * rep], exp, rtol=1e-12, atol=1e-12)
+
+
+def test_attend_window_only_equals_library_attention():
+    # a window longer than the context: nothing is quantized and the decode
+    # attention is plain fp64 attention over the fp16 K and V
+    rng = np.random.default_rng(22)
+    B, H, rep, d, G = 1, 2, 4, 128, 32
+    k = rng.standard_normal((B, H, 90, d)).astype(np.float16)
+    v = rng.standard_normal((B, H, 90, d)).astype(np.float16)
+    q = rng.standard_normal((B, H * rep, d)).astype(np.float16)
+    c = O.OracleLayerCache(B, H, d, G, 4, 2, 128)
+    c.append(k, v)
+    assert c.n_q == 0
+    got = c.attend(q)
+    for h in range(H):
+        np.testing.assert_allclose(got[0, h * rep:(h + 1) * rep], _sdpa_fp64(q[0, h * rep:(h + 1) * rep], k[0, h], v[0, h]),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_live_ring_slots_worked():
+    # flush rule with R = 64, G = 32 ([KIVI notes] 6.2): after 100 tokens two
+    # groups (64 tokens) are quantized and tokens 64..99 sit in slots 0..35;
+    # after 70 tokens one group is quantized and tokens 32..69 sit in slots
+    # 32..63 then 0..5
+    d = 64
+    for T, nq, slots in ((100, 64, list(range(36))), (70, 32, list(range(32, 64)) + list(range(6)))):
+        c = O.OracleLayerCache(1, 1, d, 32, 4, 2, 64)
+        x = np.zeros((1, 1, T, d), dtype=np.float16)
+        c.append(x, x)
+        assert c.n_q == nq
+        assert c.live_ring_slots().tolist() == slots
