@@ -109,7 +109,9 @@ kvq_status make_plan(const kvq_config* cfg, Plan* P) {
       const int64_t slice = 4LL * 32 * (lp.wk + lp.wv) + (lp.km ? 128LL : 4LL * P->D) + 128;
       const int64_t tile = 16LL * 4 * P->D;
       const int64_t setup = 16 * (slice > 2048 ? slice : 2048);  // 2 x up to 8 warps per CTA
-      const int64_t per_unit = setup + lp.max_groups * (P->G / 32) * slice + ((lp.R + 15) / 16) * tile;
+      // (stages round up to whole records and tiles: one stage of each more)
+      const int64_t per_unit = setup + lp.max_groups * (P->G / 32) * slice + ((lp.R + 15) / 16) * tile +
+                               8 * slice + 8 * tile;
       if (per_unit * P->units >= (1LL << 32)) return KVQ_ERR_UNSUPPORTED;
     }
     lp.unit_rec_stride = align_up(lp.max_groups * lp.rec_bytes, kAlign);

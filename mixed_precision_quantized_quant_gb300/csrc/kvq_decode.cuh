@@ -32,39 +32,41 @@
 
 namespace kvq {
 
-constexpr int kSlots = 4;   // copies in flight per warp (mbarrier slots)
-constexpr int kSlice = 32;  // tokens of a key group staged per work item
+constexpr int kSlice = 32;   // tokens of a key group one warp takes per stage
+constexpr int kStages = 2;   // CTA-wide stages in flight
 
-// Bytes of one staged 32-token slice of a group record: [K rows][V rows]
+// Bytes one 32-token slice of a group record stands for: [K rows][V rows]
 // then [K scale d][K zero d] (per-channel keys) or [K (scale, zero) 32 pairs]
 // (per-token keys), then [V (scale, zero) 32 pairs].
 __host__ __device__ constexpr int slice_bytes(int D, int wk, int wv, int km) {
   return kSlice * 4 * (wk + wv) + (km ? 4 * kSlice : 4 * D) + 4 * kSlice;
 }
 
-// Per-warp ring of staged items: at least two slices, and at least one
-// residual tile (a tile waits for the ring to drain when it does not fit
-// beside the slices in flight; tiles are few, and a smaller ring fits more
-// CTAs on an SM).
-__host__ __device__ constexpr int ring_bytes(int D, int cq) {
+// Bytes of one stage: W/NS whole key-group records (W slices; their bytes
+// are at most W slice_bytes for any G), or as many residual window tiles as
+// fit, at least one.
+__host__ __device__ constexpr int stage_bytes(int D, int cq, int W) {
   const int rt = kResTile * 4 * D;
-  const int need = (rt > 2 * cq) ? rt : 2 * cq;
+  const int need = (rt > W * cq) ? rt : W * cq;
   return (need + 127) / 128 * 128;
 }
 
 struct DecodeSmem {
-  int ring;
-  int off_bars, off_qs, off_qp, off_qps, off_qr, off_qsum, off_wm, off_wl, off_dm, off_flags, off_wo, total;
+  int stage;
+  int off_bars, off_cnt, off_qs, off_qp, off_qps, off_qr, off_qsum, off_wm, off_wl, off_dm, off_flags, off_wo, total;
 };
 
-// W warps per CTA, each with its own ring of `ring` bytes.
-__host__ __device__ constexpr DecodeSmem decode_smem_layout_ring(int D, int NT, int ring, int W) {
+// kStages stages of `stage` bytes shared by the CTA's W warps, then the
+// barriers, the query rows and tables, and the per-warp merge area.
+__host__ __device__ constexpr DecodeSmem decode_smem_layout_stage(int D, int NT, int stage, int W) {
   DecodeSmem s{};
   const int H = 4 * NT;
-  s.ring = ring;
-  int off = W * s.ring;
+  s.stage = stage;
+  int off = kStages * stage;
   s.off_bars = off;
-  off += (W * kSlots + 2) * 8;       // ring slots, then the two query buffers
+  off += (kStages + 2) * 8;          // stage fills, then the two query buffers
+  s.off_cnt = off;
+  off += 16;                         // per stage: warps done with it, over all fills
   s.off_qs = off;
   off += 2 * H * D * 2;              // double-buffered query rows of a unit
   // per-lane query tables, lane-interleaved in 8-byte pairs (conflict-free)
@@ -92,20 +94,20 @@ __host__ __device__ constexpr DecodeSmem decode_smem_layout_ring(int D, int NT, 
 }
 
 __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int cq, int W) {
-  return decode_smem_layout_ring(D, NT, ring_bytes(D, cq), W);
+  return decode_smem_layout_stage(D, NT, stage_bytes(D, cq, W), W);
 }
 
 // Warps per CTA of an instantiation: 8 where two such CTAs fit in an SM's
 // shared memory (fewer CTAs per unit: fewer query-table builds and split
 // merges at the same occupancy), else 4.  3-bit values keep 4: they need more
-// than the 128 registers a thread may use at 2 x 256 threads per SM.  The ring
-// size does not depend on G.
+// than the 128 registers a thread may use at 2 x 256 threads per SM.  The
+// stage size does not depend on G.
 template <int KB, int VB, int D, int NT, int KM>
 __host__ __device__ constexpr int decode_warps() {
   constexpr int WK = (KB == 3) ? (D + 10) / 11 : D * KB / 32;
   constexpr int WV = (VB == 3) ? (D + 10) / 11 : D * VB / 32;
-  constexpr int ring = ring_bytes(D, slice_bytes(D, WK, WV, KM));
-  constexpr int smem8 = decode_smem_layout_ring(D, NT, ring, 8).total;
+  constexpr int cq = slice_bytes(D, WK, WV, KM);
+  constexpr int smem8 = decode_smem_layout_stage(D, NT, stage_bytes(D, cq, 8), 8).total;
   return (NT == 1 && VB != 3 && 2 * (smem8 + 1024) <= 228 * 1024) ? 8 : 4;
 }
 
@@ -402,7 +404,7 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
 // KM: key mode, 0 = per channel over key groups, 1 = per token.
 template <int KB, int VB, int D, int NT, int KM>
 __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
-                                  decode_warps<KB, VB, D, NT, KM>() == 8 ? 2 : (NT == 1 ? 3 : 2))
+                                  decode_warps<KB, VB, D, NT, KM>() == 8 ? 2 : 3)
     decode_kernel(DecodeParams p) {
   static_assert(KM == 0 || KB != 3, "per-token keys are 2, 4 or 8 bits");
   using KS_ = KeyShape<KB, D>;
@@ -418,10 +420,12 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   constexpr int H = 4 * NT;             // padded query heads
   constexpr int W = decode_warps<KB, VB, D, NT, KM>();  // warps per CTA
   constexpr int TH = 32 * W;
+  constexpr bool kTabSmem = false;
 
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kCq = slice_bytes(D, WK, WV, KM);
   const DecodeSmem L = decode_smem_layout(D, NT, kCq, W);
+  constexpr uint32_t SB = static_cast<uint32_t>(stage_bytes(D, kCq, W));  // bytes of one stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
   __half* qs = reinterpret_cast<__half*>(smem + L.off_qs);
   uint32_t* qp_tab = reinterpret_cast<uint32_t*>(smem + L.off_qp);
@@ -435,16 +439,20 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   float* wo = reinterpret_cast<float*>(smem + L.off_wo);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t* qtab = reinterpret_cast<uint32_t*>(wo + warp * H * D);
+  int* scnt = reinterpret_cast<int*>(smem + L.off_cnt);
   const int g = lane >> 2, tig = lane & 3, part = g & 1;
   // table entry (j, pi) of lane l sits at u32 ((j*NPK + pi)/2 * 32 + l) * 2 + (pi & 1)
   auto kt_idx = [](int j, int pi, int l) { return (((j * NPK + pi) >> 1) * 32 + l) * 2 + (pi & 1); };
   auto rt_idx = [](int j, int kk, int l) { return ((j * KS + kk) * 32 + l) * 2; };
 
   // ---------------- state and this CTA's share of the work
-  // The flat list of items (per unit: its slices, then its residual tiles)
-  // is cut into P near-equal cost ranges, x(p) = p*floor(C/P) + min(p, C mod P);
+  // A unit's work is a list of stages: its key groups, NR = W / NS whole
+  // records per stage (one 32-token slice per warp), then its FP16 window,
+  // TPS 16-token tiles per stage.  The flat list of stages (unit by unit) is
+  // cut into P near-equal cost ranges, x(p) = p*floor(C/P) + min(p, C mod P);
   // each unit also carries a fixed cost for its setup and merge, so CTAs that
-  // span two units get fewer bytes.  An item belongs to the CTA whose range
+  // span two units get fewer bytes.  A stage belongs to the CTA whose range
   // holds its start.  All of it is 32-bit arithmetic (the host keeps a
   // layer's decode bytes below 2^32), computed by every thread.  The token
   // count is read once per CTA, so every thread works from the same value
@@ -452,7 +460,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   // programmatic dependent launch: the next layer's CTAs may take the SM
   // slots this grid frees; this grid's own reads of anything the previous
   // kernel writes come after its wait (mode 1: now; mode 2: once the first
-  // cache items are in flight)
+  // stage is in flight)
   if (p.pdl) {
     grid_dep_launch();
     if (p.pdl == 1) grid_dep_wait();
@@ -469,33 +477,37 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   const int r = T - nq;                   // tokens in the FP16 window (at most R)
   const int NS = p.G / kSlice;            // slices per key group (1, 2 or 4)
   const int lgNS = NS == 4 ? 2 : NS - 1;
-  const int NG = nq / kSlice;             // quantized work items (slices)
-  const int NRT = (r + kResTile - 1) / kResTile;
-  const int NI = NG + NRT;
-  constexpr uint32_t cq = kCq;                                          // staged slice bytes
+  const int NR = W >> lgNS;               // key-group records per stage
+  const int NGR = nq / p.G;               // key groups per unit
+  const int NQS = (NGR + NR - 1) / NR;    // quantized stages per unit
+  constexpr uint32_t cq = kCq;                                          // bytes per slice
   constexpr uint32_t cr = kResTile * 4 * D;                             // residual tile bytes
+  constexpr int TPS = (SB / cr < static_cast<uint32_t>(W)) ? static_cast<int>(SB / cr) : W;  // tiles per stage
+  const int NRT = (r + kResTile - 1) / kResTile;
+  const int NRS = (NRT + TPS - 1) / TPS;  // window stages per unit
+  const int NI = NQS + NRS;               // stages per unit
+  constexpr uint32_t cst_q = W * cq, cst_r = TPS * cr;                  // cost of a stage
   // per-unit setup cost (query tables, warp merge, partial write): measured
   // at about the time a CTA needs for 2*W slices
   constexpr uint32_t csu = 2 * W * (cq > 2048u ? cq : 2048u);
-  const uint32_t Cu = csu + static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(NRT) * cr;
+  const uint32_t Cu = csu + static_cast<uint32_t>(NQS) * cst_q + static_cast<uint32_t>(NRS) * cst_r;
   const uint32_t C = static_cast<uint32_t>(p.units) * Cu;
-  // a CTA range must hold at least one item start: range >= largest item + setup
-  const uint32_t maxc = csu + ((NRT > 0 && cr > cq) || NG == 0 ? cr : cq);
+  // a CTA range must hold at least one stage start: range >= largest stage + setup
+  const uint32_t maxc = csu + ((NRS > 0 && cst_r > cst_q) || NQS == 0 ? cst_r : cst_q);
   uint32_t peff_u = C / maxc;
   if (peff_u < 1) peff_u = 1;
   if (peff_u > static_cast<uint32_t>(p.grid)) peff_u = p.grid;
-  const int peff = static_cast<int>(peff_u);
   const int pid = blockIdx.x;
-  if (pid >= peff) return;
+  if (pid >= static_cast<int>(peff_u)) return;
   const uint32_t CQ = C / peff_u, CR = C - CQ * peff_u;
   auto range_start = [&](uint32_t pp) -> uint32_t { return pp * CQ + (pp < CR ? pp : CR); };
-  // start of item i of unit u in the cost order
+  // start of stage i of unit u in the cost order
   auto item_start = [&](int u, int i) -> uint32_t {
     return static_cast<uint32_t>(u) * Cu + csu +
-           (i < NG ? static_cast<uint32_t>(i) * cq
-                   : static_cast<uint32_t>(NG) * cq + static_cast<uint32_t>(i - NG) * cr);
+           (i < NQS ? static_cast<uint32_t>(i) * cst_q
+                    : static_cast<uint32_t>(NQS) * cst_q + static_cast<uint32_t>(i - NQS) * cst_r);
   };
-  // first item starting at or after x, as (unit, item) with item < NI
+  // first stage starting at or after x, as (unit, stage) with stage < NI
   auto first_item_at = [&](uint32_t x, int& u_out, int& i_out) {
     const uint32_t u = x / Cu;
     const uint32_t ox = x - u * Cu;
@@ -504,9 +516,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
       i = 0;
     } else {
       const uint32_t o = ox - csu;
-      if (NG > 0 && o <= static_cast<uint32_t>(NG - 1) * cq) i = static_cast<int>((o + cq - 1) / cq);
-      else if (o <= static_cast<uint32_t>(NG) * cq) i = NG;
-      else i = NG + static_cast<int>((o - static_cast<uint32_t>(NG) * cq + cr - 1) / cr);
+      if (NQS > 0 && o <= static_cast<uint32_t>(NQS - 1) * cst_q) i = static_cast<int>((o + cst_q - 1) / cst_q);
+      else if (o <= static_cast<uint32_t>(NQS) * cst_q) i = NQS;
+      else i = NQS + static_cast<int>((o - static_cast<uint32_t>(NQS) * cst_q + cst_r - 1) / cst_r);
     }
     u_out = static_cast<int>(u);
     i_out = i;
@@ -522,15 +534,16 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   int u0, i0, u1, i1;
   first_item_at(range_start(pid), u0, i0);
   first_item_at(range_start(pid + 1), u1, i1);
-  // flat item indices f = u*NI + i stay below 2^31: every item costs more
+  // flat stage indices f = u*NI + i stay below 2^31: every stage costs more
   // than 1024 of the fewer than 2^32 cost units
   const int f0 = u0 * NI + i0, f1 = u1 * NI + i1;
+  const int nst = f1 - f0;                // stages of this CTA
   const int u_first = u0, u_last = i1 == 0 ? u1 - 1 : u1;
 
   // ---------------- query rows of a unit, double-buffered bulk copies
-  // (issued before the ring copies: the query tables gate every item;
-  // rows past gqa are never read, the tables test h < gqa)
-  uint64_t* qbar = bars + W * kSlots;
+  // (rows past gqa are never read, the tables test h < gqa)
+  uint64_t* full = bars;                  // [kStages] a stage's fill has landed
+  uint64_t* qbar = bars + kStages;
   const uint32_t qbytes = static_cast<uint32_t>(p.gqa * D * 2);
   auto issue_q = [&](int u, int buf) {
     mbar_arrive_expect_tx(&qbar[buf], qbytes);
@@ -540,120 +553,94 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     issue_q(u_first, 0);
     if (u_first + 1 <= u_last) issue_q(u_first + 1, 1);
   };
-  if (tid == 0) {
-    mbar_init(&qbar[0], 1);
-    mbar_init(&qbar[1], 1);
-    fence_mbar_init();
-    if (p.pdl != 2) issue_first_q();
-  }
 
-  // ---------------- per-warp ring of staged items (kSlots copies in flight)
-  uint8_t* ring = smem + warp * L.ring;
-  uint64_t* wbar = bars + warp * kSlots;
-  if (lane == 0) {
-    for (int s = 0; s < kSlots; ++s) mbar_init(&wbar[s], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  // Ring bookkeeping runs identically in every lane; lane 0 issues the copies.
-  int rhead = 0, rtail = 0, rend = 0, nin = 0, kiss = 0, kcon = 0;
-  bool wrapped = false;
-  // (unit, item) of the next item to issue / to consume, advanced without division
-  int iu = u0, ii = i0 + warp;
-  while (ii >= NI) {
-    ii -= NI;
-    ++iu;
-  }
-  int ci = ii;
-  auto try_issue = [&](int cap = kSlots) {  // stage items while fewer than cap are in flight
-    while (nin < cap) {
-      const int f = f0 + warp + W * kiss;
-      if (f >= f1) break;
-      const uint32_t sz = ii < NG ? cq : cr;
-      int off;
-      if (nin == 0) {
-        rhead = rtail = 0;
-        wrapped = false;
-        off = 0;
-      } else if (!wrapped) {
-        if (rhead + static_cast<int>(sz) <= L.ring) {
-          off = rhead;
-        } else if (static_cast<int>(sz) <= rtail) {
-          rend = rhead;
-          wrapped = true;
-          off = 0;
-        } else {
-          break;
-        }
-      } else {
-        if (rhead + static_cast<int>(sz) <= rtail) off = rhead;
-        else break;
+  // ---------------- stages: the CTA's k-th stage goes to buffer k % kStages.
+  // One thread fills a buffer: the first fills at the start, later ones by
+  // the last warp to finish with the buffer's previous fill.  A key-group
+  // stage is one bulk copy of NR consecutive records of a unit; a window
+  // stage is two copies (keys, values) per 16-token tile.
+  auto issue_stage = [&](int k) {
+    const int f = f0 + k;
+    const int s = k % kStages;
+    const int u = f / NI, i = f - u * NI;  // once per stage, one thread
+    uint8_t* dst = smem + s * SB;
+    if (i < NQS) {
+      const int g0 = i * NR;
+      const int ng = (NGR - g0 < NR) ? NGR - g0 : NR;
+      const uint8_t* src = p.records + u * p.unit_rec_stride + static_cast<int64_t>(g0) * p.rec_bytes;
+      const uint32_t bytes = static_cast<uint32_t>(ng * p.rec_bytes);
+      // (debug builds: a source outside the cache buffer is recorded and
+      // skipped; the stage's barrier still completes)
+      if (!in_range(src, bytes, p.buf_lo, p.buf_hi, p.err)) {
+        mbar_arrive(&full[s]);
+        return;
       }
-      rhead = off + static_cast<int>(sz);
-      if (lane == 0) {
-        const int st = kiss & (kSlots - 1);
-        const int u = iu, i = ii;
-        uint8_t* dst = ring + off;
-        // (debug builds: a source outside the cache buffer is recorded and
-        // skipped; the slot's barrier still completes)
-        if (i < NG && !in_range(p.records + u * p.unit_rec_stride + static_cast<int64_t>(i >> lgNS) * p.rec_bytes,
-                                static_cast<size_t>(p.rec_bytes), p.buf_lo, p.buf_hi, p.err)) {
-          mbar_arrive(&wbar[st]);
-        } else if (i >= NG &&
-                   (!in_range(p.res_k + u * p.res_stride + static_cast<int64_t>((nq + (i - NG) * kResTile) % p.R) * D,
-                              kResTile * D * 2, p.buf_lo, p.buf_hi, p.err) ||
-                    !in_range(p.res_v + u * p.res_stride + static_cast<int64_t>((nq + (i - NG) * kResTile) % p.R) * D,
-                              kResTile * D * 2, p.buf_lo, p.buf_hi, p.err))) {
-          mbar_arrive(&wbar[st]);
-        } else if (i < NG) {
-          const uint8_t* rec = p.records + u * p.unit_rec_stride + static_cast<int64_t>(i >> lgNS) * p.rec_bytes;
-          if (NS == 1) {
-            mbar_arrive_expect_tx(&wbar[st], static_cast<uint32_t>(p.rec_bytes));
-            bulk_g2s(dst, rec, static_cast<uint32_t>(p.rec_bytes), &wbar[st]);
-          } else {
-            const int t0 = (i & (NS - 1)) * kSlice;
-            const uint32_t kbytes = kSlice * WK * 4, vbytes = kSlice * WV * 4;
-            mbar_arrive_expect_tx(&wbar[st], cq);
-            bulk_g2s(dst, rec + t0 * WK * 4, kbytes, &wbar[st]);
-            bulk_g2s(dst + kbytes, rec + p.G * WK * 4 + t0 * WV * 4, vbytes, &wbar[st]);
-            if constexpr (KM == 0) {  // all key scales and zeros, the slice's value pairs
-              bulk_g2s(dst + kbytes + vbytes, rec + p.G * (WK + WV) * 4, 4 * D, &wbar[st]);
-              bulk_g2s(dst + kbytes + vbytes + 4 * D, rec + p.G * (WK + WV) * 4 + 4 * D + t0 * 4, 4 * kSlice,
-                       &wbar[st]);
-            } else {  // the slice's key pairs and value pairs
-              bulk_g2s(dst + kbytes + vbytes, rec + p.G * (WK + WV) * 4 + t0 * 4, 4 * kSlice, &wbar[st]);
-              bulk_g2s(dst + kbytes + vbytes + 4 * kSlice, rec + p.G * (WK + WV) * 4 + 4 * p.G + t0 * 4,
-                       4 * kSlice, &wbar[st]);
-            }
-          }
-        } else {
-          const int slot0 = (nq + (i - NG) * kResTile) % p.R;
-          const uint32_t bytes = kResTile * D * 2;
-          mbar_arrive_expect_tx(&wbar[st], 2 * bytes);
-          bulk_g2s(dst, p.res_k + u * p.res_stride + static_cast<int64_t>(slot0) * D, bytes, &wbar[st]);
-          bulk_g2s(dst + bytes, p.res_v + u * p.res_stride + static_cast<int64_t>(slot0) * D, bytes, &wbar[st]);
-        }
+      mbar_arrive_expect_tx(&full[s], bytes);
+      bulk_g2s(dst, src, bytes, &full[s]);
+    } else {
+      const int t0 = (i - NQS) * TPS;
+      const int ntl = (NRT - t0 < TPS) ? NRT - t0 : TPS;
+      constexpr uint32_t half = kResTile * D * 2;
+      bool ok = true;
+      for (int j = 0; j < ntl; ++j) {
+        const int slot0 = (nq + (t0 + j) * kResTile) % p.R;
+        ok = ok && in_range(p.res_k + u * p.res_stride + static_cast<int64_t>(slot0) * D, half, p.buf_lo, p.buf_hi, p.err) &&
+             in_range(p.res_v + u * p.res_stride + static_cast<int64_t>(slot0) * D, half, p.buf_lo, p.buf_hi, p.err);
       }
-      ++nin;
-      ++kiss;
-      ii += W;
-      while (ii >= NI) {
-        ii -= NI;
-        ++iu;
+      if (!ok) {
+        mbar_arrive(&full[s]);
+        return;
+      }
+      mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(ntl) * cr);
+      for (int j = 0; j < ntl; ++j) {
+        const int slot0 = (nq + (t0 + j) * kResTile) % p.R;
+        bulk_g2s(dst + j * cr, p.res_k + u * p.res_stride + static_cast<int64_t>(slot0) * D, half, &full[s]);
+        bulk_g2s(dst + j * cr + half, p.res_v + u * p.res_stride + static_cast<int64_t>(slot0) * D, half, &full[s]);
       }
     }
   };
-  // (mode 2: one item per warp before the wait, so that the query copy
-  // issued after it does not queue behind a full ring of every CTA)
-  try_issue(p.pdl == 2 ? 1 : kSlots);
+  // A warp done reading stage k (every value it read consumed by an
+  // instruction) counts itself; the W-th warp of the fill refills the buffer
+  // with stage k + kStages.  The counter of a buffer runs over all its fills.
+  auto release_stage = [&](int k) {
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      const int s = k % kStages;
+      const int prev = atomicAdd(&scnt[s], 1);
+      if (prev == (k / kStages + 1) * W - 1 && k + kStages < nst) {
+        __threadfence_block();
+        fence_proxy_async_smem();  // the warps' reads of the buffer before the copy's writes
+        issue_stage(k + kStages);
+      }
+    }
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      scnt[s] = 0;
+    }
+    mbar_init(&qbar[0], 1);
+    mbar_init(&qbar[1], 1);
+    fence_mbar_init();
+    // (mode 2: the first stage before the wait, so that the query copy
+    // issued after it does not queue behind every stage of every CTA)
+    if (p.pdl != 2) {
+      issue_first_q();
+      for (int k = 0; k < kStages && k < nst; ++k) issue_stage(k);
+    } else {
+      if (nst > 0) issue_stage(0);
+      grid_dep_wait();
+      issue_first_q();
+      for (int k = 1; k < kStages && k < nst; ++k) issue_stage(k);
+    }
+  }
   if (p.pdl == 2) {
     // the query, the partials, the split counters and the output may belong
     // to the previous kernel's work: everything after this waits for it
     grid_dep_wait();
-    if (tid == 0) issue_first_q();
-    try_issue();
   }
-  __syncthreads();  // query barriers initialised before anyone waits on them
+  __syncthreads();  // barriers initialised before anyone waits on them
 
   const __half2 negmask = part ? __float2half2_rn(-1.0f) : __float2half2_rn(0.0f);
   const float alpha = p.alpha;  // residual scores (fp16 keys)
@@ -661,9 +648,12 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   const float alpha_q = p.alpha * (16777216.0f / static_cast<float>(1 << key_pos_max<KB>()));
   const uint32_t vhalf_sel = (g & 1) ? 0x7632u : 0x5410u;  // 2-bit values, D = 64
   bool failed = false;
+  const int team = warp >> lgNS, sl = warp & (NS - 1);  // record of a stage and 32-token slice of it
+  int k = 0;        // the CTA's stage
+  int si = i0;      // its index in the unit
 
   for (int u = u_first; u <= u_last; ++u) {
-    const int seg_hi = ((u + 1) * NI < f1) ? (u + 1) * NI : f1;
+    const int i_end = (u == u1) ? i1 : NI;
     const int b = u / p.kv_heads, kvh = u - b * p.kv_heads;
 
     // ---------------- per-unit query tables (from the prefetched query rows)
@@ -742,6 +732,11 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.0f;
     }
     bool has_q = false, in_res = false, dumped = false;
+    // the key group whose scaled-query table this warp holds (per-channel keys)
+    int tab_g = -1;
+    float bias_g[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) bias_g[j] = 0.0f;
 
     // online-softmax update: tmax = max of this tile's scaled scores per head
     auto softmax_update = [&](const float (&tmax_in)[NT]) {
@@ -782,43 +777,38 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
       b23 = prmt(x, y, 0x7632u);
     };
 
-    while (true) {
-      const int f = f0 + warp + W * kcon;
-      if (f >= seg_hi) break;
-      const int st = kcon & (kSlots - 1);
-      const uint32_t ph = static_cast<uint32_t>((kcon >> 2) & 1);
-      if (!failed && !mbar_wait(&wbar[st], ph, p.err)) failed = true;
-      const uint8_t* stg = ring + rtail;
-      const int i = ci;
-      // Frees the item's ring space and stages the next items.  Every value
-      // read from the slot must have been consumed by an instruction first.
+    for (; si < i_end; ++si, ++k) {
+      const int i = si;
+      if (!failed && !mbar_wait(&full[k % kStages], static_cast<uint32_t>((k / kStages) & 1), p.err)) failed = true;
+      const uint8_t* stg = smem + (k % kStages) * SB;
+      // this warp's share of the stage: slice sl of record `team`, or window tile `warp`
+      const bool q_item = i < NQS && i * NR + team < NGR;
+      const int tile = (i - NQS) * TPS + warp;
+      const bool r_item = i >= NQS && warp < TPS && tile < NRT;
+      // Counts the warp done with the stage (refilling it if last).  Every
+      // value read from the stage must have been consumed by an instruction first.
       bool released = false;
       auto release_slot = [&]() {
-        __syncwarp();
-        const int sz = static_cast<int>(i < NG ? cq : cr);
-        --nin;
-        rtail += sz;
-        if (wrapped && rtail == rend) {
-          rtail = 0;
-          wrapped = false;
-        }
-        try_issue();
+        release_stage(k);
         released = true;
       };
 
       if (failed) {
         // a copy never landed: skip the work, keep the control flow
-      } else if (i < NG) {
+      } else if (q_item) {
         // ============ quantized slice of a key group (32 tokens)
         has_q = true;
-        const uint32_t* Kc = reinterpret_cast<const uint32_t*>(stg);
-        const uint32_t* Vc = Kc + kSlice * WK;
-        const __half* Ks = reinterpret_cast<const __half*>(Vc + kSlice * WV);  // per-channel keys
+        // the record's layout: [K rows G x WK][V rows G x WV][key (scale, zero)][V (scale, zero) G pairs]
+        const uint32_t* rec = reinterpret_cast<const uint32_t*>(stg + team * p.rec_bytes);
+        const int t0 = sl * kSlice;
+        const uint32_t* Kc = rec + t0 * WK;
+        const uint32_t* Vc = rec + p.G * WK + t0 * WV;
+        const __half* Ks = reinterpret_cast<const __half*>(rec + p.G * (WK + WV));  // per-channel keys
         const __half* Kz = Ks + D;
-        const __half2* Ksz = reinterpret_cast<const __half2*>(Vc + kSlice * WV);  // per-token keys
-        const __half2* Vsz = KM == 0 ? reinterpret_cast<const __half2*>(Kz + D) : Ksz + kSlice;
+        const __half2* Ksz = reinterpret_cast<const __half2*>(rec + p.G * (WK + WV)) + t0;  // per-token keys
+        const __half2* Vsz = (KM == 0 ? reinterpret_cast<const __half2*>(Kz + D) : Ksz - t0 + p.G) + t0;
         float bias[NT];
-        uint32_t bq[NT][NPK];
+        uint32_t bq[NT][kTabSmem ? 1 : NPK];
         if constexpr (KM == 1) {
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
@@ -827,7 +817,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
             for (int pi = 0; pi < NPK; ++pi) bq[j][pi] = bqu[j][pi];
           }
         } else {
-
+        const int grp = i * NR + team;
+        if (!kTabSmem || grp != tab_g) {
+        tab_g = grp;
         uint32_t qp[NT][NPK];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
@@ -896,7 +888,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
           for (int kk = 0; kk < KSK; ++kk)
             mma_16816((kk & 1) ? c1 : c0, zp[2 * kk], zp[2 * kk], zp[2 * kk + 1], zp[2 * kk + 1], qp[j][2 * kk],
                       qp[j][2 * kk + 1]);
-          bias[j] = (c0[0] + c1[0]) * kScoreScale;  // in the scaled score domain
+          bias_g[j] = (c0[0] + c1[0]) * kScoreScale;  // in the scaled score domain
         }
         // folded query q~ = q * s (scaled): hi part in even columns, lo part in odd ones
 #pragma unroll
@@ -918,15 +910,21 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
                 if (cb >= 0 && cb % 11 == 10) sf.y = __fdiv_rn(__fmul_rn(sf.y, 7.0f), 3.0f);
                 uint32_t hi, lo;
                 split_pair(qf.x * sf.x, qf.y * sf.y, hi, lo);
-                bq[j][pj] = part ? lo : hi;
+                bq[j][kTabSmem ? 0 : pj] = part ? lo : hi;
               } else {
                 const __half2 qq = u32_as_h2(qsc);
                 const __half2 ss = u32_as_h2(sp[pj]);
                 const __half2 hi = __hmul2(qq, ss);
-                bq[j][pj] = h2_as_u32(__hfma2(qq, ss, __hmul2(hi, negmask)));
+                const uint32_t v = h2_as_u32(__hfma2(qq, ss, __hmul2(hi, negmask)));
+                if constexpr (kTabSmem) qtab[kt_idx(j, pj, lane)] = v;
+                else bq[j][pj] = v;
               }
             }
           }
+        if constexpr (kTabSmem) __syncwarp();
+        }  // table of the group
+#pragma unroll
+        for (int j = 0; j < NT; ++j) bias[j] = bias_g[j];
         }  // per-channel keys
 
         // ---- scores of the slice's 32 tokens: tiles 0 (tokens 0..15) and 1 (16..31);
@@ -944,17 +942,59 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
                 sc[t][j][q4] = 0.0f;
                 sx[t][j][q4] = 0.0f;
               }
-          uint32_t e[4][NPK];
+          // B operand of k-step kk for head tile j
+          auto bq_at = [&](int j, int kk, uint32_t& b0, uint32_t& b1) {
+            if constexpr (kTabSmem && KM == 0) {
+              const uint2 v = *reinterpret_cast<const uint2*>(qtab + kt_idx(j, 2 * kk, lane));
+              b0 = v.x;
+              b1 = v.y;
+            } else {
+              b0 = bq[j][2 * kk];
+              b1 = bq[j][2 * kk + 1];
+            }
+          };
+          if constexpr (KB == 3) {
+            uint32_t e[4][NPK];
 #pragma unroll
-          for (int rw = 0; rw < 4; ++rw) key_row_pairs<KB, D>(Kc + (8 * rw + g) * WK, tig, e[rw]);
+            for (int rw = 0; rw < 4; ++rw) key_row_pairs<KB, D>(Kc + (8 * rw + g) * WK, tig, e[rw]);
 #pragma unroll
-          for (int kk = 0; kk < KSK; ++kk)
+            for (int kk = 0; kk < KSK; ++kk)
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
+              for (int j = 0; j < NT; ++j) {
+                uint32_t b0, b1;
+                bq_at(j, kk, b0, b1);
 #pragma unroll
-              for (int j = 0; j < NT; ++j)
-                mma_16816((kk & 1) ? sx[t][j] : sc[t][j], e[2 * t][2 * kk], e[2 * t + 1][2 * kk],
-                          e[2 * t][2 * kk + 1], e[2 * t + 1][2 * kk + 1], bq[j][2 * kk], bq[j][2 * kk + 1]);
+                for (int t = 0; t < 2; ++t)
+                  mma_16816((kk & 1) ? sx[t][j] : sc[t][j], e[2 * t][2 * kk], e[2 * t + 1][2 * kk],
+                            e[2 * t][2 * kk + 1], e[2 * t + 1][2 * kk + 1], b0, b1);
+              }
+          } else {
+            // one code word of each of the 4 rows at a time: its PW pairs
+            // feed PW/2 k-steps
+            constexpr int WT = KS_::WT, PW = KS_::PW;
+            uint32_t wr[4][WT];
+#pragma unroll
+            for (int rw = 0; rw < 4; ++rw) lds_words<WT>(wr[rw], Kc + (8 * rw + g) * WK + tig * WT);
+#pragma unroll
+            for (int wi = 0; wi < WT; ++wi) {
+              uint32_t e[4][PW];
+#pragma unroll
+              for (int rw = 0; rw < 4; ++rw) k_word_pairs<KB>(wr[rw][wi], e[rw]);
+#pragma unroll
+              for (int k2 = 0; k2 < PW / 2; ++k2) {
+                const int kk = wi * (PW / 2) + k2;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                  uint32_t b0, b1;
+                  bq_at(j, kk, b0, b1);
+#pragma unroll
+                  for (int t = 0; t < 2; ++t)
+                    mma_16816((kk & 1) ? sx[t][j] : sc[t][j], e[2 * t][2 * k2], e[2 * t + 1][2 * k2],
+                              e[2 * t][2 * k2 + 1], e[2 * t + 1][2 * k2 + 1], b0, b1);
+                }
+              }
+            }
+          }
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -963,10 +1003,14 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
               for (int q4 = 0; q4 < 4; ++q4) sc[t][j][q4] += sx[t][j][q4];
         }
 
-        // ---- value code pairs of both tiles (independent of the softmax)
+        // ---- value codes of both tiles, read before the slot is released:
+        // 3-bit values are unpacked here, the others keep their code words
+        // and are unpacked just before their P.V
         constexpr int NE = (VB == 3) ? 2 * VS_::MT3 : NP;
-        uint32_t hv[2][2][NE];   // [tile][token pair (tig,tig+4) | (tig+8,tig+12)][entry]
+        constexpr int VW = VS_::VW;
+        uint32_t hv[VB == 3 ? 2 : 1][2][VB == 3 ? NE : 1];   // [tile][token pair (tig,tig+4) | (tig+8,tig+12)][entry]
         uint32_t h2v[2][2][2];   // 3-bit values: 2-bit-field tile entries
+        uint32_t vw[2][4][VW];   // other widths: [tile][token tig + 4r][word]
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int tb = 16 * t;
@@ -998,15 +1042,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
               }
             }
           } else {
-            constexpr int VW = VS_::VW;
             const int voff = (VB == 2 && D == 64) ? (g >> 1) : g * VW;
-            uint32_t w0[VW], w1[VW], w2[VW], w3[VW];
-            lds_words<VW>(w0, Vc + (tb + tig) * WV + voff);
-            lds_words<VW>(w1, Vc + (tb + tig + 4) * WV + voff);
-            lds_words<VW>(w2, Vc + (tb + tig + 8) * WV + voff);
-            lds_words<VW>(w3, Vc + (tb + tig + 12) * WV + voff);
-            v_pairs<VB, D>(w0, w1, vhalf_sel, hv[t][0]);
-            v_pairs<VB, D>(w2, w3, vhalf_sel, hv[t][1]);
+#pragma unroll
+            for (int r4 = 0; r4 < 4; ++r4) lds_words<VW>(vw[t][r4], Vc + (tb + tig + 4 * r4) * WV + voff);
           }
         }
 
@@ -1079,15 +1117,17 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
             for (int j = 0; j < NT; ++j)
               mma_16816(acc[MT3][j], h2v[t][0][0], h2v[t][0][1], h2v[t][1][0], h2v[t][1][1], c01[j], c23[j]);
           } else {
+            uint32_t hvt[2][NE];
+            v_pairs<VB, D>(vw[t][0], vw[t][1], vhalf_sel, hvt[0]);
+            v_pairs<VB, D>(vw[t][2], vw[t][3], vhalf_sel, hvt[1]);
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
               for (int j = 0; j < NT; ++j)
-                mma_16816(acc[mt][j], hv[t][0][mt], hv[t][0][KS + mt], hv[t][1][mt], hv[t][1][KS + mt], b01[j],
-                          b23[j]);
+                mma_16816(acc[mt][j], hvt[0][mt], hvt[0][KS + mt], hvt[1][mt], hvt[1][KS + mt], b01[j], b23[j]);
           }
         }
-      } else {
+      } else if (r_item) {
         // ============ residual tile: 16 FP16 tokens (chunk-swizzled rows)
         if (!in_res) {
           if (has_q) {
@@ -1115,9 +1155,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
           }
           in_res = true;
         }
-        const __half* Kr = reinterpret_cast<const __half*>(stg);
+        const __half* Kr = reinterpret_cast<const __half*>(stg + warp * cr);
         const __half* Vr = Kr + kResTile * D;
-        const int left = r - (i - NG) * kResTile;
+        const int left = r - tile * kResTile;
         const int vt = left < kResTile ? left : kResTile;
 
         float sc[NT][4], sx[NT][4];
@@ -1171,10 +1211,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
 
       // release the consumed item's ring space (if not done yet), then refill
       if (!released) release_slot();
-      ++kcon;
-      ci += W;
-      while (ci >= NI) ci -= NI;
     }
+    si = 0;
 
     // ---------------- warp -> shared memory
     // (a parked quantized part, already in wo, is rescaled to the final max)
