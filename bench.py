@@ -418,7 +418,7 @@ def measure_decode(w, args, dev, world, e2e=True):
     # cache state after the warm-up is saved once (kvq_state_save) and restored
     # before every repetition, so each one decodes the same tokens from the
     # same state, flush step included.
-    reps = max(10, args.reps)
+    win_reps = max(10, args.reps)
     win_ms, step_rows = [], []
     with torch.cuda.stream(stream):
         for s in range(warm):
@@ -427,7 +427,7 @@ def measure_decode(w, args, dev, world, e2e=True):
         stream.synchronize()
         nq_before = [cache.view(l)["quantized_tokens"] for l in range(L)]
         bytes_first = sum(cache.decode_bytes(l) for l in range(L))
-        for r in range(reps):
+        for r in range(win_reps):
             if r:
                 cache.restore_state(snapshot, stream=stream)
             stream.synchronize()
@@ -490,7 +490,7 @@ def measure_decode(w, args, dev, world, e2e=True):
         "w": w, "steps": steps, "warmup": warm, "ms_total": ms_total, "ms_step": ms_step,
         "tokens_per_s": world * B * steps / (ms_total / 1e3),
         "window_ms": {"median": round(ms_total, 4), "min": round(min(win_ms), 4), "max": round(max(win_ms), 4),
-                      "repetitions": reps},
+                      "repetitions": win_reps},
         "step_ms": {"median": round(statistics.median(step_ms), 4), "mean": round(ms_step, 4),
                     "flush_step": round(step_ms[flush_i], 4) if 0 <= flush_i < steps else None,
                     "median_without_flush_step": round(statistics.median(others), 4),
@@ -578,7 +578,7 @@ def measure_decode(w, args, dev, world, e2e=True):
         run(0, warm)
         e2e_snap = e2e_cache.save_state(stream=stream)
         e2e_win = []
-        for r in range(reps):
+        for r in range(win_reps):
             if r:
                 e2e_cache.restore_state(e2e_snap, stream=stream)
             stream.synchronize()
@@ -592,7 +592,7 @@ def measure_decode(w, args, dev, world, e2e=True):
         e2e_s = statistics.median(e2e_win)
         res["e2e_tps"] = world * B * steps / e2e_s
         res["e2e_window_s"] = {"median": round(e2e_s, 5), "min": round(min(e2e_win), 5),
-                               "max": round(max(e2e_win), 5), "repetitions": reps}
+                               "max": round(max(e2e_win), 5), "repetitions": win_reps}
         if e2e_cache.device_error(stream):
             raise RuntimeError("device error word set (end-to-end leg)")
         e2e_cache.close()
