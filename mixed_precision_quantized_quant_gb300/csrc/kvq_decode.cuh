@@ -421,6 +421,12 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
   constexpr int W = decode_warps<KB, VB, D, NT, KM>();  // warps per CTA
   constexpr int TH = 32 * W;
   constexpr bool kTabSmem = false;
+  // 5-8 query heads per kv head (2-, 4- or 8-bit codes): the 16 MMA rows are
+  // the 8 heads x {hi, lo} and the tokens are the columns, so the score
+  // accumulator is already the A operand of P.V (no shuffles), and the
+  // query's scale fold takes two half2 operations per channel pair.
+  constexpr bool kT = (NT == 2) && (KB != 3) && (VB != 3);
+  constexpr int NEV = D / 8;  // P.V n-tiles of 8 channels (transposed form)
 
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kCq = slice_bytes(D, WK, WV, KM);
@@ -660,7 +666,38 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     const int seg = u - u_first;
     const __half* qu = qs + (seg & 1) * H * D;
     if (!failed && !mbar_wait(&qbar[seg & 1], static_cast<uint32_t>((seg >> 1) & 1), p.err)) failed = true;
-    {
+    if constexpr (kT) {
+      // lane (g, tig): head g, channel pairs key_pair_channels(tig, pi)
+      const int h = g;
+      const bool live = h < p.gqa;
+      for (int pi = warp; pi < NPK; pi += W) {
+        int ca, cb;
+        key_pair_channels<KB, D>(tig, pi, ca, cb);
+        const __half z0 = __float2half(0.0f);
+        const __half2 q2 = __halves2half2(live ? qu[h * D + ca] : z0, live ? qu[h * D + cb] : z0);
+        qp_tab[kt_idx(0, pi, lane)] = h2_as_u32(q2);
+        const float f = static_cast<float>(1 << (key_pos_max<KB>() - key_pos<KB, D>(pi)));
+        qps_tab[kt_idx(0, pi, lane)] = h2_as_u32(__hmul2(q2, __float2half2_rn(f)));
+      }
+      // window keys (natural channel order): channels 16kk + 8rr + 2tig, +1
+      for (int kk = warp; kk < KS; kk += W) {
+        for (int rr = 0; rr < 2; ++rr) {
+          const int c = 16 * kk + 8 * rr + 2 * tig;
+          qr_tab[rt_idx(0, kk, lane) + rr] = live ? h2_as_u32(__halves2half2(qu[h * D + c], qu[h * D + c + 1])) : 0u;
+        }
+      }
+      if constexpr (KM == 1) {
+        constexpr float kSS = static_cast<float>(1 << key_pos_max<KB>()) / 16777216.0f;
+        for (int hh = warp; hh < H; hh += W) {
+          float sum = 0.0f;
+#pragma unroll
+          for (int c = lane; c < D; c += 32) sum += __half2float(qu[hh * D + c]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          if (lane == 0) qsum_s[hh] = hh < p.gqa ? sum * kSS : 0.0f;
+        }
+      }
+    } else {
       // every warp fills a quarter of the per-lane tables (lane = tid & 31)
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
@@ -705,7 +742,15 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     // per-token keys: the B operand of the scores is fixed for the unit
     uint32_t bqu[KM == 1 ? NT : 1][KM == 1 ? NPK : 1];
     float qsj[NT];
-    if constexpr (KM == 1) {
+    if constexpr (KM == 1 && kT) {
+      qsj[0] = qsum_s[g];
+#pragma unroll
+      for (int pi = 0; pi < NPK; pi += 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(qps_tab + kt_idx(0, pi, lane));
+        bqu[0][pi] = v.x;
+        bqu[0][pi + 1] = v.y;
+      }
+    } else if constexpr (KM == 1) {
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         qsj[j] = qsum_s[4 * j + tig];
@@ -732,6 +777,30 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.0f;
     }
     bool has_q = false, in_res = false, dumped = false;
+    // transposed form: this lane's head g; rows g (hi) and g + 8 (lo) of the
+    // P.V accumulator, n-tile c = 8 channels
+    float m1 = -INFINITY, l1 = 0.0f, vb1 = 0.0f;
+    float acc2[kT ? NEV : 1][4];
+#pragma unroll
+    for (int c = 0; c < (kT ? NEV : 1); ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc2[c][e] = 0.0f;
+    // online-softmax update of the transposed form: tmax = this lane's maximum
+    auto softmax_update1 = [&](float tmax_in) {
+      if (__any_sync(0xffffffffu, tmax_in > m1 + 8.0f)) {
+        float t = fmaxf(tmax_in, __shfl_xor_sync(0xffffffffu, tmax_in, 1));
+        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 2));
+        const float mn = fmaxf(m1, t);
+        const float f = (mn == -INFINITY) ? 1.0f : ex2(m1 - mn);
+        m1 = mn;
+        l1 *= f;
+        vb1 *= f;
+#pragma unroll
+        for (int c = 0; c < (kT ? NEV : 1); ++c)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc2[c][e] *= f;
+      }
+    };
     // the key group whose scaled-query table this warp holds (per-channel keys)
     int tab_g = -1;
     float bias_g[NT];
@@ -795,7 +864,170 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
 
       if (failed) {
         // a copy never landed: skip the work, keep the control flow
-      } else if (q_item) {
+      } else if (kT && q_item) {
+        // ============ quantized slice, transposed form (8 heads x {hi, lo} rows)
+        has_q = true;
+        const uint32_t* rec = reinterpret_cast<const uint32_t*>(stg + team * p.rec_bytes);
+        const int t0 = sl * kSlice;
+        const uint32_t* Kc = rec + t0 * WK;
+        const uint32_t* Vc = rec + p.G * WK + t0 * WV;
+        const __half* Ks = reinterpret_cast<const __half*>(rec + p.G * (WK + WV));
+        const __half* Kz = Ks + D;
+        const __half2* Ksz = reinterpret_cast<const __half2*>(rec + p.G * (WK + WV)) + t0;
+        const __half2* Vsz = (KM == 0 ? reinterpret_cast<const __half2*>(Kz + D) : Ksz - t0 + p.G) + t0;
+        constexpr float kScoreScale = static_cast<float>(1 << key_pos_max<KB>()) / 16777216.0f;
+        constexpr int WT = KS_::WT, PW = KS_::PW;
+        // per-channel keys: the group's key scale (pairs, for q~ = q s) and the
+        // zero term sum_c q_c z_c of head g (one MMA chain, q in row g)
+        uint32_t sp[KM == 0 ? NPK : 1];
+        float bias1 = 0.0f;
+        if constexpr (KM == 0) {
+          uint32_t zp[NPK];
+          uint32_t zn[NPK], sn[NPK];
+          const uint32_t* zsrc = reinterpret_cast<const uint32_t*>(Kz + tig * (D / 4));
+          const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(Ks + tig * (D / 4));
+#pragma unroll
+          for (int pi = 0; pi < NPK; pi += 4) {
+            const uint4 vz = *reinterpret_cast<const uint4*>(zsrc + pi);
+            const uint4 vs = *reinterpret_cast<const uint4*>(ssrc + pi);
+            zn[pi] = vz.x; zn[pi + 1] = vz.y; zn[pi + 2] = vz.z; zn[pi + 3] = vz.w;
+            sn[pi] = vs.x; sn[pi + 1] = vs.y; sn[pi + 2] = vs.z; sn[pi + 3] = vs.w;
+          }
+#pragma unroll
+          for (int wi = 0; wi < WT; ++wi) {
+            const uint32_t* nz = zn + wi * PW;
+            const uint32_t* ns = sn + wi * PW;
+            uint32_t* oz = zp + wi * PW;
+            uint32_t* os = sp + wi * PW;
+            if constexpr (KB == 4) {
+              oz[0] = prmt(nz[0], nz[2], 0x5410u); oz[1] = prmt(nz[0], nz[2], 0x7632u);
+              oz[2] = prmt(nz[1], nz[3], 0x5410u); oz[3] = prmt(nz[1], nz[3], 0x7632u);
+              os[0] = prmt(ns[0], ns[2], 0x5410u); os[1] = prmt(ns[0], ns[2], 0x7632u);
+              os[2] = prmt(ns[1], ns[3], 0x5410u); os[3] = prmt(ns[1], ns[3], 0x7632u);
+            } else if constexpr (KB == 2) {
+#pragma unroll
+              for (int kq = 0; kq < 4; ++kq) {
+                oz[2 * kq] = prmt(nz[kq], nz[kq + 4], 0x5410u);
+                oz[2 * kq + 1] = prmt(nz[kq], nz[kq + 4], 0x7632u);
+                os[2 * kq] = prmt(ns[kq], ns[kq + 4], 0x5410u);
+                os[2 * kq + 1] = prmt(ns[kq], ns[kq + 4], 0x7632u);
+              }
+            } else {
+              oz[0] = prmt(nz[0], nz[1], 0x5410u); oz[1] = prmt(nz[0], nz[1], 0x7632u);
+              os[0] = prmt(ns[0], ns[1], 0x5410u); os[1] = prmt(ns[0], ns[1], 0x7632u);
+            }
+          }
+          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < KSK; ++kk) {
+            const uint2 qv = *reinterpret_cast<const uint2*>(qp_tab + kt_idx(0, 2 * kk, lane));
+            mma_16816((kk & 1) ? c1 : c0, qv.x, 0u, qv.y, 0u, zp[2 * kk], zp[2 * kk + 1]);
+          }
+          bias1 = (c0[0] + c1[0]) * kScoreScale;  // row g: head g, in the scaled score domain
+        }
+        // ---- scores of the slice's 32 tokens: n-tile n = tokens 8n..8n+7,
+        // column 2tig + e = token 8n + 2tig + e; rows g (hi part) and g + 8 (lo)
+        float sc[4][4], sx[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[n][e] = 0.0f;
+            sx[n][e] = 0.0f;
+          }
+        {
+          uint32_t wr[4][WT];
+#pragma unroll
+          for (int rw = 0; rw < 4; ++rw) lds_words<WT>(wr[rw], Kc + (8 * rw + g) * WK + tig * WT);
+#pragma unroll
+          for (int wi = 0; wi < WT; ++wi) {
+            uint32_t e[4][PW];
+#pragma unroll
+            for (int rw = 0; rw < 4; ++rw) k_word_pairs<KB>(wr[rw][wi], e[rw]);
+#pragma unroll
+            for (int k2 = 0; k2 < PW / 2; ++k2) {
+              const int kk = wi * (PW / 2) + k2;
+              // A of k-step kk: q~ = q s of head g as fp16 hi (row g) + lo (row g + 8)
+              uint32_t a0, a1, a2, a3;
+              if constexpr (KM == 0) {
+                const uint2 q2 = *reinterpret_cast<const uint2*>(qps_tab + kt_idx(0, 2 * kk, lane));
+                const __half2 qa = u32_as_h2(q2.x), qb = u32_as_h2(q2.y);
+                const __half2 sa = u32_as_h2(sp[2 * kk]), sb = u32_as_h2(sp[2 * kk + 1]);
+                const __half2 ha = __hmul2(qa, sa), hb = __hmul2(qb, sb);
+                a0 = h2_as_u32(ha);
+                a1 = h2_as_u32(__hfma2(qa, sa, __hneg2(ha)));
+                a2 = h2_as_u32(hb);
+                a3 = h2_as_u32(__hfma2(qb, sb, __hneg2(hb)));
+              } else {
+                a0 = bqu[0][2 * kk];
+                a1 = 0u;
+                a2 = bqu[0][2 * kk + 1];
+                a3 = 0u;
+              }
+#pragma unroll
+              for (int n = 0; n < 4; ++n)
+                mma_16816((kk & 1) ? sx[n] : sc[n], a0, a1, a2, a3, e[n][2 * k2], e[n][2 * k2 + 1]);
+            }
+          }
+        }
+        // ---- value code words (tokens 16kb + 2tig, +1, +8, +9), the tokens'
+        // value (scale, zero) and per-token key (scale, zero): the last reads
+        constexpr int VW = VS_::VW;
+        const int voff = (VB == 2 && D == 64) ? (g >> 1) : g * VW;
+        uint32_t vw[2][4][VW];
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int r4 = 0; r4 < 4; ++r4)
+            lds_words<VW>(vw[kb][r4], Vc + (16 * kb + 2 * tig + (r4 & 1) + 8 * (r4 >> 1)) * WV + voff);
+        float2 vsz[4][2], ksz[KM == 1 ? 4 : 1][2];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          const uint2 v2 = *reinterpret_cast<const uint2*>(Vsz + 8 * n + 2 * tig);
+          vsz[n][0] = __half22float2(u32_as_h2(v2.x));
+          vsz[n][1] = __half22float2(u32_as_h2(v2.y));
+          if constexpr (KM == 1) {
+            const uint2 k2 = *reinterpret_cast<const uint2*>(Ksz + 8 * n + 2 * tig);
+            ksz[n][0] = __half22float2(u32_as_h2(k2.x));
+            ksz[n][1] = __half22float2(u32_as_h2(k2.y));
+          }
+        }
+        release_slot();
+
+        // ---- softmax over head g's 8 tokens of this lane
+        float sv[4][2];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if constexpr (KM == 1) {
+              sv[n][e] = fmaf(ksz[n][e].x, sc[n][e] + sx[n][e], ksz[n][e].y * qsj[0]);
+            } else {
+              sv[n][e] = ((sc[n][e] + sx[n][e]) + (sc[n][e + 2] + sx[n][e + 2])) + bias1;
+            }
+            tmax = fmaxf(tmax, sv[n][e]);
+          }
+        softmax_update1(alpha_q * tmax);
+        uint32_t ph[4], pl[4];  // P~ = p s_v of tokens (8n + 2tig, +1) as fp16 hi + lo
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          const float pa = ex2(fmaf(sv[n][0], alpha_q, -m1)), pb = ex2(fmaf(sv[n][1], alpha_q, -m1));
+          l1 += pa + pb;
+          vb1 = fmaf(pa, vsz[n][0].y, fmaf(pb, vsz[n][1].y, vb1));
+          split_pair(pa * vsz[n][0].x, pb * vsz[n][1].x, ph[n], pl[n]);
+        }
+        // ---- P~.V: k-block kb = tokens 16kb..16kb+15 (n-tiles 2kb, 2kb + 1)
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          uint32_t hvt[2][NEV];
+          v_pairs<VB, D>(vw[kb][0], vw[kb][1], vhalf_sel, hvt[0]);
+          v_pairs<VB, D>(vw[kb][2], vw[kb][3], vhalf_sel, hvt[1]);
+#pragma unroll
+          for (int c = 0; c < NEV; ++c)
+            mma_16816(acc2[c], ph[2 * kb], pl[2 * kb], ph[2 * kb + 1], pl[2 * kb + 1], hvt[0][c], hvt[1][c]);
+        }
+      } else if (!kT && q_item) {
         // ============ quantized slice of a key group (32 tokens)
         has_q = true;
         // the record's layout: [K rows G x WK][V rows G x WV][key (scale, zero)][V (scale, zero) G pairs]
@@ -1127,7 +1359,82 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
                 mma_16816(acc[mt][j], hvt[0][mt], hvt[0][KS + mt], hvt[1][mt], hvt[1][KS + mt], b01[j], b23[j]);
           }
         }
-      } else if (r_item) {
+      } else if (kT && r_item) {
+        // ============ residual tile, transposed form
+        if (!in_res) {
+          if (has_q) {
+            // park the quantized-token part (its channel map: column 2tig + e of
+            // n-tile c is channel (2tig + e) * D/8 + c) in wo
+            float vbt = vb1 + __shfl_xor_sync(0xffffffffu, vb1, 1);
+            vbt += __shfl_xor_sync(0xffffffffu, vbt, 2);
+            vb1 = 0.0f;
+            float* dd = wo + (warp * H + g) * D;
+#pragma unroll
+            for (int c = 0; c < NEV; ++c) {
+              const float fs = 16777216.0f / static_cast<float>(1 << value_pos<VB, D>(c % KS));
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                dd[(2 * tig + e) * (D / 8) + c] = fmaf(acc2[c][e] + acc2[c][e + 2], fs, vbt);
+                acc2[c][e] = 0.0f;
+                acc2[c][e + 2] = 0.0f;
+              }
+            }
+            if (tig == 0) dm[warp * H + g] = m1;
+            dumped = true;
+          }
+          in_res = true;
+        }
+        const __half* Kr = reinterpret_cast<const __half*>(stg + warp * cr);
+        const __half* Vr = Kr + kResTile * D;
+        const int left = r - tile * kResTile;
+        const int vt = left < kResTile ? left : kResTile;
+        // scores: rows g = head g (fp16 keys need no lo part), n-tiles 0, 1 = tokens 0-7, 8-15
+        float sc[2][4], sx[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[n][e] = 0.0f;
+            sx[n][e] = 0.0f;
+          }
+        const int ltok = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row address of this lane
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const int ch = 2 * kk + (lane >> 4);
+          uint32_t b[4];  // (tokens 0-7 | 8-15) x (channels 16kk..+7 | +8..+15)
+          ldsm_x4(b, Kr + ltok * D + ((ch ^ (ltok & 7)) * 8));
+          const uint2 q2 = *reinterpret_cast<const uint2*>(qr_tab + rt_idx(0, kk, lane));
+          mma_16816((kk & 1) ? sx[0] : sc[0], q2.x, 0u, q2.y, 0u, b[0], b[2]);
+          mma_16816((kk & 1) ? sx[1] : sc[1], q2.x, 0u, q2.y, 0u, b[1], b[3]);
+        }
+        float sv[2][2];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tk = 8 * n + 2 * tig + e;
+            sv[n][e] = (tk < vt) ? sc[n][e] + sx[n][e] : -INFINITY;
+            tmax = fmaxf(tmax, sv[n][e]);
+          }
+        softmax_update1(alpha * tmax);
+        uint32_t ph[2], pl[2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const float pa = ex2(fmaf(sv[n][0], alpha, -m1)), pb = ex2(fmaf(sv[n][1], alpha, -m1));
+          l1 += pa + pb;
+          split_pair(pa, pb, ph[n], pl[n]);
+        }
+        // P.V: n-tile c = channels 8c..8c+7 (natural order), values by ldmatrix.trans
+#pragma unroll
+        for (int c = 0; c < NEV; c += 2) {
+          const int ch = c + (lane >> 4);
+          uint32_t b[4];  // (tokens 0-7 | 8-15) x (channel chunk c | c + 1)
+          ldsm_x4_t(b, Vr + ltok * D + ((ch ^ (ltok & 7)) * 8));
+          mma_16816(acc2[c], ph[0], pl[0], ph[1], pl[1], b[0], b[1]);
+          mma_16816(acc2[c + 1], ph[0], pl[0], ph[1], pl[1], b[2], b[3]);
+        }
+      } else if (!kT && r_item) {
         // ============ residual tile: 16 FP16 tokens (chunk-swizzled rows)
         if (!in_res) {
           if (has_q) {
@@ -1217,8 +1524,34 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
     // ---------------- warp -> shared memory
     // (a parked quantized part, already in wo, is rescaled to the final max)
     if (dumped) __syncwarp();
+    if constexpr (kT) {
+      float lt = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+      float vbt = vb1 + __shfl_xor_sync(0xffffffffu, vb1, 1);
+      vbt += __shfl_xor_sync(0xffffffffu, vbt, 2);
+      if (tig == 0) {
+        wm[warp * H + g] = m1;
+        wl[warp * H + g] = lt;
+      }
+      float* oo = wo + (warp * H + g) * D;
+      const float fd = dumped ? ex2(dm[warp * H + g] - m1) : 0.0f;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
+      for (int c = 0; c < NEV; ++c) {
+        const float fs = 16777216.0f / static_cast<float>(1 << value_pos<VB, D>(c % KS));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float o = acc2[c][e] + acc2[c][e + 2];
+          if (in_res) {
+            const int ch = 8 * c + 2 * tig + e;
+            oo[ch] = dumped ? fmaf(oo[ch], fd, o) : o;
+          } else {
+            oo[(2 * tig + e) * (D / 8) + c] = fmaf(o, fs, vbt);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < (kT ? 0 : NT); ++j) {
       const float lt = reduce_over_g(l[j]);
       const float vbt = reduce_over_g(vb[j]);
       const int h = 4 * j + tig;
