@@ -689,6 +689,8 @@ def run_gpu(args):
                               "clocks": mx["clocks"]}
     if extra:
         result["other_workloads"] = extra
+    if not args.layers and not args.no_chunk:
+        result["chunk_tflops"] = measure_chunk_layers(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, step_s, cores, desc = oracle_sample(w, budget_s=args.cpu_budget, prefill=m["prefill"])
         result["cpu_baseline"] = {"value": round(tps, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -812,6 +814,56 @@ def _tensor_peak():
             return float(json.load(f)["bf16_tflops"]), "measured"
     except Exception:
         return 1900.0, "fallback"
+
+
+def measure_chunk_layers(dev, workload=2, layers=3, batch=2, reps=10):
+    """Causal chunk attention (every query of the context over the layer's
+    quantized cache) on the first `layers` layers of a workload at `batch`
+    sequences: median over `reps` timed passes of the layers (CUDA events on
+    the launching stream); TFLOP/s counts 4 d per visible (query, key) pair."""
+    import torch
+
+    from mixed_precision_quantized_quant_gb300 import kvq as K
+    from mixed_precision_quantized_quant_gb300 import workloads as W
+
+    w = W.scaled(W.workload(workload), batch=batch)
+    w = W.scaled(w, num_layers=layers, layers=tuple(w.layers[:layers]))
+    L, B, Hq, Hkv, D, T = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.context
+    stream = torch.cuda.Stream(device=dev)
+    cache = K.KVQCache(w.layers, B, Hq, Hkv, D, w.group_size, T, device=dev)
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            k, v = W.gen_kv(w, l, 0, T, device=dev)
+            cache.append(l, k, v, stream=stream)
+            del k, v
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(11)
+        q = torch.randn((B, Hq, T, D), generator=gen, device=dev).half()
+        out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            for l in range(L):
+                cache.chunk_attn(l, q, out, stream=stream)
+        stream.synchronize()
+        ms = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for l in range(L):
+                cache.chunk_attn(l, q, out, stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            ms.append(e0.elapsed_time(e1))
+    if cache.device_error(stream):
+        raise RuntimeError("device error word set (chunk attention)")
+    cache.close()
+    med = statistics.median(ms)
+    tflops = L * _chunk_flops(B, Hq, D, T, T) / (med / 1e3) / 1e12
+    peak, kind = _tensor_peak()
+    return {"value": round(tflops, 2), "unit": "TFLOP/s", "frac_of_bf16_peak": round(tflops / peak, 4),
+            "peak": peak, "peak_source": f"{kind} bf16 dense",
+            "config": {"workload": w.name, "layers": L, "batch": B, "queries": T, "context": T},
+            "ms_per_pass": round(med, 4), "passes": reps,
+            "kernel": "chunk_attn_kernel (tcgen05, accumulators in tensor memory) after its dequantize pass"}
 
 
 def run_chunk(args):
@@ -1033,6 +1085,7 @@ def main():
                     help="repetitions of the timed window (at least 10), each from the same saved cache state")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="profiling runs: skip the end-to-end leg")
+    ap.add_argument("--no-chunk", action="store_true", help="skip the chunk-attention extra key")
     ap.add_argument("--layers", type=int, default=0, help="profiling runs: only the workload's first N layers")
     ap.add_argument("--key-mode", choices=["channel", "token"], default="channel",
                     help="keys per channel over groups (KIVI) or per token (per-token-asym) on every layer")

@@ -45,7 +45,7 @@ constexpr int kChunkRows = 256;                        // (query, head) rows per
 constexpr int kChunkM = 128;                           // rows per group: the MMA's M
 constexpr int kChunkTile = 64;                         // tokens per tile
 constexpr int kChunkThreads = 256;                     // softmax threads, one per row
-constexpr int kChunkCtaThreads = kChunkThreads + 32;   // and the copy/MMA warp
+constexpr int kChunkCtaThreads = kChunkThreads + 64;   // the copy + score-MMA warp, the P.V-MMA warp
 constexpr int kDequantThreads = 256;
 
 // One dequantized tile, in the workspace and (copied verbatim) in shared
@@ -72,8 +72,8 @@ struct ChunkSmem {
   static constexpr uint32_t ph = stage + 2 * T::bytes;              // [256 rows][64 tokens] f16, hi
   static constexpr uint32_t pl = ph + kChunkRows * kChunkTile * 2;  // lo
   static constexpr uint32_t pgroup = kChunkM * kChunkTile * 2;      // bytes of one group's P
-  static constexpr uint32_t bars = pl + kChunkRows * kChunkTile * 2;  // 16 mbarriers
-  static constexpr uint32_t tslot = bars + 128;                     // tensor-memory address
+  static constexpr uint32_t bars = pl + kChunkRows * kChunkTile * 2;  // 20 mbarriers
+  static constexpr uint32_t tslot = bars + 192;                     // tensor-memory address
   static constexpr uint32_t bytes = tslot + 16;
   // tensor memory: S of buffer b, group g in columns [64 (2b + g), +64); O of
   // group g in [256 + D g, +D)
@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
   uint64_t* s_done = kfull + 8;  // [stage][group]: scores ready (commit)
   uint64_t* p_full = kfull + 12; // [group]: P' written, O rescaled (128 arrivals)
   uint64_t* o_done = kfull + 14; // [group]: P.V done (commit)
+  uint64_t* s_free = kfull + 16; // [stage][group]: the group's rows have read their scores (128 arrivals)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::tslot);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int grp = (tid >> 7) & 1;  // row group of a softmax thread
@@ -353,6 +354,7 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
     mbar_init(p_full + 1, kChunkM);
     mbar_init(o_done, 1);
     mbar_init(o_done + 1, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(s_free + i, kChunkM);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, L::tcols);
@@ -368,11 +370,15 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
   const int ntw = endW > p.n_q ? (endW - p.n_q + kTile - 1) / kTile : 0;
   const int ntiles = ntq + ntw;  // the unit's tiles 0 .. ntiles-1 (same numbering as the workspace)
 
-  if (warp == kChunkThreads / 32) {
-    // ================= copy/MMA warp: its first thread issues every bulk
-    // copy and every MMA.  Per tile it: S(it); the keys of tile it+1 into the
-    // other stage (freed by S(it-1)); the values and pairs of tile it into
-    // its stage (freed by P.V(it-2)); then P.V(it-1) once its softmax is done.
+  if (warp >= kChunkThreads / 32) {
+    // ================= MMA warps.  The first thread of warp 8 issues every
+    // bulk copy and the score MMAs: per tile it, S(it) (once the rows have
+    // read S(it-2) from the same buffer); the keys of tile it+1 into the other
+    // stage (freed by S(it-1)); the values and pairs of tile it into its stage
+    // (freed by P.V(it-2)).  The first thread of warp 9 issues the P.V MMAs
+    // of each tile once its softmax is done, so the two MMA streams are
+    // issued by different warps.
+    const bool score_warp = warp == kChunkThreads / 32;
     if ((tid & 31) == 0) {
       const uint32_t sq = smem_u32(sm + L::q);
       const uint32_t sst = smem_u32(sm + L::stage);
@@ -426,6 +432,10 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
         umma_commit(vfree + bs);
       };
       bool bad = false;
+      if (!score_warp) {
+#pragma unroll 1
+        for (int it = 0; it < ntiles && !bad; ++it) issue_pv(it, bad);
+      } else {
       copy_k(0);
       copy_v(0);
 #pragma unroll 1
@@ -437,6 +447,10 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
         const uint32_t kb_h = sst + bs * T::bytes, kb_l = kb_h + T::kl;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
+          // the group's rows have read S(it-2), the buffer's previous scores
+          if (it >= 2) bad = bad || !mbar_wait(s_free + 2 * bs + g, ((it - 2) >> 1) & 1, p.err);
+          if (bad) break;
+          tc_fence_after_sync();
           const uint32_t qg = sq + g * (kChunkM * D * 2);
           const uint32_t dS = tb + kTile * (2 * bs + g);
           const uint64_t dq = smem_desc(qg, 128, KC * 128);
@@ -447,6 +461,7 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
           for (int ks = 0; ks < D / 16; ++ks) umma_f16(dS, dq + 16 * ks, dkl + 16 * ks, idS, 1u);
           umma_commit(s_done + 2 * bs + g);
         }
+        if (bad) break;
         umma_commit(kfree + bs);
         // keys of tile it+1 into the other stage (its scores of tile it-1 are long done)
         if (it + 1 < ntiles) {
@@ -461,13 +476,12 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
           if (bad) break;
           copy_v(it);
         }
-        if (it >= 1) issue_pv(it - 1, bad);
       }
-      if (!bad && ntiles > 0) issue_pv(ntiles - 1, bad);
       // copies still in flight (only after a failed wait) must land before exit
       if (bad) {
         mbar_wait(kfull, 0, p.err, 1u << 16);
         mbar_wait(vfull, 0, p.err, 1u << 16);
+      }
       }
     }
     __syncwarp();
@@ -511,6 +525,8 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
       tmem_ld_wait(x1);
       tmem_ld_wait(x2);
       tmem_ld_wait(x3);
+      tc_fence_before_sync();
+      mbar_arrive(s_free + 2 * bs + grp);  // S buffer bs may take tile it+2
       auto score = [&](int j) -> float {
         const uint32_t v = j < 16 ? x0[j] : j < 32 ? x1[j - 16] : j < 48 ? x2[j - 32] : x3[j - 48];
         return (full || j < nvis) ? __uint_as_float(v) : -INFINITY;

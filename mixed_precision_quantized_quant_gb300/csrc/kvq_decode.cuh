@@ -974,12 +974,25 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         // value (scale, zero) and per-token key (scale, zero): the last reads
         constexpr int VW = VS_::VW;
         const int voff = (VB == 2 && D == 64) ? (g >> 1) : g * VW;
+        // (lanes with tig >= 2 read the odd token of each pair first: rows
+        // 0, 2, 5, 7, then 1, 3, 4, 6 of a pair group hit four different
+        // quarters of the banks for 32-byte rows)
         uint32_t vw[2][4][VW];
+        const int sw = tig >> 1;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-          for (int r4 = 0; r4 < 4; ++r4)
-            lds_words<VW>(vw[kb][r4], Vc + (16 * kb + 2 * tig + (r4 & 1) + 8 * (r4 >> 1)) * WV + voff);
+          for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t* vrow = Vc + (16 * kb + 8 * pr + 2 * tig) * WV + voff;
+            uint32_t wa[VW], wb[VW];
+            lds_words<VW>(wa, vrow + sw * WV);
+            lds_words<VW>(wb, vrow + (1 - sw) * WV);
+#pragma unroll
+            for (int x = 0; x < VW; ++x) {
+              vw[kb][2 * pr][x] = sw ? wb[x] : wa[x];
+              vw[kb][2 * pr + 1][x] = sw ? wa[x] : wb[x];
+            }
+          }
         float2 vsz[4][2], ksz[KM == 1 ? 4 : 1][2];
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
