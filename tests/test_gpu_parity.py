@@ -87,6 +87,15 @@ def test_per_token_keys_gqa_and_group_sizes(gqa, G):
                 key_mode=K.KEY_PER_TOKEN)
 
 
+@pytest.mark.parametrize("kb,vb", [(4, 2), (8, 4), (4, 8), (8, 8), (2, 4)])
+@pytest.mark.parametrize("gqa", [5, 8])
+def test_eight_head_tiles_group_128(kb, vb, gqa):
+    # 5-8 query heads per kv head at G = 128: the transposed 8-head form, whose
+    # four warps take the four 32-token slices of one key group per stage; a
+    # ragged prefill, then decode steps through a flush
+    _run_stream(kb, vb, 128, 128, 128, gqa, [3 * 128 + 5] + [1] * 130, attn_every=9, seed=kb * 16 + vb + gqa)
+
+
 @pytest.mark.parametrize("gqa", [1, 2, 3, 4, 5, 7, 8])
 def test_gqa_ratios(gqa):
     _run_stream(4, 2, 128, 32, 32, gqa, [96 + 17] + [1] * 20, attn_every=4, seed=gqa)
