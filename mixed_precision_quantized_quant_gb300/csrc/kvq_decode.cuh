@@ -97,6 +97,21 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int D, int NT, int cq, 
   return decode_smem_layout_stage(D, NT, stage_bytes(D, cq, W), W);
 }
 
+// Word of channel ch of head h inside a warp's partial-output rows: ch XOR a
+// 5-bit key of (h, ch / 32), a permutation within each 32-channel block, so
+// the merge still reads 32 consecutive channels from 32 banks.  The keys
+// spread the epilogue's stores over the banks: the 8-head form stores, per
+// instruction, one channel offset for all (head g, lane column tig) and the
+// key (g bits 0, 3, 4; tig = block bits 1, 2) tells the 32 lanes apart; the
+// 1-4-head form stores channel 16g + mt of head 4j + tig and the key (tig
+// bits 2, 3; block bits 0, 1) does the same with the channel's own bit 4.
+template <bool kT>
+__device__ __forceinline__ int wo_chan(int h, int ch) {
+  const int b = ch >> 5;
+  const int key = kT ? (((h & 1) | ((h >> 1) << 3)) ^ (b << 1)) : (((h & 3) << 2) | (b & 3));
+  return ch ^ (key & 31);
+}
+
 // Warps per CTA of an instantiation: 8 where two such CTAs fit in an SM's
 // shared memory (fewer CTAs per unit: fewer query-table builds and split
 // merges at the same occupancy), else 4.  3-bit values keep 4: they need more
@@ -670,7 +685,10 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
       // lane (g, tig): head g, channel pairs key_pair_channels(tig, pi)
       const int h = g;
       const bool live = h < p.gqa;
-      for (int pi = warp; pi < NPK; pi += W) {
+      // (each head's lanes start at another pair: the eight query rows are
+      // D/2 words apart, so the same pair of all heads would share a bank)
+      for (int pr = warp; pr < NPK; pr += W) {
+        const int pi = (pr + 2 * g) % NPK;
         int ca, cb;
         key_pair_channels<KB, D>(tig, pi, ca, cb);
         const __half z0 = __float2half(0.0f);
@@ -680,7 +698,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         qps_tab[kt_idx(0, pi, lane)] = h2_as_u32(__hmul2(q2, __float2half2_rn(f)));
       }
       // window keys (natural channel order): channels 16kk + 8rr + 2tig, +1
-      for (int kk = warp; kk < KS; kk += W) {
+      for (int kr = warp; kr < KS; kr += W) {
+        const int kk = (kr + g) % KS;
         for (int rr = 0; rr < 2; ++rr) {
           const int c = 16 * kk + 8 * rr + 2 * tig;
           qr_tab[rt_idx(0, kk, lane) + rr] = live ? h2_as_u32(__halves2half2(qu[h * D + c], qu[h * D + c + 1])) : 0u;
@@ -703,7 +722,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + (g >> 1);
         const bool live = h < p.gqa;
-        for (int pi = warp; pi < NPK; pi += W) {
+        for (int pr = warp; pr < NPK; pr += W) {
+          const int pi = (pr + 2 * (g >> 1)) % NPK;  // (bank spread, as above)
           int ca, cb;
           key_pair_channels<KB, D>(tig, pi, ca, cb);
           const __half z0 = __float2half(0.0f);
@@ -716,7 +736,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
           // per-token keys: the scaled query is the whole B operand (hi column; lo = 0)
           qps_tab[kt_idx(j, pi, lane)] = (KM == 1 && part) ? 0u : scaled;
         }
-        for (int kk = warp; kk < KS; kk += W) {
+        for (int kr = warp; kr < KS; kr += W) {
+          const int kk = (kr + (g >> 1)) % KS;
           for (int rr = 0; rr < 2; ++rr) {
             const int c = 16 * kk + 8 * rr + 2 * tig;
             qr_tab[rt_idx(j, kk, lane) + rr] =
@@ -1387,7 +1408,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
               const float fs = 16777216.0f / static_cast<float>(1 << value_pos<VB, D>(c % KS));
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                dd[(2 * tig + e) * (D / 8) + c] = fmaf(acc2[c][e] + acc2[c][e + 2], fs, vbt);
+                dd[wo_chan<true>(g, (2 * tig + e) * (D / 8) + c)] = fmaf(acc2[c][e] + acc2[c][e + 2], fs, vbt);
                 acc2[c][e] = 0.0f;
                 acc2[c][e + 2] = 0.0f;
               }
@@ -1462,8 +1483,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
               for (int mt = 0; mt < MTV; ++mt) {
                 const float fs = 16777216.0f / static_cast<float>(1 << value_pos<VB, D>(mt));
                 const int c0 = vq_channel<VB, D>(g, mt, 0), c1 = vq_channel<VB, D>(g, mt, 1);
-                if (c0 >= 0) dd[c0] = fmaf(acc[mt][j][0] + acc[mt][j][1], fs, vbt);
-                if (c1 >= 0) dd[c1] = fmaf(acc[mt][j][2] + acc[mt][j][3], fs, vbt);
+                if (c0 >= 0) dd[wo_chan<false>(h, c0)] = fmaf(acc[mt][j][0] + acc[mt][j][1], fs, vbt);
+                if (c1 >= 0) dd[wo_chan<false>(h, c1)] = fmaf(acc[mt][j][2] + acc[mt][j][3], fs, vbt);
               }
 #pragma unroll
               for (int mt = 0; mt < MTA; ++mt)
@@ -1555,10 +1576,10 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         for (int e = 0; e < 2; ++e) {
           const float o = acc2[c][e] + acc2[c][e + 2];
           if (in_res) {
-            const int ch = 8 * c + 2 * tig + e;
+            const int ch = wo_chan<true>(g, 8 * c + 2 * tig + e);
             oo[ch] = dumped ? fmaf(oo[ch], fd, o) : o;
           } else {
-            oo[(2 * tig + e) * (D / 8) + c] = fmaf(o, fs, vbt);
+            oo[wo_chan<true>(g, (2 * tig + e) * (D / 8) + c)] = fmaf(o, fs, vbt);
           }
         }
       }
@@ -1578,16 +1599,17 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           const float o0 = acc[mt][j][0] + acc[mt][j][1], o1 = acc[mt][j][2] + acc[mt][j][3];
-          oo[16 * mt + g] = dumped ? fmaf(oo[16 * mt + g], fd, o0) : o0;
-          oo[16 * mt + 8 + g] = dumped ? fmaf(oo[16 * mt + 8 + g], fd, o1) : o1;
+          const int w0 = wo_chan<false>(h, 16 * mt + g), w1 = wo_chan<false>(h, 16 * mt + 8 + g);
+          oo[w0] = dumped ? fmaf(oo[w0], fd, o0) : o0;
+          oo[w1] = dumped ? fmaf(oo[w1], fd, o1) : o1;
         }
       } else {
 #pragma unroll
         for (int mt = 0; mt < MTV; ++mt) {
           const float fs = 16777216.0f / static_cast<float>(1 << value_pos<VB, D>(mt));
           const int c0 = vq_channel<VB, D>(g, mt, 0), c1 = vq_channel<VB, D>(g, mt, 1);
-          if (c0 >= 0) oo[c0] = fmaf(acc[mt][j][0] + acc[mt][j][1], fs, vbt);
-          if (c1 >= 0) oo[c1] = fmaf(acc[mt][j][2] + acc[mt][j][3], fs, vbt);
+          if (c0 >= 0) oo[wo_chan<false>(h, c0)] = fmaf(acc[mt][j][0] + acc[mt][j][1], fs, vbt);
+          if (c1 >= 0) oo[wo_chan<false>(h, c1)] = fmaf(acc[mt][j][2] + acc[mt][j][3], fs, vbt);
         }
       }
     }
@@ -1612,7 +1634,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         const float mw = wm[w * H + h];
         if (mw == -INFINITY) continue;
         const float f = ex2(mw - M);
-        O += wo[(w * H + h) * D + c] * f;
+        O += wo[(w * H + h) * D + wo_chan<kT>(h, c)] * f;
         Lsum += wl[w * H + h] * f;
       }
       if (nparts == 1) {
