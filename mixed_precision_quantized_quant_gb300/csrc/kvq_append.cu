@@ -374,8 +374,8 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
       kpf[pi] = sc.mn;
       kpf[D + pi] = sc.r;
     }
-    ks16[ch] = sc.s16;
-    kz16[ch] = sc.z16;
+    ks16[kscale_pos(ch, D)] = sc.s16;
+    kz16[kscale_pos(ch, D)] = sc.z16;
   }
   if (tid < G) {
     const __half2 r = vpart[tid];

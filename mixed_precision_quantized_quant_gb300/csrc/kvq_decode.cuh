@@ -905,12 +905,13 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         if constexpr (KM == 0) {
           uint32_t zp[NPK];
           uint32_t zn[NPK], sn[NPK];
-          const uint32_t* zsrc = reinterpret_cast<const uint32_t*>(Kz + tig * (D / 4));
-          const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(Ks + tig * (D / 4));
+          // chunk j of this lane's channel quarter tig is stored chunk 4j + tig
+          const uint4* zsrc = reinterpret_cast<const uint4*>(Kz) + tig;
+          const uint4* ssrc = reinterpret_cast<const uint4*>(Ks) + tig;
 #pragma unroll
           for (int pi = 0; pi < NPK; pi += 4) {
-            const uint4 vz = *reinterpret_cast<const uint4*>(zsrc + pi);
-            const uint4 vs = *reinterpret_cast<const uint4*>(ssrc + pi);
+            const uint4 vz = zsrc[pi];
+            const uint4 vs = ssrc[pi];
             zn[pi] = vz.x; zn[pi + 1] = vz.y; zn[pi + 2] = vz.z; zn[pi + 3] = vz.w;
             sn[pi] = vs.x; sn[pi + 1] = vs.y; sn[pi + 2] = vs.z; sn[pi + 3] = vs.w;
           }
@@ -1106,18 +1107,20 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
             int ca, cb;
             key_pair_channels<KB, D>(tig, pi, ca, cb);
             const __half h0 = __float2half(0.0f);
-            zp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Kz[ca] : h0, cb >= 0 ? Kz[cb] : h0));
-            sp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Ks[ca] : h0, cb >= 0 ? Ks[cb] : h0));
+            const int pa = ca >= 0 ? kscale_pos(ca, D) : 0, pb = cb >= 0 ? kscale_pos(cb, D) : 0;
+            zp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Kz[pa] : h0, cb >= 0 ? Kz[pb] : h0));
+            sp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Ks[pa] : h0, cb >= 0 ? Ks[pb] : h0));
           }
         } else {
           constexpr int PW = KS_::PW;
           uint32_t zn[NPK], sn[NPK];
-          const uint32_t* zsrc = reinterpret_cast<const uint32_t*>(Kz + tig * (D / 4));
-          const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(Ks + tig * (D / 4));
+          // chunk j of this lane's channel quarter tig is stored chunk 4j + tig
+          const uint4* zsrc = reinterpret_cast<const uint4*>(Kz) + tig;
+          const uint4* ssrc = reinterpret_cast<const uint4*>(Ks) + tig;
 #pragma unroll
           for (int pi = 0; pi < NPK; pi += 4) {
-            const uint4 vz = *reinterpret_cast<const uint4*>(zsrc + pi);
-            const uint4 vs = *reinterpret_cast<const uint4*>(ssrc + pi);
+            const uint4 vz = zsrc[pi];
+            const uint4 vs = ssrc[pi];
             zn[pi] = vz.x; zn[pi + 1] = vz.y; zn[pi + 2] = vz.z; zn[pi + 3] = vz.w;
             sn[pi] = vs.x; sn[pi + 1] = vs.y; sn[pi + 2] = vs.z; sn[pi + 3] = vs.w;
           }

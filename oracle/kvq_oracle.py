@@ -310,10 +310,42 @@ KEY_PER_CHANNEL = 0   # keys per channel over the G tokens of a group (KIVI)
 KEY_PER_TOKEN = 1     # keys per token over their d channels, like values
 
 
+def key_scale_chunk_order(d: int) -> np.ndarray:
+    """Storage order of the per-channel key scale row and zero row of a record.
+
+    The pages fix the values (one fp16 scale and zero per channel and group), not
+    where a record keeps them; this is the library's storage decision.  Split the
+    d channels into chunks of 8 and the chunks into 4 equal quarters; the row
+    stores chunk j of every quarter together: position 4*j + t holds chunk
+    t*(d/32) + j.  Returns, for each stored position, the natural chunk index."""
+    per_quarter = d // 32
+    order = np.empty(d // 8, dtype=np.int64)
+    for t in range(4):
+        for j in range(per_quarter):
+            order[4 * j + t] = t * per_quarter + j
+    return order
+
+
+def key_scale_row_store(row: np.ndarray) -> np.ndarray:
+    """A length-d per-channel row (natural channel order) in record storage order."""
+    d = row.shape[0]
+    chunks = row.reshape(d // 8, 8)
+    return chunks[key_scale_chunk_order(d)].reshape(d)
+
+
+def key_scale_row_load(stored: np.ndarray) -> np.ndarray:
+    """Inverse of key_scale_row_store: back to natural channel order."""
+    d = stored.shape[0]
+    out = np.empty((d // 8, 8), dtype=stored.dtype)
+    out[key_scale_chunk_order(d)] = stored.reshape(d // 8, 8)
+    return out.reshape(d)
+
+
 def record_layout(d: int, group: int, k_bits: int, v_bits: int, key_mode: int = KEY_PER_CHANNEL) -> Dict[str, int]:
     """Byte offsets inside one group record.
 
-    Per-channel keys: [K codes][V codes][K scale d][K zero d][V (scale, zero) G].
+    Per-channel keys: [K codes][V codes][K scale d][K zero d][V (scale, zero) G],
+    the two d-long rows in key_scale_chunk_order.
     Per-token keys:   [K codes][V codes][K (scale, zero) G][V (scale, zero) G]."""
     wk = words_per_row(d, k_bits)
     wv = words_per_row(d, v_bits)
@@ -343,7 +375,7 @@ def build_group_record(k_grp: np.ndarray, v_grp: np.ndarray, k_bits: int, v_bits
         kparts = [np.stack([ks.astype(F16), kz.astype(F16)], axis=1).tobytes()]
     else:
         kc, ks, kz = quantize_keys_group(k_grp, k_bits)
-        kparts = [ks.astype(F16).tobytes(), kz.astype(F16).tobytes()]
+        kparts = [key_scale_row_store(ks.astype(F16)).tobytes(), key_scale_row_store(kz.astype(F16)).tobytes()]
     parts = [pack_rows(kc, k_bits).tobytes(), pack_rows(vc, v_bits).tobytes(), *kparts, vsz.tobytes()]
     return b"".join(parts)
 
@@ -361,8 +393,8 @@ def parse_group_record(rec: bytes, d: int, group: int, k_bits: int, v_bits: int,
         ksz = buf[lay["k_scale"]:lay["v_scale"]].view(F16).reshape(group, 2)
         k_hat = dequant_values(unpack_rows(kw, k_bits, d), ksz[:, 0], ksz[:, 1], k_bits)
     else:
-        ks = buf[lay["k_scale"]:lay["k_zero"]].view(F16)
-        kz = buf[lay["k_zero"]:lay["v_scale"]].view(F16)
+        ks = key_scale_row_load(buf[lay["k_scale"]:lay["k_zero"]].view(F16))
+        kz = key_scale_row_load(buf[lay["k_zero"]:lay["v_scale"]].view(F16))
         k_hat = dequant_keys(unpack_rows(kw, k_bits, d), ks, kz, k_bits)
     v_hat = dequant_values(unpack_rows(vw, v_bits, d), vs, vz, v_bits)
     return k_hat, v_hat

@@ -440,6 +440,34 @@ def test_record_layout_sizes():
                     assert O.record_layout(d, G, kb, vb)["bytes"] % 16 == 0
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_key_scale_rows_stored_chunk_order_worked(d):
+    # Per-channel key scale and zero rows are stored in 8-channel chunks, chunk j
+    # of each channel quarter side by side.  Worked orders (natural chunk index
+    # at each stored position), written out by hand:
+    #   d = 64:  quarters {0,1} {2,3} {4,5} {6,7} -> 0 2 4 6 | 1 3 5 7
+    #   d = 128: quarters {0..3} {4..7} {8..11} {12..15}
+    #            -> 0 4 8 12 | 1 5 9 13 | 2 6 10 14 | 3 7 11 15
+    hand = {64: [0, 2, 4, 6, 1, 3, 5, 7],
+            128: [0, 4, 8, 12, 1, 5, 9, 13, 2, 6, 10, 14, 3, 7, 11, 15]}[d]
+    assert list(O.key_scale_chunk_order(d)) == hand
+    # a group whose channel c spans [c, c + 1]: zero row = c, scale row = 1/qmax
+    G, bits = 32, 4
+    k = (np.arange(d)[None, :] + (np.arange(G)[:, None] % 2)).astype(np.float16)
+    v = np.zeros((G, d), dtype=np.float16)
+    rec = O.build_group_record(k, v, bits, 2)
+    lay = O.record_layout(d, G, bits, 2)
+    buf = np.frombuffer(rec, dtype=np.uint8)
+    zero_row = buf[lay["k_zero"]:lay["v_scale"]].view(np.float16).astype(np.int64)
+    expect = np.concatenate([np.arange(8 * c, 8 * c + 8) for c in hand])
+    assert (zero_row == expect).all()
+    scale_row = buf[lay["k_scale"]:lay["k_zero"]].view(np.float16)
+    assert (scale_row == np.float16(1.0 / 15.0)).all()
+    # and the parse restores every channel: dequantized keys are exact here
+    kh, _ = O.parse_group_record(rec, d, G, bits, 2)
+    assert np.abs(kh - k.astype(np.float64)).max() <= 2.0 ** -9
+
+
 # ---------------------------------------------------------------------------
 # Per-token-asym key mode ([KVTuner] A3-A4: the second quantization mode,
 # keys quantized per token like values)
