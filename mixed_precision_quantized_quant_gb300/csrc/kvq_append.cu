@@ -398,13 +398,14 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
   auto put_k = [&](int t, const uint32_t (&code)[8]) {
     uint32_t w0, w1;
     pack8<KB>(code, w0, w1);
+    const int xk = code_word_xor(WK, true, t);
     if (KB == 8) {
-      *reinterpret_cast<uint2*>(kc + t * WK + 2 * c) = make_uint2(w0, w1);
+      *reinterpret_cast<uint2*>(kc + t * WK + ((2 * c) ^ xk)) = make_uint2(w0, w1);
     } else if (KB == 4) {
-      kc[t * WK + c] = w0;
+      kc[t * WK + (c ^ xk)] = w0;
     } else {  // KB == 2: two lanes form one word
       const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
-      if ((c & 1) == 0) kc[t * WK + c / 2] = w0 | (other << 16);
+      if ((c & 1) == 0) kc[t * WK + ((c / 2) ^ xk)] = w0 | (other << 16);
     }
   };
   if (ktok) {
@@ -462,13 +463,14 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
       quant8(xv[k], mn2, r2, (1u << VB) - 1, vsc + t, 0, static_cast<float>((1 << VB) - 1), code);
       uint32_t w0, w1;
       pack8<VB>(code, w0, w1);
+      const int xv = code_word_xor(WV, false, t);
       if (VB == 8) {
-        *reinterpret_cast<uint2*>(vc + t * WV + 2 * c) = make_uint2(w0, w1);
+        *reinterpret_cast<uint2*>(vc + t * WV + ((2 * c) ^ xv)) = make_uint2(w0, w1);
       } else if (VB == 4) {
-        vc[t * WV + c] = w0;
+        vc[t * WV + (c ^ xv)] = w0;
       } else {
         const uint32_t other = __shfl_xor_sync(0xffffffffu, w0, 1);
-        if ((c & 1) == 0) vc[t * WV + c / 2] = w0 | (other << 16);
+        if ((c & 1) == 0) vc[t * WV + ((c / 2) ^ xv)] = w0 | (other << 16);
       }
     }
   } else {

@@ -183,10 +183,11 @@ __global__ void __launch_bounds__(kDequantThreads) chunk_dequant_kernel(ChunkPar
         if (!in_range(rec, p.rec_bytes, p.buf_lo, p.buf_hi, p.err)) continue;  // debug builds
         const uint32_t* krow = reinterpret_cast<const uint32_t*>(rec) + rr * p.wk;
         const uint32_t* vrow = reinterpret_cast<const uint32_t*>(rec) + voff + rr * p.wv;
-        kw0[j] = krow[ku.wa];
-        if (ku.second_word()) kw1[j] = krow[ku.wa + 1];
-        vw0[j] = vrow[vu.wa];
-        if (vu.second_word()) vw1[j] = vrow[vu.wa + 1];
+        const int xk = code_word_xor(p.wk, true, rr), xv = code_word_xor(p.wv, false, rr);
+        kw0[j] = krow[ku.wa ^ xk];
+        if (ku.second_word()) kw1[j] = krow[(ku.wa + 1) ^ xk];
+        vw0[j] = vrow[vu.wa ^ xv];
+        if (vu.second_word()) vw1[j] = vrow[(vu.wa + 1) ^ xv];
         if (p.km) ksz[j] = *reinterpret_cast<const __half2*>(rec + p.off_kscale + rr * 4);
       }
     }

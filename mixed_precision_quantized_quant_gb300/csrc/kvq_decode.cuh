@@ -129,6 +129,27 @@ __host__ __device__ constexpr int decode_warps() {
 // ------------------------------------------------------------------ unpacking
 
 template <int N>
+__device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint32_t* p);
+
+// N words w0 .. w0 + N - 1 of a code row stored with word-index XOR xm (xm
+// moves whole 4-word groups, or N-word groups when N < 4)
+template <int N>
+__device__ __forceinline__ void lds_row_words(uint32_t (&w)[N], const uint32_t* row, int w0, int xm) {
+  if constexpr (N < 4) {
+    lds_words<N>(w, row + (w0 ^ xm));
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + ((w0 + i) ^ xm));
+      w[i] = v.x;
+      w[i + 1] = v.y;
+      w[i + 2] = v.z;
+      w[i + 3] = v.w;
+    }
+  }
+}
+
+template <int N>
 __device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint32_t* p) {
   if constexpr (N == 1) {
     w[0] = p[0];
@@ -960,7 +981,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         {
           uint32_t wr[4][WT];
 #pragma unroll
-          for (int rw = 0; rw < 4; ++rw) lds_words<WT>(wr[rw], Kc + (8 * rw + g) * WK + tig * WT);
+          for (int rw = 0; rw < 4; ++rw)
+            lds_row_words<WT>(wr[rw], Kc + (8 * rw + g) * WK, tig * WT, code_word_xor(WK, true, g));
 #pragma unroll
           for (int wi = 0; wi < WT; ++wi) {
             uint32_t e[4][PW];
@@ -1005,10 +1027,10 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
           for (int pr = 0; pr < 2; ++pr) {
-            const uint32_t* vrow = Vc + (16 * kb + 8 * pr + 2 * tig) * WV + voff;
+            const int ra = 16 * kb + 8 * pr + 2 * tig + sw, rb = 16 * kb + 8 * pr + 2 * tig + 1 - sw;
             uint32_t wa[VW], wb[VW];
-            lds_words<VW>(wa, vrow + sw * WV);
-            lds_words<VW>(wb, vrow + (1 - sw) * WV);
+            lds_row_words<VW>(wa, Vc + ra * WV, voff, code_word_xor(WV, false, ra));
+            lds_row_words<VW>(wb, Vc + rb * WV, voff, code_word_xor(WV, false, rb));
 #pragma unroll
             for (int x = 0; x < VW; ++x) {
               vw[kb][2 * pr][x] = sw ? wb[x] : wa[x];
@@ -1243,7 +1265,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
             constexpr int WT = KS_::WT, PW = KS_::PW;
             uint32_t wr[4][WT];
 #pragma unroll
-            for (int rw = 0; rw < 4; ++rw) lds_words<WT>(wr[rw], Kc + (8 * rw + g) * WK + tig * WT);
+            for (int rw = 0; rw < 4; ++rw)
+              lds_row_words<WT>(wr[rw], Kc + (8 * rw + g) * WK, tig * WT, code_word_xor(WK, true, g));
 #pragma unroll
             for (int wi = 0; wi < WT; ++wi) {
               uint32_t e[4][PW];
@@ -1313,7 +1336,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
           } else {
             const int voff = (VB == 2 && D == 64) ? (g >> 1) : g * VW;
 #pragma unroll
-            for (int r4 = 0; r4 < 4; ++r4) lds_words<VW>(vw[t][r4], Vc + (tb + tig + 4 * r4) * WV + voff);
+            for (int r4 = 0; r4 < 4; ++r4)
+              lds_row_words<VW>(vw[t][r4], Vc + (tb + tig + 4 * r4) * WV, voff, code_word_xor(WV, false, tig));
           }
         }
 

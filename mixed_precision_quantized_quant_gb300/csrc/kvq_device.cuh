@@ -91,6 +91,16 @@ constexpr int kFlush = 1, kResidual = 2, kUpdateState = 4;
 // one instruction then fall in four different bank groups.
 __host__ __device__ constexpr int kscale_chunk_pos(int c, int D) { return (c % (D / 32)) * 4 + c / (D / 32); }
 __host__ __device__ constexpr int kscale_pos(int ch, int D) { return kscale_chunk_pos(ch >> 3, D) * 8 + (ch & 7); }
+
+// XOR applied to the word index inside token row t (within its record) of a
+// record's code rows.  Rows of 128 or 64 bytes would otherwise put the rows a
+// warp reads at once on the same banks: 8-bit keys at 32 words a row swap the
+// 16-byte halves of each 32-byte block on odd rows; values at 16 words a row
+// swap the row's 32-byte halves when t & 2; values at 32 words a row XOR the
+// 32-byte block index with t & 3.  Shorter rows are stored as packed.
+__host__ __device__ constexpr int code_word_xor(int words, bool key, int t) {
+  return key ? (words == 32 ? (t & 1) << 2 : 0) : (words == 16 ? (t & 2) << 2 : (words == 32 ? (t & 3) << 3 : 0));
+}
 // one CTA per unit (a single-token append): each CTA reads and advances its
 // own unit's counter, no cross-CTA handshake
 constexpr int kPerUnit = 8;

@@ -341,11 +341,53 @@ def key_scale_row_load(stored: np.ndarray) -> np.ndarray:
     return out.reshape(d)
 
 
+def code_row_word_xor(words_per_token: int, is_key: bool, t: int) -> int:
+    """Where token row t (0-based inside its record) keeps its packed words.
+
+    Like the scale rows, this is the library's storage decision; the pages fix
+    the packing inside a word only.  Word w of the row is stored at index
+    w XOR (the value returned):
+      keys with 32 words a row (8-bit, d = 128): 4 on odd rows, else 0;
+      values with 16 words a row: 8 when bit 1 of t is set, else 0;
+      values with 32 words a row: 8 * (t mod 4);
+      every other row is stored as packed (0)."""
+    if is_key:
+        return 4 * (t % 2) if words_per_token == 32 else 0
+    if words_per_token == 16:
+        return 8 if (t // 2) % 2 == 1 else 0
+    if words_per_token == 32:
+        return 8 * (t % 4)
+    return 0
+
+
+def code_rows_store(words: np.ndarray, is_key: bool) -> np.ndarray:
+    """Packed rows [G, W] (row t = token t of the record) in storage order."""
+    n, w = words.shape
+    out = np.empty_like(words)
+    for t in range(n):
+        x = code_row_word_xor(w, is_key, t)
+        for i in range(w):
+            out[t, i ^ x] = words[t, i]
+    return out
+
+
+def code_rows_load(stored: np.ndarray, is_key: bool) -> np.ndarray:
+    """Inverse of code_rows_store."""
+    n, w = stored.shape
+    out = np.empty_like(stored)
+    for t in range(n):
+        x = code_row_word_xor(w, is_key, t)
+        for i in range(w):
+            out[t, i] = stored[t, i ^ x]
+    return out
+
+
 def record_layout(d: int, group: int, k_bits: int, v_bits: int, key_mode: int = KEY_PER_CHANNEL) -> Dict[str, int]:
     """Byte offsets inside one group record.
 
     Per-channel keys: [K codes][V codes][K scale d][K zero d][V (scale, zero) G],
-    the two d-long rows in key_scale_chunk_order.
+    the two d-long rows in key_scale_chunk_order; code rows in the word order
+    of code_row_word_xor.
     Per-token keys:   [K codes][V codes][K (scale, zero) G][V (scale, zero) G]."""
     wk = words_per_row(d, k_bits)
     wv = words_per_row(d, v_bits)
@@ -376,7 +418,8 @@ def build_group_record(k_grp: np.ndarray, v_grp: np.ndarray, k_bits: int, v_bits
     else:
         kc, ks, kz = quantize_keys_group(k_grp, k_bits)
         kparts = [key_scale_row_store(ks.astype(F16)).tobytes(), key_scale_row_store(kz.astype(F16)).tobytes()]
-    parts = [pack_rows(kc, k_bits).tobytes(), pack_rows(vc, v_bits).tobytes(), *kparts, vsz.tobytes()]
+    parts = [code_rows_store(pack_rows(kc, k_bits), True).tobytes(),
+             code_rows_store(pack_rows(vc, v_bits), False).tobytes(), *kparts, vsz.tobytes()]
     return b"".join(parts)
 
 
@@ -385,8 +428,8 @@ def parse_group_record(rec: bytes, d: int, group: int, k_bits: int, v_bits: int,
     """Inverse of build_group_record's layout: returns dequantized K, V [G, d] fp64."""
     lay = record_layout(d, group, k_bits, v_bits, key_mode)
     buf = np.frombuffer(rec, dtype=np.uint8)
-    kw = buf[lay["k_codes"]:lay["v_codes"]].view(np.uint32).reshape(group, lay["wk"])
-    vw = buf[lay["v_codes"]:lay["k_scale"]].view(np.uint32).reshape(group, lay["wv"])
+    kw = code_rows_load(buf[lay["k_codes"]:lay["v_codes"]].view(np.uint32).reshape(group, lay["wk"]), True)
+    vw = code_rows_load(buf[lay["v_codes"]:lay["k_scale"]].view(np.uint32).reshape(group, lay["wv"]), False)
     vsz = buf[lay["v_scale"]:lay["bytes"]].view(F16).reshape(group, 2)
     vs, vz = vsz[:, 0], vsz[:, 1]
     if key_mode == KEY_PER_TOKEN:

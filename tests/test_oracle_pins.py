@@ -468,6 +468,46 @@ def test_key_scale_rows_stored_chunk_order_worked(d):
     assert np.abs(kh - k.astype(np.float64)).max() <= 2.0 ** -9
 
 
+def test_code_row_word_order_worked():
+    # Stored word order of code rows, written out by hand for rows whose packed
+    # words are 0, 1, 2, ... (entry i = the packed word kept at index i).
+    a16, a32 = list(range(16)), list(range(32))
+    swap4 = [4, 5, 6, 7, 0, 1, 2, 3]
+    k8_row1 = [w + 8 * b for b in range(4) for w in swap4]            # 8-bit keys, d = 128, odd row
+    v16_row2 = list(range(8, 16)) + list(range(8))                    # 16-word value rows, t & 2
+    v32 = {1: list(range(8, 16)) + list(range(8)) + list(range(24, 32)) + list(range(16, 24)),
+           2: list(range(16, 32)) + list(range(16)),
+           3: list(range(24, 32)) + list(range(16, 24)) + list(range(8, 16)) + list(range(8))}
+    rows32 = np.tile(np.arange(32, dtype=np.uint32), (4, 1))
+    rows16 = np.tile(np.arange(16, dtype=np.uint32), (4, 1))
+    k = O.code_rows_store(rows32, True)
+    assert list(k[0]) == a32 and list(k[1]) == k8_row1 and list(k[2]) == a32 and list(k[3]) == k8_row1
+    v = O.code_rows_store(rows16, False)
+    assert list(v[0]) == a16 and list(v[1]) == a16 and list(v[2]) == v16_row2 and list(v[3]) == v16_row2
+    v = O.code_rows_store(rows32, False)
+    assert list(v[0]) == a32 and all(list(v[t]) == v32[t] for t in (1, 2, 3))
+    # 16-word key rows (4-bit, d = 128) and 8-word rows are kept as packed
+    assert (O.code_rows_store(rows16, True) == rows16).all()
+    assert (O.code_rows_store(rows32[:, :8], False) == rows32[:, :8]).all()
+    for is_key, rows in ((True, rows32), (False, rows16), (False, rows32)):
+        assert (O.code_rows_load(O.code_rows_store(rows, is_key), is_key) == rows).all()
+    # through a record: an 8-bit key code row and a 4-bit value code row in storage order
+    G, d = 32, 128
+    rng = np.random.default_rng(5)
+    kx = rng.standard_normal((G, d)).astype(np.float16)
+    vx = rng.standard_normal((G, d)).astype(np.float16)
+    rec = O.build_group_record(kx, vx, 8, 4)
+    lay = O.record_layout(d, G, 8, 4)
+    buf = np.frombuffer(rec, dtype=np.uint8)
+    kc, _, _ = O.quantize_keys_group(kx, 8)
+    vc, _, _ = O.quantize_values_tokens(vx, 4)
+    kst = buf[lay["k_codes"]:lay["v_codes"]].view(np.uint32).reshape(G, 32)
+    vst = buf[lay["v_codes"]:lay["k_scale"]].view(np.uint32).reshape(G, 16)
+    assert (kst[1] == O.pack_rows(kc, 8)[1][k8_row1]).all()
+    assert (vst[2] == O.pack_rows(vc, 4)[2][v16_row2]).all()
+    assert (vst[0] == O.pack_rows(vc, 4)[0]).all()
+
+
 # ---------------------------------------------------------------------------
 # Per-token-asym key mode ([KVTuner] A3-A4: the second quantization mode,
 # keys quantized per token like values)
@@ -487,7 +527,7 @@ def test_per_token_key_record_quantizes_along_tokens(bits):
     lay = O.record_layout(d, G, bits, 4, O.KEY_PER_TOKEN)
     assert len(rec) == lay["bytes"]
     buf = np.frombuffer(rec, dtype=np.uint8)
-    codes = O.unpack_rows(buf[lay["k_codes"]:lay["v_codes"]].view(np.uint32).reshape(G, lay["wk"]), bits, d)
+    codes = O.unpack_rows(O.code_rows_load(buf[lay["k_codes"]:lay["v_codes"]].view(np.uint32).reshape(G, lay["wk"]), True), bits, d)
     ksz = buf[lay["k_scale"]:lay["v_scale"]].view(np.float16).reshape(G, 2)
     kf = k.astype(np.float64)
     rows = np.arange(G)
