@@ -125,7 +125,10 @@ typedef struct kvq_handle kvq_handle;
  *   A code row is one token's head_dim codes, least significant field first:
  *   for b in {2,4,8} field j of word w is channel w*32/b + j at bits [b*j, b*j+b);
  *   for b = 3 word w holds channels 11w .. 11w+10, fields 0..9 3-bit at bit 3j
- *   and field 10 2-bit at bits 30..31.
+ *   and field 10 2-bit at bits 30..31.  Packed word w of token row t (t counted
+ *   inside the record) is stored at index w XOR x: key rows of 32 words:
+ *   x = 4 on odd t; value rows of 16 words: x = 8 when t & 2; value rows of 32
+ *   words: x = 8 * (t & 3); all other rows x = 0.
  *   residual_k + u * residual_stride (and residual_v likewise) is a ring of
  *   `residual` slots of head_dim fp16 holding the window tokens
  *   [quantized_tokens, tokens); token i sits in slot i % residual, and
