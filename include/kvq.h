@@ -119,9 +119,10 @@ typedef struct kvq_handle kvq_handle;
  *     [K scale: head_dim f16][K zero: head_dim f16]   (per-channel keys), or
  *     [K (scale, zero): G pairs of f16]               (per-token keys)
  *     [V (scale, zero): G pairs of f16]
- *   Each per-channel key row is stored in 8-channel chunks, chunk j of each
- *   channel quarter side by side: position 4j + t holds the channels of chunk
- *   t*head_dim/32 + j (head_dim 64: chunks 0 2 4 6 1 3 5 7).
+ *   With 2-, 4- or 8-bit keys each per-channel key row is stored in 8-channel
+ *   chunks, chunk j of each channel quarter side by side: position 4j + t
+ *   holds the channels of chunk t*head_dim/32 + j (head_dim 64: chunks
+ *   0 2 4 6 1 3 5 7); 3-bit keys keep channel order.
  *   A code row is one token's head_dim codes, least significant field first:
  *   for b in {2,4,8} field j of word w is channel w*32/b + j at bits [b*j, b*j+b);
  *   for b = 3 word w holds channels 11w .. 11w+10, fields 0..9 3-bit at bit 3j

@@ -374,8 +374,9 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
       kpf[pi] = sc.mn;
       kpf[D + pi] = sc.r;
     }
-    ks16[kscale_pos(ch, D)] = sc.s16;
-    kz16[kscale_pos(ch, D)] = sc.z16;
+    const int pos = KB == 3 ? ch : kscale_pos(ch, D);
+    ks16[pos] = sc.s16;
+    kz16[pos] = sc.z16;
   }
   if (tid < G) {
     const __half2 r = vpart[tid];

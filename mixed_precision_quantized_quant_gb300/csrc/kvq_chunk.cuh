@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kDequantThreads) chunk_dequant_kernel(ChunkPar
       const uint8_t* recB = urec + static_cast<int64_t>(gB) * p.rec_bytes + p.off_kscale;
       if (!in_range(recA, 4 * D, p.buf_lo, p.buf_hi, p.err) || !in_range(recB, 4 * D, p.buf_lo, p.buf_hi, p.err))
         return;  // debug builds
-      const int cs = kscale_pos(c0, D);  // (c0 starts an 8-channel chunk)
+      const int cs = KB == 3 ? c0 : kscale_pos(c0, D);  // (c0 starts an 8-channel chunk)
       const uint4 sa = *reinterpret_cast<const uint4*>(recA + cs * 2);
       const uint4 za = *reinterpret_cast<const uint4*>(recA + D * 2 + cs * 2);
       const uint4 sb = *reinterpret_cast<const uint4*>(recB + cs * 2);

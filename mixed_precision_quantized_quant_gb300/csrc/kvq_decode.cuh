@@ -970,14 +970,12 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
         }
         // ---- scores of the slice's 32 tokens: n-tile n = tokens 8n..8n+7,
         // column 2tig + e = token 8n + 2tig + e; rows g (hi part) and g + 8 (lo)
-        float sc[4][4], sx[4][4];
+        // one accumulator chain per n-tile, started at the key zero term (row g)
+        float sc[4][4];
 #pragma unroll
         for (int n = 0; n < 4; ++n)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            sc[n][e] = 0.0f;
-            sx[n][e] = 0.0f;
-          }
+          for (int e = 0; e < 4; ++e) sc[n][e] = (e < 2) ? bias1 : 0.0f;
         {
           uint32_t wr[4][WT];
 #pragma unroll
@@ -1010,7 +1008,7 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
               }
 #pragma unroll
               for (int n = 0; n < 4; ++n)
-                mma_16816((kk & 1) ? sx[n] : sc[n], a0, a1, a2, a3, e[n][2 * k2], e[n][2 * k2 + 1]);
+                mma_16816(sc[n], a0, a1, a2, a3, e[n][2 * k2], e[n][2 * k2 + 1]);
             }
           }
         }
@@ -1059,9 +1057,9 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             if constexpr (KM == 1) {
-              sv[n][e] = fmaf(ksz[n][e].x, sc[n][e] + sx[n][e], ksz[n][e].y * qsj[0]);
+              sv[n][e] = fmaf(ksz[n][e].x, sc[n][e], ksz[n][e].y * qsj[0]);
             } else {
-              sv[n][e] = ((sc[n][e] + sx[n][e]) + (sc[n][e + 2] + sx[n][e + 2])) + bias1;
+              sv[n][e] = sc[n][e] + sc[n][e + 2];
             }
             tmax = fmaxf(tmax, sv[n][e]);
           }
@@ -1129,9 +1127,8 @@ __global__ void __launch_bounds__(32 * decode_warps<KB, VB, D, NT, KM>(),
             int ca, cb;
             key_pair_channels<KB, D>(tig, pi, ca, cb);
             const __half h0 = __float2half(0.0f);
-            const int pa = ca >= 0 ? kscale_pos(ca, D) : 0, pb = cb >= 0 ? kscale_pos(cb, D) : 0;
-            zp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Kz[pa] : h0, cb >= 0 ? Kz[pb] : h0));
-            sp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Ks[pa] : h0, cb >= 0 ? Ks[pb] : h0));
+            zp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Kz[ca] : h0, cb >= 0 ? Kz[cb] : h0));
+            sp[pi] = h2_as_u32(__halves2half2(ca >= 0 ? Ks[ca] : h0, cb >= 0 ? Ks[cb] : h0));
           }
         } else {
           constexpr int PW = KS_::PW;

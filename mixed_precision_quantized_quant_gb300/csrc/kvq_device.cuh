@@ -85,10 +85,12 @@ struct AppendParams {
 constexpr int kFlush = 1, kResidual = 2, kUpdateState = 4;
 
 // Stored position of channel ch in a group record's per-channel key scale row
-// and zero row.  The rows are kept in 8-channel chunks with chunk j of each of
-// the four channel quarters side by side (position 4j + t holds chunk
-// t*D/32 + j): decode lanes own one quarter each, and their four chunk loads of
-// one instruction then fall in four different bank groups.
+// and zero row (2-, 4- and 8-bit keys; 3-bit keys keep channel order).  The
+// rows are kept in 8-channel chunks with chunk j of each of the four channel
+// quarters side by side (position 4j + t holds chunk t*D/32 + j): decode lanes
+// own one quarter each, and their four chunk loads of one instruction then
+// fall in four different bank groups.  The 3-bit decode path reads single
+// channels of 11-channel words, which gains nothing from the order.
 __host__ __device__ constexpr int kscale_chunk_pos(int c, int D) { return (c % (D / 32)) * 4 + c / (D / 32); }
 __host__ __device__ constexpr int kscale_pos(int ch, int D) { return kscale_chunk_pos(ch >> 3, D) * 8 + (ch & 7); }
 

@@ -311,7 +311,8 @@ KEY_PER_TOKEN = 1     # keys per token over their d channels, like values
 
 
 def key_scale_chunk_order(d: int) -> np.ndarray:
-    """Storage order of the per-channel key scale row and zero row of a record.
+    """Storage order of the per-channel key scale row and zero row of a record
+    with 2-, 4- or 8-bit keys (3-bit keys keep the natural channel order).
 
     The pages fix the values (one fp16 scale and zero per channel and group), not
     where a record keeps them; this is the library's storage decision.  Split the
@@ -386,8 +387,8 @@ def record_layout(d: int, group: int, k_bits: int, v_bits: int, key_mode: int = 
     """Byte offsets inside one group record.
 
     Per-channel keys: [K codes][V codes][K scale d][K zero d][V (scale, zero) G],
-    the two d-long rows in key_scale_chunk_order; code rows in the word order
-    of code_row_word_xor.
+    the two d-long rows in key_scale_chunk_order (2-, 4-, 8-bit keys; channel
+    order for 3-bit keys); code rows in the word order of code_row_word_xor.
     Per-token keys:   [K codes][V codes][K (scale, zero) G][V (scale, zero) G]."""
     wk = words_per_row(d, k_bits)
     wv = words_per_row(d, v_bits)
@@ -417,7 +418,10 @@ def build_group_record(k_grp: np.ndarray, v_grp: np.ndarray, k_bits: int, v_bits
         kparts = [np.stack([ks.astype(F16), kz.astype(F16)], axis=1).tobytes()]
     else:
         kc, ks, kz = quantize_keys_group(k_grp, k_bits)
-        kparts = [key_scale_row_store(ks.astype(F16)).tobytes(), key_scale_row_store(kz.astype(F16)).tobytes()]
+        ks, kz = ks.astype(F16), kz.astype(F16)
+        if k_bits != 3:
+            ks, kz = key_scale_row_store(ks), key_scale_row_store(kz)
+        kparts = [ks.tobytes(), kz.tobytes()]
     parts = [code_rows_store(pack_rows(kc, k_bits), True).tobytes(),
              code_rows_store(pack_rows(vc, v_bits), False).tobytes(), *kparts, vsz.tobytes()]
     return b"".join(parts)
@@ -436,8 +440,10 @@ def parse_group_record(rec: bytes, d: int, group: int, k_bits: int, v_bits: int,
         ksz = buf[lay["k_scale"]:lay["v_scale"]].view(F16).reshape(group, 2)
         k_hat = dequant_values(unpack_rows(kw, k_bits, d), ksz[:, 0], ksz[:, 1], k_bits)
     else:
-        ks = key_scale_row_load(buf[lay["k_scale"]:lay["k_zero"]].view(F16))
-        kz = key_scale_row_load(buf[lay["k_zero"]:lay["v_scale"]].view(F16))
+        ks = buf[lay["k_scale"]:lay["k_zero"]].view(F16)
+        kz = buf[lay["k_zero"]:lay["v_scale"]].view(F16)
+        if k_bits != 3:
+            ks, kz = key_scale_row_load(ks), key_scale_row_load(kz)
         k_hat = dequant_keys(unpack_rows(kw, k_bits, d), ks, kz, k_bits)
     v_hat = dequant_values(unpack_rows(vw, v_bits, d), vs, vz, v_bits)
     return k_hat, v_hat

@@ -466,6 +466,11 @@ def test_key_scale_rows_stored_chunk_order_worked(d):
     # and the parse restores every channel: dequantized keys are exact here
     kh, _ = O.parse_group_record(rec, d, G, bits, 2)
     assert np.abs(kh - k.astype(np.float64)).max() <= 2.0 ** -9
+    # 3-bit keys keep the natural channel order
+    rec3 = O.build_group_record(k, v, 3, 2)
+    lay3 = O.record_layout(d, G, 3, 2)
+    buf3 = np.frombuffer(rec3, dtype=np.uint8)
+    assert (buf3[lay3["k_zero"]:lay3["v_scale"]].view(np.float16).astype(np.int64) == np.arange(d)).all()
 
 
 def test_code_row_word_order_worked():
