@@ -222,7 +222,7 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
     // one CTA per unit: its flush jobs (if the window reaches its bound) and its new token
     ap.mode = kvq::kFlush | kvq::kResidual | kvq::kUpdateState | kvq::kPerUnit;
     ap.ctas = P.units;
-    e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(P.units, 1), kvq::append_block_threads(P.G), smem, s);
+    e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(P.units, 1), kvq::append_block_threads(lp.kb, lp.vb, P.G), smem, s);
   } else {
     if (nflush > 0) {
       const int64_t jobs = nflush * P.units;
@@ -230,7 +230,7 @@ kvq_status launch_append(kvq_handle* h, int layer, const void* K, const void* V,
       ap.mode = kvq::kFlush | (nres == 0 ? kvq::kUpdateState : 0);
       ap.ctas = ctas;
       e = kvq::append_dispatch(lp.kb, lp.vb, P.D, ap, dim3(static_cast<unsigned>(ctas), 1),
-                               kvq::append_block_threads(P.G), smem, s);
+                               kvq::append_block_threads(lp.kb, lp.vb, P.G), smem, s);
     }
     if (e == cudaSuccess && nres > 0) {
       const int64_t chunks = (nres + 15) / 16;
@@ -392,7 +392,7 @@ kvq_status kvq_create(const kvq_config* cfg, void* dev_buf, size_t bytes, kvq_ha
     if (gsz > kMaxGrid) gsz = kMaxGrid;
     h->grid.push_back(gsz);
     const size_t asmem = kvq::append_smem_bytes(lp.kb, lp.vb, P.D, P.G, static_cast<int>(lp.rec_bytes));
-    const int aocc = kvq::append_ctas_per_sm(lp.kb, lp.vb, P.D, kvq::append_block_threads(P.G), asmem);
+    const int aocc = kvq::append_ctas_per_sm(lp.kb, lp.vb, P.D, P.G, kvq::append_block_threads(lp.kb, lp.vb, P.G), asmem);
     if (aocc < 1) {
       delete h;
       return KVQ_ERR_UNSUPPORTED;

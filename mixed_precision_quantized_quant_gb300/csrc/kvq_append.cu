@@ -95,16 +95,22 @@ struct AppendSmem {
       off_bars, total;
 };
 
-// Flush CTAs run 4*G threads: each thread owns one 16-byte chunk of D/32 rows.
-__host__ __device__ constexpr int append_threads(int G) { return 4 * G; }
+// Flush CTAs run 4*G threads, each owning one 16-byte chunk of D/32 rows, with
+// two stages; "wide" CTAs (G = 128 without 3-bit codes) run 2*G threads, each
+// owning one chunk of D/16 rows, with one stage that is refilled as soon as
+// every thread holds its rows in registers, so that two CTAs fit an SM instead
+// of one and cover each other's barrier waits.  (At G = 64 the same form, four
+// 128-thread CTAs per SM instead of two of 256, measured no faster.)
+__host__ __device__ constexpr bool append_wide(int KB, int VB, int G) { return G == 128 && KB != 3 && VB != 3; }
+__host__ __device__ constexpr int append_threads(int G, bool wide) { return (wide ? 2 : 4) * G; }
 
-__host__ __device__ inline AppendSmem append_smem_layout(int D, int G, int rec_bytes) {
+__host__ __device__ inline AppendSmem append_smem_layout(int D, int G, int rec_bytes, bool wide) {
   AppendSmem a;
   a.tile = G * D * 2;
-  const int warps = append_threads(G) / 32;
+  const int warps = append_threads(G, wide) / 32;
   int off = 2 * a.tile;  // stage 0 at offset 0: K tile, then V tile
   a.off_stage1 = off;
-  off += 2 * a.tile;
+  if (!wide) off += 2 * a.tile;
   a.off_rec = off;
   off += (rec_bytes + 127) / 128 * 128;
   a.off_ksc = off;
@@ -241,18 +247,19 @@ __device__ __forceinline__ void quant8(const uint4& xv, const uint64_t (&mn2)[4]
 // Quantizes one staged group (rows of the stage are the group's G tokens; a
 // row that came from the ring has its 16-byte chunks swizzled by t & 7) into
 // the record staging area.  Thread (chunk c, row group rg) owns chunk c of
-// rows rg + k*RG, k < D/32, and keeps them in registers from the min/max pass
-// to the code pass.
-template <int KB, int VB, int D>
+// rows rg + k*RG, k < RT, and keeps them in registers from the min/max pass
+// to the code pass.  after_load() runs once every thread holds its rows (the
+// stage may then be refilled: with 2- to 8-bit codes nothing reads it again).
+template <int KB, int VB, int D, bool kWide, typename AfterLoad>
 __device__ bool flush_group(const AppendParams& p, const __half* kt, const __half* vt, int nring, uint8_t* smem,
-                            const AppendSmem& L, bool staged) {
+                            const AppendSmem& L, bool staged, AfterLoad&& after_load) {
   constexpr int WK = words_per_row(D, KB);
   constexpr int WV = words_per_row(D, VB);
   constexpr int CH = D / 8;     // 16-byte chunks per row
-  constexpr int RT = D / 32;    // rows per thread
+  constexpr int RT = kWide ? D / 16 : D / 32;  // rows per thread
   constexpr int LPC = 32 / CH;  // lanes of a warp on the same chunk
   const int G = p.G;
-  const int RG = 4 * G / CH;    // row groups
+  const int RG = (kWide ? 2 : 4) * G / CH;     // row groups
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = tid % CH, rg = tid / CH;
   uint8_t* rec = smem + L.off_rec;
@@ -346,6 +353,7 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
   if (tid == 0) bulk_wait_read_all();  // the previous record has left the staging area
   // every thread saw its stage arrive, or all of them stop here
   if (__syncthreads_or(!staged)) return false;
+  after_load();
 
   // ---- phase 2: one scale per thread (channel tid, token tid; per-token
   // keys: token tid - G)
@@ -360,7 +368,7 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
   } else if (tid < D) {
     // thread tid takes channel 8*(tid % CH) + tid / CH, whose table slot is tid
     const int ch = 8 * (tid % CH) + tid / CH;
-    const int warps = 4 * G / 32;
+    const int warps = (kWide ? 2 : 4) * G / 32;
     __half mn = kmn[ch], mx = kmx[ch];
     for (int w = 1; w < warps; ++w) {
       mn = __hmin(mn, kmn[w * D + ch]);
@@ -378,8 +386,11 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
     ks16[pos] = sc.s16;
     kz16[pos] = sc.z16;
   }
-  if (tid < G) {
-    const __half2 r = vpart[tid];
+  // value scales: token vtk (wide CTAs with G >= D: the threads after the D
+  // channel ones)
+  const int vtk = (kWide && !ktok && G >= D) ? tid - D : tid;
+  if (vtk >= 0 && vtk < G) {
+    const __half2 r = vpart[vtk];
     const __half mn = __low2half(r), mx = __hneg(__high2half(r));
     const Scale s3 = make_scale<VB>(mn, mx, false);
     float s2 = s3.s, r2 = s3.r;
@@ -388,9 +399,9 @@ __device__ bool flush_group(const AppendParams& p, const __half* kt, const __hal
       s2 = t2.s;
       r2 = t2.r;
     }
-    vsc[tid] = make_float4(s3.mn, s3.s, s3.r, s2);
-    vr2[tid] = r2;
-    vsz[tid] = __halves2half2(s3.s16, s3.z16);
+    vsc[vtk] = make_float4(s3.mn, s3.s, s3.r, s2);
+    vr2[vtk] = r2;
+    vsz[vtk] = __halves2half2(s3.s16, s3.z16);
   }
   __syncthreads();
 
@@ -542,7 +553,7 @@ __device__ void write_residual(const AppendParams& p, int u, int64_t lo, int64_t
 template <int KB, int VB>
 __host__ __device__ constexpr int append_min_ctas_128() { return (KB == 8 || VB == 8) ? 4 : 5; }
 
-template <int KB, int VB, int D, int TPB, int MINB>
+template <int KB, int VB, int D, int TPB, int MINB, bool kWide>
 __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -588,7 +599,7 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
     // jobs: a single-token append's CTA quantizes its unit's groups nq0/G ..
     // nq1/G - 1 in order; a multi-token append's job j is (unit j / nflush,
     // group nq0/G + j % nflush), CTA-strided.  job(k) is this CTA's k-th job.
-    const AppendSmem L = append_smem_layout(D, p.G, p.rec_bytes);
+    const AppendSmem L = append_smem_layout(D, p.G, p.rec_bytes, kWide);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
     const int nflush = (nq1 - nq0) / p.G;
     const int njobs = per_unit ? nflush : nflush * p.units;
@@ -646,21 +657,26 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
       mbar_init(&bars[1], 1);
       fence_mbar_init();
       if (job_valid(0)) issue(0, 0);
-      if (job_valid(1)) issue(1, 1);
+      if (!kWide && job_valid(1)) issue(1, 1);
     }
     __syncthreads();
     for (int k = 0; job_valid(k); ++k) {
-      const int st = k & 1;
+      // two stages alternate; a wide CTA's single stage completes once per job
+      const int st = kWide ? 0 : (k & 1);
+      const uint32_t parity = static_cast<uint32_t>(kWide ? (k & 1) : ((k >> 1) & 1));
       int u, grp;
       job_of(k, u, grp);
       const int t0 = grp * p.G;
       const int nring = T > t0 ? (T - t0 < p.G ? T - t0 : p.G) : 0;
-      const bool ok = mbar_wait(&bars[st], static_cast<uint32_t>((k >> 1) & 1), p.err);
+      const bool ok = mbar_wait(&bars[st], parity, p.err);
       const __half* kt = reinterpret_cast<const __half*>(smem + st * L.off_stage1);
-      if (!flush_group<KB, VB, D>(p, kt, kt + p.G * D, nring, smem, L, ok)) {
+      auto refill = [&]() {
+        if (kWide && tid == 0 && job_valid(k + 1)) issue(k + 1, 0);
+      };
+      if (!flush_group<KB, VB, D, kWide>(p, kt, kt + p.G * D, nring, smem, L, ok, refill)) {
         // a copy never landed (all threads agree): give the other stage's copy
-        // its bounded wait, then stop
-        if (job_valid(k + 1)) mbar_wait(&bars[st ^ 1], static_cast<uint32_t>(((k + 1) >> 1) & 1), p.err);
+        // its bounded wait, then stop (a wide CTA has issued no other copy)
+        if (!kWide && job_valid(k + 1)) mbar_wait(&bars[st ^ 1], static_cast<uint32_t>(((k + 1) >> 1) & 1), p.err);
         break;
       }
       __syncthreads();  // stage and record staging complete
@@ -670,7 +686,7 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
         if (in_range(dst, static_cast<size_t>(p.rec_bytes), p.buf_lo, p.buf_hi, p.err))  // debug builds
           bulk_s2g(dst, smem + L.off_rec, static_cast<uint32_t>(p.rec_bytes));
         bulk_commit();
-        if (job_valid(k + 2)) issue(k + 2, st);
+        if (!kWide && job_valid(k + 2)) issue(k + 2, st);
       }
     }
     if (tid == 0) bulk_wait_all();
@@ -722,10 +738,21 @@ __global__ void __launch_bounds__(TPB, MINB) append_kernel(AppendParams p) {
 
 }  // namespace
 
+// The instantiation for a launch of `threads` threads: wide G = 128 flushes
+// (256 threads, two CTAs per SM), 128-thread flushes (G = 32) and window
+// writes, or the 512-thread bound for the other G = 64 and 128 flushes.
+template <int KB, int VB, int D>
+static void (*append_kernel_for(int threads, int G))(AppendParams) {
+  if constexpr (append_wide(KB, VB, 128)) {
+    if (G == 128 && threads == append_threads(128, true)) return append_kernel<KB, VB, D, 256, 2, true>;
+  }
+  if (threads <= 128) return append_kernel<KB, VB, D, 128, append_min_ctas_128<KB, VB>(), false>;
+  return append_kernel<KB, VB, D, 512, 1, false>;
+}
+
 template <int KB, int VB, int D>
 static cudaError_t launch_append(const AppendParams& p, dim3 grid, int threads, size_t smem, cudaStream_t s) {
-  auto k = threads <= 128 ? append_kernel<KB, VB, D, 128, append_min_ctas_128<KB, VB>()>
-                          : append_kernel<KB, VB, D, 512, 1>;
+  auto k = append_kernel_for<KB, VB, D>(threads, p.G);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -735,9 +762,8 @@ static cudaError_t launch_append(const AppendParams& p, dim3 grid, int threads, 
 }
 
 template <int KB, int VB, int D>
-static int occupancy_append(int threads, size_t smem) {
-  auto k = threads <= 128 ? append_kernel<KB, VB, D, 128, append_min_ctas_128<KB, VB>()>
-                          : append_kernel<KB, VB, D, 512, 1>;
+static int occupancy_append(int threads, int G, size_t smem) {
+  auto k = append_kernel_for<KB, VB, D>(threads, G);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return 0;
   int occ = 0;
@@ -765,9 +791,9 @@ cudaError_t append_dispatch(int kb, int vb, int D, const AppendParams& p, dim3 g
 
 #define KVQ_APPEND_OCC(KB, VB) \
   case (KB * 16 + VB):        \
-    return D == 128 ? occupancy_append<KB, VB, 128>(threads, smem) : occupancy_append<KB, VB, 64>(threads, smem);
+    return D == 128 ? occupancy_append<KB, VB, 128>(threads, G, smem) : occupancy_append<KB, VB, 64>(threads, G, smem);
 
-int append_ctas_per_sm(int kb, int vb, int D, int threads, size_t smem) {
+int append_ctas_per_sm(int kb, int vb, int D, int G, int threads, size_t smem) {
   switch (kb * 16 + vb) {
     KVQ_APPEND_OCC(2, 2) KVQ_APPEND_OCC(2, 3) KVQ_APPEND_OCC(2, 4) KVQ_APPEND_OCC(2, 8)
     KVQ_APPEND_OCC(3, 2) KVQ_APPEND_OCC(3, 3) KVQ_APPEND_OCC(3, 4) KVQ_APPEND_OCC(3, 8)
@@ -779,12 +805,10 @@ int append_ctas_per_sm(int kb, int vb, int D, int threads, size_t smem) {
 }
 #undef KVQ_APPEND_OCC
 
-int append_block_threads(int G) { return append_threads(G); }
+int append_block_threads(int kb, int vb, int G) { return append_threads(G, append_wide(kb, vb, G)); }
 
 size_t append_smem_bytes(int kb, int vb, int D, int G, int rec_bytes) {
-  (void)kb;
-  (void)vb;
-  return static_cast<size_t>(append_smem_layout(D, G, rec_bytes).total);
+  return static_cast<size_t>(append_smem_layout(D, G, rec_bytes, append_wide(kb, vb, G)).total);
 }
 
 }  // namespace kvq

@@ -12,9 +12,9 @@ cudaError_t append_dispatch(int kb, int vb, int D, const AppendParams& p, dim3 g
                             cudaStream_t s);
 size_t append_smem_bytes(int kb, int vb, int D, int G, int rec_bytes);
 // Threads of a CTA that quantizes key groups of G tokens.
-int append_block_threads(int G);
+int append_block_threads(int kb, int vb, int G);
 // CTAs of the append kernel resident per SM at that block and shared-memory size (0 on error).
-int append_ctas_per_sm(int kb, int vb, int D, int threads, size_t smem);
+int append_ctas_per_sm(int kb, int vb, int D, int G, int threads, size_t smem);
 
 // Decode attention, specialised on (k_bits, v_bits, head_dim, n-tiles).
 typedef void (*decode_kernel_t)(DecodeParams);
