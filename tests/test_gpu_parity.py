@@ -96,6 +96,17 @@ def test_eight_head_tiles_group_128(kb, vb, gqa):
     _run_stream(kb, vb, 128, 128, 128, gqa, [3 * 128 + 5] + [1] * 130, attn_every=9, seed=kb * 16 + vb + gqa)
 
 
+@pytest.mark.parametrize("kb,vb,D,key_mode", [(4, 2, 64, 0), (8, 8, 64, 0), (2, 4, 64, 0), (8, 4, 64, 1),
+                                              (3, 4, 128, 0), (4, 3, 64, 0)])
+def test_append_group_128_cta_forms(kb, vb, D, key_mode):
+    # G = 128 flushes run 256-thread single-stage CTAs without 3-bit codes and
+    # 512-thread double-stage CTAs with them: head_dim 64 for the first form
+    # (value scales on the threads after the 64 channel ones), 3-bit pairs for
+    # the second; a ragged prefill, then decode steps through a flush
+    _run_stream(kb, vb, D, 128, 128, 4, [3 * 128 + 5] + [1] * 130, attn_every=13, seed=kb * 16 + vb + D,
+                key_mode=key_mode)
+
+
 @pytest.mark.parametrize("gqa", [1, 2, 3, 4, 5, 7, 8])
 def test_gqa_ratios(gqa):
     _run_stream(4, 2, 128, 32, 32, gqa, [96 + 17] + [1] * 20, attn_every=4, seed=gqa)
