@@ -447,23 +447,33 @@ __global__ void __launch_bounds__(kChunkCtaThreads, 1) chunk_attn_kernel(ChunkPa
         if (bad) break;
         tc_fence_after_sync();
         const uint32_t kb_h = sst + bs * T::bytes, kb_l = kb_h + T::kl;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          // the group's rows have read S(it-2), the buffer's previous scores
-          if (it >= 2) bad = bad || !mbar_wait(s_free + 2 * bs + g, ((it - 2) >> 1) & 1, p.err);
-          if (bad) break;
-          tc_fence_after_sync();
-          const uint32_t qg = sq + g * (kChunkM * D * 2);
-          const uint32_t dS = tb + kTile * (2 * bs + g);
-          const uint64_t dq = smem_desc(qg, 128, KC * 128);
-          const uint64_t dkh = smem_desc(kb_h, 128, KC * 128), dkl = smem_desc(kb_l, 128, KC * 128);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) umma_f16(dS, dq + 16 * ks, dkh + 16 * ks, idS, ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) umma_f16(dS, dq + 16 * ks, dkl + 16 * ks, idS, 1u);
-          umma_commit(s_done + 2 * bs + g);
+        // both groups' rows have read S(it-2), the buffer's previous scores
+        if (it >= 2) {
+          bad = !mbar_wait(s_free + 2 * bs, ((it - 2) >> 1) & 1, p.err);
+          bad = bad || !mbar_wait(s_free + 2 * bs + 1, ((it - 2) >> 1) & 1, p.err);
         }
         if (bad) break;
+        tc_fence_after_sync();
+        {
+          // the two groups' accumulation chains alternate: an MMA whose
+          // accumulator the previous MMA writes waits for it, one into the
+          // other group's columns need not
+          const uint32_t dS0 = tb + kTile * (2 * bs), dS1 = dS0 + kTile;
+          const uint64_t dq0 = smem_desc(sq, 128, KC * 128), dq1 = smem_desc(sq + kChunkM * D * 2, 128, KC * 128);
+          const uint64_t dkh = smem_desc(kb_h, 128, KC * 128), dkl = smem_desc(kb_l, 128, KC * 128);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            umma_f16(dS0, dq0 + 16 * ks, dkh + 16 * ks, idS, ks > 0);
+            umma_f16(dS1, dq1 + 16 * ks, dkh + 16 * ks, idS, ks > 0);
+          }
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            umma_f16(dS0, dq0 + 16 * ks, dkl + 16 * ks, idS, 1u);
+            umma_f16(dS1, dq1 + 16 * ks, dkl + 16 * ks, idS, 1u);
+          }
+          umma_commit(s_done + 2 * bs);
+          umma_commit(s_done + 2 * bs + 1);
+        }
         umma_commit(kfree + bs);
         // keys of tile it+1 into the other stage (its scores of tile it-1 are long done)
         if (it + 1 < ntiles) {
