@@ -58,7 +58,7 @@ typedef enum {
   KVQ_ERR_CAPACITY = 4, /* appending past max_tokens, or buffer too small    */
   KVQ_ERR_CUDA = 5,     /* a CUDA runtime call failed                        */
   KVQ_ERR_STATE = 6,    /* call not valid now (e.g. attention on empty layer)*/
-  KVQ_ERR_UNSUPPORTED = 7 /* a shape this build has no kernel for          */
+  KVQ_ERR_UNSUPPORTED = 7 /* a shape the library has no kernel for        */
 } kvq_status;
 
 /* Key quantization mode of a layer (KVTuner sections A3-A4 evaluate both):
